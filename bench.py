@@ -1,0 +1,333 @@
+"""Benchmark: one paged GQA decode step (workqueue + split-KV decode + LSE
+merge) on the batch-8 bimodal fp16 workload (Hq=32, Hkv=8, d=128, page 16,
+lengths half U[512, 2048] and half U[16384, 32768], pages scattered in a pool
+of 1.25x the pages used), measured as KV HBM GB/s and tokens/s.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--workload bimodal|uniform|zipf|bucket32k|bucket64k|bucket128k|tiny]
+
+Prints one JSON line.  `value` is algorithmic bytes (valid K/V tokens + q +
+block-table entries) per step / device time per step, with inputs resident in
+HBM and L2 flushed between steps (a 512 MiB memset, outside the timed
+events).  `e2e` times the host-buffer entry point (q, block table and
+lengths copied in, out and lse copied back, per step).  `roofline` reports
+the attention kernel alone (events bracket it inside the call) against the
+measured HBM copy bandwidth.  `cpu_baseline` times the CPU oracle on a
+bounded sample of the same workload.  With --impl reference the CPU oracle is
+the measured arm.  Under torchrun (N > 1) every rank runs an independent
+replica (the step does not shard), the max time over ranks is reported and
+`value` sums all ranks' bytes.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from paged_kv_cache_492_b300 import workloads as W  # noqa: E402
+
+WORKLOADS = {
+    "bimodal": W.bimodal,
+    "uniform": W.uniform_lengths,
+    "zipf": W.zipf_lengths,
+    "bucket32k": lambda: W.bucketed_long(32768),
+    "bucket64k": lambda: W.bucketed_long(65536),
+    "bucket128k": lambda: W.bucketed_long(131072),
+    "tiny": lambda: W.tiny()["decode"],
+}
+METRIC = "paged GQA decode attention: KV HBM GB/s (% of B300 peak), tokens/s"
+
+
+def measured_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            j = json.load(f)
+        return float(j["hbm_gbs"]), "measured"
+    return 6400.0, "fallback"
+
+
+def workload_config(x: W.DecodeInputs, name: str):
+    return {"workload": name, "batch": x.B, "Hq": x.Hq, "Hkv": x.Hkv, "d": x.d,
+            "page_size": x.page_size, "dtype": W.DTYPE_NAMES[x.dtype],
+            "seq_lens": [int(v) for v in x.seq_lens], "num_pages": x.num_pages,
+            "kv_bytes_per_step": x.kv_bytes(), "algorithmic_bytes_per_step": x.algorithmic_bytes(),
+            "l2": "flushed between steps (512 MiB memset outside the timed events)",
+            "parallelism": "replicas (one independent decode per GPU)"}
+
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clocks and throttle reasons during the timed region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.f = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"], stdout=self.f,
+                stderr=subprocess.DEVNULL)
+        except FileNotFoundError:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+        return False
+
+    def summary(self):
+        self.f.flush()
+        self.f.seek(0)
+        rows = [r.split(",") for r in self.f.read().strip().splitlines() if r.strip()]
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            try:
+                sm.append(float(r[1]))
+                mx.append(float(r[2]))
+                for n, v in zip(names, r[5:9]):
+                    if v.strip().lower() == "active":
+                        reasons.add(n)
+            except (ValueError, IndexError):
+                continue
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def oracle_sample(x: W.DecodeInputs, heads: int = 2):
+    """A bounded sample of the workload for the CPU oracle: every sequence,
+    the first `heads` KV heads (with their query heads)."""
+    G = x.Hq // x.Hkv
+    y = W.DecodeInputs(name=x.name + "_sample", B=x.B, Hq=heads * G, Hkv=heads, d=x.d,
+                       page_size=x.page_size, dtype=x.dtype, scale=x.scale,
+                       q=np.ascontiguousarray(x.q[:, : heads * G]),
+                       k_pool=np.ascontiguousarray(x.k_pool[:, :heads]),
+                       v_pool=np.ascontiguousarray(x.v_pool[:, :heads]),
+                       block_table=x.block_table, seq_lens=x.seq_lens)
+    return y
+
+
+def time_oracle(x: W.DecodeInputs, steps: int, warmup: int):
+    from oracle import oracle as O
+
+    cores = len(os.sched_getaffinity(0))
+    y = oracle_sample(x)
+    O.decode(y, nthreads=cores)  # build + page in
+    for _ in range(max(0, warmup - 1)):
+        pass
+    t = []
+    for _ in range(steps):
+        t0 = time.perf_counter()
+        O.decode(y, nthreads=cores)
+        t.append(time.perf_counter() - t0)
+    sec = statistics.median(t)
+    return {"value": y.algorithmic_bytes() / sec / 1e9, "unit": "GB/s", "cores": cores,
+            "kind": "oracle",
+            "tokens_per_s": x.B / sec * (y.Hkv / x.Hkv),
+            "sample": f"all {x.B} sequences, KV heads 0..{y.Hkv - 1} of {x.Hkv} "
+                      f"({y.algorithmic_bytes() / 1e6:.1f} MB of K/V+q+table per step), "
+                      f"fp64 C oracle, {steps} timed step(s), median {sec:.2f} s"}
+
+
+def run_reference(args, x, name, rank, world):
+    if rank != 0:
+        return
+    cpu = time_oracle(x, max(1, args.steps), args.warmup)
+    line = {"impl": "reference", "metric": METRIC, "value": cpu["value"], "unit": "GB/s",
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": None, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": workload_config(x, name),
+            "cpu_baseline": cpu,
+            "e2e": {"value": cpu["value"], "unit": "GB/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def run_ours(args, x, name, rank, world):
+    import torch
+    import torch.distributed as dist
+
+    from paged_kv_cache_492_b300 import kv
+
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
+    torch.cuda.set_device(dev)
+    stream = torch.cuda.current_stream()
+
+    def dev_bits(a):
+        return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).to(dev).view(
+            torch.float16 if x.dtype == W.F16 else torch.bfloat16)
+
+    q = dev_bits(x.q)
+    k = dev_bits(x.k_pool)
+    v = dev_bits(x.v_pool)
+    table = torch.from_numpy(x.block_table).to(dev)
+    lens = torch.from_numpy(x.seq_lens).to(dev)
+    out = torch.empty((x.B, x.Hq, x.d), dtype=torch.float32, device=dev)
+    lse = torch.empty((x.B, x.Hq), dtype=torch.float32, device=dev)
+    ws = kv.alloc_workspace(kv.kv_decode_hostio_workspace_size(x.B, x.Hq, x.Hkv, x.d, x.max_pages),
+                            device=dev)
+    flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
+
+    # host-side copies for the end-to-end (host buffers) leg
+    hq = torch.from_numpy(x.q.view(np.int16).copy()).view(q.dtype).pin_memory()
+    ht = torch.from_numpy(x.block_table.copy()).pin_memory()
+    hl = torch.from_numpy(x.seq_lens.copy()).pin_memory()
+    ho = torch.empty((x.B, x.Hq, x.d), dtype=torch.float32).pin_memory()
+    hls = torch.empty((x.B, x.Hq), dtype=torch.float32).pin_memory()
+
+    def step():
+        kv.kv_decode(q, k, v, table, lens, x.scale, out, lse, ws)
+
+    for _ in range(max(3, args.warmup)):
+        step()
+    torch.cuda.synchronize()
+    if kv.kv_get_status(ws) != 0:
+        raise SystemExit("device error during warm-up")
+
+    n = args.steps
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(n)]
+    evk = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(n)]
+    for a, b in evk:  # materialise the events before handing them to the library
+        a.record(stream)
+        b.record(stream)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(dev.index if dev.index is not None else 0) as clk:
+        t_wall0 = time.perf_counter()
+        for i in range(n):
+            flush.zero_()
+            ev[i][0].record(stream)
+            kv.kv_profile_next_decode(evk[i][0], evk[i][1])
+            step()
+            ev[i][1].record(stream)
+        torch.cuda.synchronize()
+        t_wall = time.perf_counter() - t_wall0
+        if world > 1:
+            dist.barrier()
+        torch.cuda.synchronize()
+        # end-to-end through the host-buffer entry point
+        e2e_t = []
+        for i in range(max(3, n // 2)):
+            flush.zero_()
+            torch.cuda.synchronize()
+            t0 = time.perf_counter()
+            kv.kv_decode_hostio(hq, k, v, ht, hl, x.scale, ho, hls, ws)
+            torch.cuda.synchronize()
+            e2e_t.append(time.perf_counter() - t0)
+    clocks = clk.summary()
+    if kv.kv_get_status(ws) != 0:
+        raise SystemExit("device error during the timed region")
+    step_ms = [a.elapsed_time(b) for a, b in ev]
+    kern_ms = [a.elapsed_time(b) for a, b in evk]
+    t_step = sum(step_ms) / n / 1e3
+    t_kern = sum(kern_ms) / n / 1e3
+    t_e2e = statistics.median(e2e_t)
+    if world > 1:
+        tt = torch.tensor([t_step, t_e2e, t_kern], device=dev, dtype=torch.float64)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        t_step, t_e2e, t_kern = tt.tolist()
+    if rank != 0:
+        return
+    nbytes = x.algorithmic_bytes()
+    peak, peak_kind = measured_peaks()
+    value = world * nbytes / t_step / 1e9
+    achieved = nbytes / t_kern / 1e9
+    traffic = None
+    prof = os.path.join(ROOT, "profiles", f"decode_{name}_traffic.json")
+    if os.path.exists(prof):
+        with open(prof) as f:
+            tj = json.load(f)
+        if tj.get("kernel_source_hash") == kernel_hash():
+            traffic = tj.get("dram_bytes_per_launch")
+    h2d = x.q.nbytes + x.block_table.nbytes + x.seq_lens.nbytes
+    d2h = x.B * x.Hq * x.d * 4 + x.B * x.Hq * 4
+    line = {
+        "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": n,
+        "warmup": args.warmup, "ms_per_step": t_step * 1e3, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": W.DTYPE_NAMES[x.dtype],
+        "data": "synthetic", "config": workload_config(x, name),
+        "tokens_per_s": world * x.B / t_step, "kv_tokens_per_s": world * float(x.seq_lens.sum()) / t_step,
+        "pct_of_peak": 100.0 * (nbytes / t_step / 1e9) / peak,
+        "wall_ms_per_step_incl_flush": t_wall / n * 1e3,
+        "e2e": {"value": world * nbytes / t_e2e / 1e9, "unit": "GB/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "ms_per_step": t_e2e * 1e3,
+                "entry": "kv_decode_hostio (pinned host q/table/lens in, out/lse out)"},
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                     "frac": achieved / peak, "traffic": traffic,
+                     "kernel": "decode_kernel<128,4,F16>" if x.dtype == W.F16 else "decode_kernel<128,4,BF16>",
+                     "kernel_ms": t_kern * 1e3, "peak_source": f"MEASURED_PEAKS.json hbm_gbs ({peak_kind})"},
+        "gpu_launches": 3 * n,
+        "clocks": clocks,
+    }
+    if not args.no_cpu_baseline:
+        line["cpu_baseline"] = time_oracle(x, 1, 0)
+    print(json.dumps(line), flush=True)
+
+
+def kernel_hash():
+    import hashlib
+
+    h = hashlib.sha256()
+    for f in ("kv_decode.cu", "kv_common.cuh"):
+        with open(os.path.join(ROOT, "paged_kv_cache_492_b300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=30)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="bimodal", choices=list(WORKLOADS))
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if world > 1 and args.impl == "ours":
+        import torch.distributed as dist
+
+        dist.init_process_group("nccl")
+    x = WORKLOADS[args.workload]()
+    if args.impl == "reference":
+        run_reference(args, x, args.workload, rank, world)
+    else:
+        run_ours(args, x, args.workload, rank, world)
+    if world > 1 and args.impl == "ours":
+        import torch.distributed as dist
+
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

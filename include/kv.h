@@ -1,0 +1,261 @@
+/*
+ * kv.h -- C ABI of the B300 (sm_103a) paged KV-cache library: one decode step
+ * of grouped-query attention over a block-table KV cache, and the page
+ * budgeting step (query summaries, page scoring, top-k retention,
+ * compress-or-grow, compaction, append).
+ *
+ * Sources for what each call computes:
+ *  [PKV] aissential.tech, "PersistentKV: Page-Aware Decode Scheduling for
+ *        Long-Context LLM Serving on Commodity GPUs" -- Summary, Method:
+ *        native block-table decode attention for GQA that reuses each K/V
+ *        tile across the grouped query heads and runs a compact workqueue of
+ *        non-empty (sequence, KV-head, split) tasks.
+ *  [GP]  mlsanity.com, "GrowPage: On-Demand KV Budgeting for Efficient LLM
+ *        Reasoning Serving" -- Abstract; aitrending.vip GrowPage summary --
+ *        Technical Details: dual-timescale query summaries, relative attention
+ *        working sets, compress-or-grow at every capacity boundary, on top of
+ *        PagedAttention's page abstraction.
+ *  [EKV] paperlayer.ai, "Elastic KV Cache for LLM Serving" -- section 2:
+ *        fixed-size KV blocks handed out from an integer free list.
+ *
+ * Conventions shared by every call
+ *  - Pointers marked (device) are device memory owned by the caller; (host)
+ *    pointers are host memory (pinned for asynchronous copies).  The library
+ *    never allocates memory and never keeps a pointer past the call.
+ *  - `stream` is a cudaStream_t (NULL = legacy default stream).  Calls only
+ *    enqueue work and return; none synchronises except kv_get_status.
+ *  - Return value: KV_OK, or a negative KV_E* code for an argument rejected
+ *    on the host (nothing was enqueued).  Errors found on the device (a bad
+ *    page id, an exhausted free list, ...) are recorded in the status word of
+ *    the workspace `ws` and read back with kv_get_status; the kernels never
+ *    trap and never read or write outside the buffers described here.
+ *  - 16-bit element types: dtype KV_F16 (IEEE binary16) or KV_BF16.
+ *    Floating outputs are fp32.
+ *  - Layouts (row-major):
+ *      q            [B][Hq][d]                    16-bit
+ *      k_pool/v_pool [num_pages][Hkv][page_size][d] 16-bit (page-major, then
+ *                   KV head: one (page, head) tile is page_size*d contiguous
+ *                   elements, all heads of a page are contiguous)
+ *      block_table  [B][max_pages] int32: logical page j of sequence b lives
+ *                   in pool page block_table[b][j]; entries at j >= ceil(L_b /
+ *                   page_size) are never read (-1 padding is customary)
+ *      seq_lens     [B] int32, tokens held by each sequence (L_b >= 0)
+ *    Query head hq attends with KV head hq / (Hq / Hkv) (contiguous groups).
+ *  - Supported shapes: page_size 16; d in {64, 128}; Hq / Hkv in {1, 2, 4, 8};
+ *    Hkv <= 8.  Others return KV_EINVAL.
+ *  - Workspace: `ws` is caller-allocated device memory of at least the size
+ *    the matching *_workspace_size function returns, 256-byte aligned.  Its
+ *    first 256 bytes hold the status word.  One workspace may serve several
+ *    calls that run in order on one stream; calls that overlap on the device
+ *    must not share one.  Zero it once before first use (kv_workspace_reset).
+ */
+#ifndef PAGED_KV_B300_KV_H
+#define PAGED_KV_B300_KV_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define KV_OK 0
+#define KV_EINVAL (-1)     /* bad argument (host) or bad length (device) */
+#define KV_EBADPAGE (-2)   /* a page id in use is < 0 or >= num_pages */
+#define KV_ENOSPACE (-3)   /* free list holds fewer pages than needed */
+#define KV_EWORKSPACE (-4) /* workspace too small for the work found */
+#define KV_ECUDA (-5)      /* a CUDA runtime call failed */
+#define KV_EFULL (-6)      /* a block-table row has no room for a new page */
+#define KV_ETIMEOUT (-7)   /* a kernel's bounded wait gave up (never expected) */
+
+#define KV_F16 0
+#define KV_BF16 1
+
+/* Text for a status code (static storage). */
+const char *kv_status_string(int code);
+
+/* Bytes of the workspace header (the status word); the minimum workspace. */
+size_t kv_status_workspace_size(void);
+
+/* Zero the workspace header (status word) on `stream`. */
+int kv_workspace_reset(void *ws, void *stream);
+
+/* Synchronise `stream`, return the first device-side error recorded in `ws`
+ * since the last call (KV_OK if none) and clear it. */
+int kv_get_status(void *ws, void *stream);
+
+/* ------------------------------------------------------------------------ */
+/* Decode [PKV].                                                              */
+/* ------------------------------------------------------------------------ */
+
+/* Number of decode workers (resident CTAs, one per split-chunk at a time) on
+ * the current device for this shape; the automatic split size spreads the
+ * batch's pages evenly over them. */
+int kv_decode_num_workers(int Hq, int Hkv, int d, int page_size, int dtype);
+
+/* Workspace bytes kv_decode needs for a batch of B sequences whose tables are
+ * max_pages wide.  pages_per_split as passed to kv_decode (0 = automatic). */
+size_t kv_decode_workspace_size(int B, int Hq, int Hkv, int d, int max_pages, int page_size,
+                                int pages_per_split);
+
+/* One decode step.  For every sequence b and query head hq (h = hq / G):
+ *   s_t   = scale * <q[b][hq], k_t>      over tokens t < L_b of the paged cache
+ *   lse   = ln sum_t exp(s_t)            (natural log, scale included)
+ *   out   = sum_t exp(s_t - lse) v_t
+ * out [B][Hq][d] fp32 (device), lse [B][Hq] fp32 (device).  L_b = 0 gives
+ * out = 0 and lse = -inf.
+ * Work split: the non-empty pages of the batch, laid end to end, are cut into
+ * chunks of `pages_per_split` pages (0 = automatic: ceil(W / workers), at
+ * least 8, W = total pages); each (sequence, chunk) overlap is one split, and
+ * each split is one task per KV head.  A task streams each (page, KV head)
+ * tile once from HBM and reuses it for all G = Hq/Hkv query heads; splits of
+ * one sequence are recombined by a log-sum-exp merge.
+ * Device errors: KV_EBADPAGE (an entry in [0, ceil(L_b/16)) outside
+ * [0, num_pages); page 0 is read in its place), KV_EINVAL (L_b < 0 or more
+ * pages than max_pages), KV_EWORKSPACE, KV_ETIMEOUT. */
+int kv_decode(const void *q, const void *k_pool, const void *v_pool, int num_pages,
+              const int32_t *block_table, int max_pages, const int32_t *seq_lens, int B,
+              int page_size, int Hq, int Hkv, int d, int dtype, float scale,
+              int pages_per_split, float *out, float *lse, void *ws, size_t ws_bytes,
+              void *stream);
+
+/* Profiling aid: the next kv_decode (or kv_decode_hostio) issued from the
+ * calling host thread records `event_before` (a cudaEvent_t) on its stream
+ * just before the attention kernel and `event_after` just after it, so the
+ * kernel's own duration can be timed with CUDA events.  One-shot; NULL
+ * events disarm it. */
+int kv_profile_next_decode(void *event_before, void *event_after);
+
+/* Workspace bytes for kv_decode_hostio: kv_decode's plus staging for q, the
+ * block table, seq_lens, out and lse. */
+size_t kv_decode_hostio_workspace_size(int B, int Hq, int Hkv, int d, int max_pages,
+                                       int page_size, int pages_per_split);
+
+/* kv_decode with the per-step inputs and outputs in host memory: copies
+ * h_q, h_block_table, h_seq_lens (host) into the workspace, runs kv_decode
+ * against the device-resident pools, and copies out/lse back into h_out and
+ * h_lse (host), all enqueued on `stream` (one cudaMemcpyAsync per buffer).
+ * The host buffers must stay valid until the stream reaches that point. */
+int kv_decode_hostio(const void *h_q, const void *k_pool, const void *v_pool, int num_pages,
+                     const int32_t *h_block_table, int max_pages, const int32_t *h_seq_lens,
+                     int B, int page_size, int Hq, int Hkv, int d, int dtype, float scale,
+                     int pages_per_split, float *h_out, float *h_lse, void *ws, size_t ws_bytes,
+                     void *stream);
+
+/* The decode workqueue on its own (for inspection and tests).  With
+ * chunk = pages_per_split (> 0) or the automatic size for n_workers workers
+ * (pages_per_split = 0): writes, in (b, split, h) order, one 8 x int32 record
+ * per task: b, h, split, nsplit_b, page_begin, page_end (pages of b), chunk
+ * index, L_b.  chunk_begin [nchunks + 1]: first (b, split) group of each
+ * chunk.  seq_group_begin [B], seq_nsplit [B].  meta [5] int32: tasks,
+ * groups, chunk, nchunks, W.  Capacities max_tasks / max_chunks (entries);
+ * overflow -> KV_EWORKSPACE in the status word.  All arrays (device); `ws`
+ * of kv_workqueue_workspace_size(B) bytes holds the status word and scratch. */
+size_t kv_workqueue_workspace_size(int B);
+int kv_build_workqueue(const int32_t *seq_lens, int B, int Hkv, int page_size, int max_pages,
+                       int pages_per_split, int n_workers, int32_t *tasks, int max_tasks,
+                       int32_t *chunk_begin, int max_chunks, int32_t *seq_group_begin,
+                       int32_t *seq_nsplit, int32_t *meta, void *ws, void *stream);
+
+/* ------------------------------------------------------------------------ */
+/* Page budgeting [GP].  Build's instantiation of the summaries the pages     */
+/* describe without a formula (every value that decides an integer is fp32    */
+/* with the operation order stated, so results are reproducible bit for bit):*/
+/*   query summaries: per KV head the group-mean query g (sum over the G      */
+/*     query heads in ascending order, then / G), and two EMAs               */
+/*     ema = (a * ema) + ((1 - a) * g), a = a_fast or a_slow;                */
+/*   page key summaries: per (page, KV head, channel) mean (sum of the 16    */
+/*     slots in order, / 16), min and max;                                    */
+/*   page score S_u(j) = sum_h sum_c [u*mean + max(u*min, u*max)], summed    */
+/*     per lane l (channels l*d/32 .. +d/32, heads then channels ascending)  */
+/*     and across lanes by xor-butterfly 16, 8, 4, 2, 1.                      */
+/* ------------------------------------------------------------------------ */
+
+/* ema [B][2][Hkv][d] fp32 (device), index 0 fast, 1 slow; first != 0
+ * initialises both to g.  q [B][Hq][d] (device). */
+int kv_update_query_summaries(const void *q, int B, int Hq, int Hkv, int d, int dtype,
+                              float a_fast, float a_slow, int first, float *ema, void *stream);
+
+/* active [B] uint8 (device).  mode 0: ceil(L_b/16) > budget[b] (sequences
+ * over budget); mode 1: capacity boundary, L_b > 0, L_b % 16 == 0 and
+ * L_b / 16 >= budget[b]. */
+int kv_mark_active(const int32_t *seq_lens, const int32_t *budget, int B, int page_size, int mode,
+                   uint8_t *active, void *stream);
+
+/* summ [num_pages][Hkv][3][d] fp32 (device): for each listed pool page,
+ * mean/min/max over its 16 slots.  page_ids [n] (device). */
+int kv_page_summaries(const void *k_pool, int num_pages, const int32_t *page_ids, int n, int Hkv,
+                      int page_size, int d, int dtype, float *summ, void *ws, size_t ws_bytes,
+                      void *stream);
+
+/* Same summaries for the last page of every active sequence
+ * (block_table[b][L_b/16 - 1]), i.e. the page that has just filled. */
+int kv_summarize_last_pages(const void *k_pool, int num_pages, const int32_t *block_table,
+                            int max_pages, const int32_t *seq_lens, const uint8_t *active, int B,
+                            int Hkv, int page_size, int d, int dtype, float *summ, void *ws,
+                            size_t ws_bytes, void *stream);
+
+/* scores [B][max_pages][2] fp32 (device): S_fast, S_slow of each resident
+ * logical page of each active sequence (active NULL = all); -inf for
+ * j >= ceil(L_b/16); inactive rows untouched. */
+int kv_score_pages(const float *query_summaries, const float *page_key_summaries, int num_pages,
+                   const int32_t *block_table, int max_pages, const int32_t *seq_lens,
+                   const uint8_t *active, int B, int Hkv, int d, int page_size, float *scores,
+                   void *ws, size_t ws_bytes, void *stream);
+
+#define KV_SELECT_TOPK 0
+#define KV_SELECT_BOUNDARY 1
+
+size_t kv_select_workspace_size(int B, int max_pages);
+
+/* Top-k retention and compress-or-grow.  n = ceil(L_b/16); forced pages
+ * F = {j < n_first} U {j >= n - n_last}; candidates C = the rest; ranking by
+ * larger key first, equal keys by lower logical index; R = S_fast + S_slow.
+ * KV_SELECT_TOPK: keep = F U top_(budget[b]-|F|)(C, R) for active rows.
+ * KV_SELECT_BOUNDARY: w = ceil(ws_frac*|C|) (fp32, clipped to [1, |C|]);
+ *   drift D = |top_w(C, S_fast) \ top_w(C, S_slow)|; a row wants to grow iff
+ *   D > delta*w (fp32) or C is empty; grows are granted in ascending b while
+ *   fewer than *free_top (device) have been granted: grow[b] = 1,
+ *   budget[b] += 1, keep every page.  Otherwise keep = F U top_(n-1-|F|)(C, R).
+ * Inactive rows keep every page.  keep_mask [B][max_pages] uint8, grow [B]
+ * uint8, drift [B] int32 (may be NULL), budget [B] int32 in/out (device). */
+int kv_select_pages(const float *scores, const int32_t *seq_lens, const uint8_t *active,
+                    int32_t *budget, int B, int max_pages, int page_size, int n_first, int n_last,
+                    float delta, float ws_frac, int mode, const int32_t *free_top,
+                    uint8_t *keep_mask, uint8_t *grow, int32_t *drift, void *ws, size_t ws_bytes,
+                    void *stream);
+
+size_t kv_compact_workspace_size(int B, int max_pages, int page_size, int token_granular);
+
+/* Stable compaction [GP] with the free list of [EKV]: the kept tokens of
+ * each sequence (keep_mask [B][max_pages] per page, or [B][max_pages*16]
+ * per token when token_granular) fill new slots 0, 1, ... in order.  New
+ * page m reuses old page j when it holds exactly j's first tokens at the
+ * same slots (page masks always do: no K/V moves); otherwise it takes a
+ * fresh page popped from free_list[*free_top - 1 - i] in (b, m) order and
+ * the tokens' K and V (all heads) are copied there.  Old pages not reused
+ * are then pushed in (b, j) order.  block_table rows are rewritten (-1
+ * padded), seq_lens become the kept counts, *free_top is updated.
+ * free_list has num_pages entries (device).  Device errors: KV_ENOSPACE
+ * (nothing is changed), KV_EBADPAGE. */
+int kv_compact(int32_t *block_table, int max_pages, int32_t *seq_lens, const uint8_t *keep_mask,
+               int token_granular, void *k_pool, void *v_pool, int num_pages, int32_t *free_list,
+               int32_t *free_top, int B, int Hkv, int d, int page_size, int dtype, void *ws,
+               size_t ws_bytes, void *stream);
+
+size_t kv_append_workspace_size(int B);
+
+/* Append one token per sequence: K/V (k_new, v_new [B][Hkv][d], device) go
+ * to slot L_b % 16 of page block_table[b][L_b / 16]; when L_b % 16 == 0 that
+ * page is first popped from the free list (pops in ascending b).  Then
+ * L_b += 1.  Device errors (nothing is changed): KV_ENOSPACE, KV_EFULL. */
+int kv_append(const void *k_new, const void *v_new, void *k_pool, void *v_pool, int num_pages,
+              int32_t *block_table, int max_pages, int32_t *seq_lens, int32_t *free_list,
+              int32_t *free_top, int B, int Hkv, int d, int page_size, int dtype, void *ws,
+              size_t ws_bytes, void *stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PAGED_KV_B300_KV_H */

@@ -769,20 +769,36 @@ out:
 /* Append: write the new token's K/V at slot L_b % ps of page               */
 /* block_table[b][L_b / ps]; when L_b % ps == 0 the page is first popped     */
 /* from the free list (pops in ascending b).  Then L_b += 1.  Nothing        */
-/* changes if the pops exceed the stack (-3) or a row is full (-6).          */
+/* changes on an error: a full row (-6), else a bad page id in use or about  */
+/* to be popped (-2), else too few free pages (-3).                          */
 /* k_new, v_new: [B][Hkv][d].                                                 */
 /* ------------------------------------------------------------------------ */
 int or_append(const uint16_t *k_new, const uint16_t *v_new, uint16_t *k_pool, uint16_t *v_pool,
               int num_pages, int32_t *table, int max_pages, int32_t *seq_lens, int32_t *free_list,
               int32_t *free_top, int B, int Hkv, int d, int ps) {
+  /* checks first, in this order of precedence: a full row, a bad page id (one
+   * in use, or one that would be popped), too few free pages */
   int64_t need = 0;
+  int full = 0, bad = 0;
   for (int b = 0; b < B; ++b) {
     int64_t L = seq_lens[b];
-    if (L % ps == 0) {
-      if (L / ps >= max_pages) return OR_EFULL;
+    if (L < 0) {
+      bad = 1;
+    } else if (L % ps == 0) {
+      if (L / ps >= max_pages) full = 1;
       ++need;
+    } else {
+      int32_t p = table[(size_t)b * max_pages + L / ps];
+      if (p < 0 || p >= num_pages) bad = 1;
     }
   }
+  if (need <= *free_top)
+    for (int64_t i = 0; i < need; ++i) {
+      int32_t p = free_list[*free_top - 1 - i];
+      if (p < 0 || p >= num_pages) bad = 1;
+    }
+  if (full) return OR_EFULL;
+  if (bad) return OR_EBADPAGE;
   if (need > *free_top) return OR_ENOSPACE;
   int64_t top = *free_top;
   for (int b = 0; b < B; ++b) {
@@ -790,7 +806,6 @@ int or_append(const uint16_t *k_new, const uint16_t *v_new, uint16_t *k_pool, ui
     int32_t *slot = &table[(size_t)b * max_pages + L / ps];
     if (L % ps == 0) *slot = free_list[--top];
     int32_t p = *slot;
-    if (p < 0 || p >= num_pages) return OR_EBADPAGE;
     for (int h = 0; h < Hkv; ++h) {
       size_t dst = (((size_t)p * Hkv + h) * ps + (size_t)(L % ps)) * d;
       memcpy(k_pool + dst, k_new + ((size_t)b * Hkv + h) * d, sizeof(uint16_t) * d);

@@ -1,0 +1,176 @@
+// C ABI entry points: status handling, decode (device and host buffers), and
+// the stand-alone workqueue builder.  Argument checks happen here, on the
+// host, before anything is enqueued.
+#include <string.h>
+
+#include <algorithm>
+
+#include "kv_internal.h"
+
+using namespace kvb;
+
+extern "C" {
+
+const char* kv_status_string(int code) {
+  switch (code) {
+    case KV_OK: return "ok";
+    case KV_EINVAL: return "invalid argument";
+    case KV_EBADPAGE: return "page id outside the pool";
+    case KV_ENOSPACE: return "free list exhausted";
+    case KV_EWORKSPACE: return "workspace too small";
+    case KV_ECUDA: return "CUDA runtime error";
+    case KV_EFULL: return "block-table row full";
+    case KV_ETIMEOUT: return "kernel wait timed out";
+    default: return "unknown status";
+  }
+}
+
+size_t kv_status_workspace_size(void) { return kHeaderBytes; }
+
+int kv_workspace_reset(void* ws, void* stream) {
+  if (!ws) return KV_EINVAL;
+  return cudaMemsetAsync(ws, 0, kHeaderBytes, static_cast<cudaStream_t>(stream)) == cudaSuccess
+             ? KV_OK
+             : KV_ECUDA;
+}
+
+int kv_get_status(void* ws, void* stream) {
+  if (!ws) return KV_EINVAL;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  int host = 0;
+  if (cudaMemcpyAsync(&host, ws, sizeof(int), cudaMemcpyDeviceToHost, s) != cudaSuccess)
+    return KV_ECUDA;
+  if (cudaStreamSynchronize(s) != cudaSuccess) return KV_ECUDA;
+  if (host != 0) {
+    if (cudaMemsetAsync(ws, 0, sizeof(int), s) != cudaSuccess) return KV_ECUDA;
+    if (cudaStreamSynchronize(s) != cudaSuccess) return KV_ECUDA;
+  }
+  return host;
+}
+
+int kv_decode_num_workers(int Hq, int Hkv, int d, int page_size, int dtype) {
+  return decode_num_workers(Hq, Hkv, d, page_size, dtype);
+}
+
+size_t kv_decode_workspace_size(int B, int Hq, int Hkv, int d, int max_pages, int page_size,
+                                int pages_per_split) {
+  if (B < 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv || max_pages < 0 || pages_per_split < 0) return 0;
+  // the worker count can differ between the fp16 and bf16 kernels: size for both
+  const int nw = std::max(decode_num_workers(Hq, Hkv, d, page_size, KV_F16),
+                          decode_num_workers(Hq, Hkv, d, page_size, KV_BF16));
+  if (nw <= 0) return 0;
+  return decode_layout(B, Hq, Hkv, d, max_pages, page_size, pages_per_split, nw).total;
+}
+
+int kv_decode(const void* q, const void* k_pool, const void* v_pool, int num_pages,
+              const int32_t* block_table, int max_pages, const int32_t* seq_lens, int B,
+              int page_size, int Hq, int Hkv, int d, int dtype, float scale, int pages_per_split,
+              float* out, float* lse, void* ws, size_t ws_bytes, void* stream) {
+  return decode_launch(q, k_pool, v_pool, num_pages, block_table, max_pages, seq_lens, B,
+                       page_size, Hq, Hkv, d, dtype, scale, pages_per_split, out, lse, ws, ws_bytes,
+                       static_cast<cudaStream_t>(stream));
+}
+
+namespace {
+struct HostIoLayout {
+  size_t q, table, seq_lens, out, lse, total;
+};
+HostIoLayout hostio_layout(size_t base, int B, int Hq, int d, int max_pages) {
+  HostIoLayout L{};
+  size_t off = align_up(base, 256);
+  auto take = [&](size_t bytes) {
+    size_t o = off;
+    off = align_up(off + bytes, 256);
+    return o;
+  };
+  L.q = take((size_t)B * Hq * d * 2);
+  L.table = take((size_t)B * max_pages * 4);
+  L.seq_lens = take((size_t)B * 4);
+  L.out = take((size_t)B * Hq * d * 4);
+  L.lse = take((size_t)B * Hq * 4);
+  L.total = off;
+  return L;
+}
+}  // namespace
+
+size_t kv_decode_hostio_workspace_size(int B, int Hq, int Hkv, int d, int max_pages, int page_size,
+                                       int pages_per_split) {
+  const size_t base = kv_decode_workspace_size(B, Hq, Hkv, d, max_pages, page_size, pages_per_split);
+  if (!base) return 0;
+  return hostio_layout(base, B, Hq, d, max_pages).total;
+}
+
+int kv_decode_hostio(const void* h_q, const void* k_pool, const void* v_pool, int num_pages,
+                     const int32_t* h_block_table, int max_pages, const int32_t* h_seq_lens, int B,
+                     int page_size, int Hq, int Hkv, int d, int dtype, float scale,
+                     int pages_per_split, float* h_out, float* h_lse, void* ws, size_t ws_bytes,
+                     void* stream) {
+  if (B < 0 || max_pages < 0) return KV_EINVAL;
+  if (B == 0) return KV_OK;
+  if (!h_q || !h_block_table || !h_seq_lens || !h_out || !h_lse || !ws) return KV_EINVAL;
+  const size_t base = kv_decode_workspace_size(B, Hq, Hkv, d, max_pages, page_size, pages_per_split);
+  if (!base) return KV_EINVAL;
+  const HostIoLayout L = hostio_layout(base, B, Hq, d, max_pages);
+  if (ws_bytes < L.total) return KV_EWORKSPACE;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  uint8_t* w = static_cast<uint8_t*>(ws);
+  const size_t qb = (size_t)B * Hq * d * 2, tb = (size_t)B * max_pages * 4, sb = (size_t)B * 4;
+  if (cudaMemcpyAsync(w + L.q, h_q, qb, cudaMemcpyHostToDevice, s) != cudaSuccess ||
+      cudaMemcpyAsync(w + L.table, h_block_table, tb, cudaMemcpyHostToDevice, s) != cudaSuccess ||
+      cudaMemcpyAsync(w + L.seq_lens, h_seq_lens, sb, cudaMemcpyHostToDevice, s) != cudaSuccess)
+    return KV_ECUDA;
+  int rc = decode_launch(w + L.q, k_pool, v_pool, num_pages,
+                         reinterpret_cast<const int32_t*>(w + L.table), max_pages,
+                         reinterpret_cast<const int32_t*>(w + L.seq_lens), B, page_size, Hq, Hkv, d,
+                         dtype, scale, pages_per_split, reinterpret_cast<float*>(w + L.out),
+                         reinterpret_cast<float*>(w + L.lse), ws, base, s);
+  if (rc) return rc;
+  if (cudaMemcpyAsync(h_out, w + L.out, (size_t)B * Hq * d * 4, cudaMemcpyDeviceToHost, s) !=
+          cudaSuccess ||
+      cudaMemcpyAsync(h_lse, w + L.lse, (size_t)B * Hq * 4, cudaMemcpyDeviceToHost, s) != cudaSuccess)
+    return KV_ECUDA;
+  return KV_OK;
+}
+
+int kv_build_workqueue(const int32_t* seq_lens, int B, int Hkv, int page_size, int max_pages,
+                       int pages_per_split, int n_workers, int32_t* tasks, int max_tasks,
+                       int32_t* chunk_begin, int max_chunks, int32_t* seq_group_begin,
+                       int32_t* seq_nsplit, int32_t* meta, void* ws, void* stream) {
+  if (B < 0 || Hkv <= 0 || page_size <= 0 || max_pages < 0 || pages_per_split < 0 ||
+      max_tasks < 0 || max_chunks < 1)
+    return KV_EINVAL;
+  if (pages_per_split == 0 && n_workers <= 0) return KV_EINVAL;
+  if (!tasks || !chunk_begin || !meta || !ws || (B > 0 && (!seq_lens || !seq_group_begin || !seq_nsplit)))
+    return KV_EINVAL;
+  if (((uintptr_t)tasks & 15) || ((uintptr_t)ws & 255)) return KV_EINVAL;
+  // scratch for per-sequence page offsets lives after the workspace header
+  WorkqueueArgs a{};
+  a.seq_lens = seq_lens;
+  a.B = B;
+  a.Hkv = Hkv;
+  a.page_size = page_size;
+  a.max_pages = max_pages;
+  a.chunk_req = pages_per_split;
+  a.n_workers = n_workers;
+  a.min_chunk = kMinChunk;
+  a.tasks = tasks;
+  a.max_tasks = max_tasks;
+  a.chunk_begin = chunk_begin;
+  a.max_chunks = max_chunks;
+  a.seq_group_begin = seq_group_begin;
+  a.seq_nsplit = seq_nsplit;
+  a.seq_page_off = reinterpret_cast<long long*>(static_cast<uint8_t*>(ws) + kHeaderBytes);
+  a.meta = meta;
+  a.status = static_cast<int*>(ws);
+  return launch_build_workqueue(a, static_cast<cudaStream_t>(stream)) == cudaSuccess ? KV_OK
+                                                                                     : KV_ECUDA;
+}
+
+int kv_profile_next_decode(void* event_before, void* event_after) {
+  set_profile_events(static_cast<cudaEvent_t>(event_before), static_cast<cudaEvent_t>(event_after));
+  return KV_OK;
+}
+
+size_t kv_workqueue_workspace_size(int B) { return kHeaderBytes + align_up((size_t)(B > 0 ? B : 1) * 8, 256); }
+
+}  // extern "C"

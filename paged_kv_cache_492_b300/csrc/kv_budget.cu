@@ -1,0 +1,988 @@
+// Page budgeting (GrowPage, mlsanity.com -- Abstract; aitrending.vip summary
+// -- Technical Details): dual-timescale query summaries, page key summaries,
+// page scores, top-k retention with compress-or-grow at capacity boundaries,
+// compaction of the block table (and K/V for token-granular masks), and the
+// per-token append that draws pages from the integer free list (Elastic KV
+// Cache, paperlayer.ai -- section 2).
+//
+// Every floating-point value that decides an integer (EMAs, summaries,
+// scores, the drift threshold) is computed in fp32 with explicitly rounded
+// operations (__fadd_rn / __fmul_rn / __fdiv_rn, no contraction) in the order
+// stated in include/kv.h, so selections are reproducible bit for bit.
+#include <math.h>
+
+#include "kv_internal.h"
+
+namespace kvb {
+namespace {
+
+constexpr unsigned FULL = 0xffffffffu;
+
+template <class T>
+__device__ __forceinline__ float ld16(const uint16_t* p, size_t i) {
+  return T::to_f(p[i]);
+}
+
+// ------------------------------------------------------------------ EMA
+template <class T>
+__global__ void ema_kernel(const uint16_t* __restrict__ q, int Hq, int Hkv, int d, float a_fast,
+                           float a_slow, int first, float* __restrict__ ema) {
+  const int b = blockIdx.x / Hkv, h = blockIdx.x - b * Hkv;
+  const int G = Hq / Hkv;
+  for (int c = threadIdx.x; c < d; c += blockDim.x) {
+    float acc = 0.0f;
+    for (int g = 0; g < G; ++g)
+      acc = __fadd_rn(acc, ld16<T>(q, ((size_t)b * Hq + (size_t)h * G + g) * d + c));
+    const float gm = __fdiv_rn(acc, (float)G);
+    for (int u = 0; u < 2; ++u) {
+      float* e = ema + (((size_t)b * 2 + u) * Hkv + h) * d + c;
+      const float a = u == 0 ? a_fast : a_slow;
+      *e = first ? gm : __fadd_rn(__fmul_rn(a, *e), __fmul_rn(__fsub_rn(1.0f, a), gm));
+    }
+  }
+}
+
+// ------------------------------------------------------------------ boundary marks
+__global__ void mark_kernel(const int32_t* __restrict__ seq_lens, const int32_t* __restrict__ budget,
+                            int B, int ps, int mode, uint8_t* __restrict__ active) {
+  const int b = blockIdx.x * blockDim.x + threadIdx.x;
+  if (b >= B) return;
+  const long long L = seq_lens[b];
+  if (mode == 0)
+    active[b] = ceil_div_ll(L, ps) > budget[b];
+  else
+    active[b] = L > 0 && L % ps == 0 && L / ps >= budget[b];
+}
+
+// ------------------------------------------------------------------ page summaries
+// One block per (listed page, KV head); thread c: mean/min/max over the page's slots.
+template <class T>
+__global__ void summary_kernel(const uint16_t* __restrict__ k_pool, int num_pages,
+                               const int32_t* __restrict__ page_ids, int n,
+                               const int32_t* __restrict__ table, int max_pages,
+                               const int32_t* __restrict__ seq_lens,
+                               const uint8_t* __restrict__ active, int Hkv, int ps, int d,
+                               float* __restrict__ summ, int* status) {
+  const int i = blockIdx.x / Hkv, h = blockIdx.x - i * Hkv;
+  int page;
+  if (page_ids) {
+    page = page_ids[i];
+  } else {
+    // last full page of an active sequence
+    if (active && !active[i]) return;
+    const int L = seq_lens[i];
+    if (L < ps) return;
+    page = table[(size_t)i * max_pages + (L / ps - 1)];
+  }
+  if (page < 0 || page >= num_pages) {
+    if (threadIdx.x == 0) set_status(status, KV_EBADPAGE);
+    return;
+  }
+  for (int c = threadIdx.x; c < d; c += blockDim.x) {
+    float acc = 0.0f, mn = INFINITY, mx = -INFINITY;
+    for (int t = 0; t < ps; ++t) {
+      const float x = ld16<T>(k_pool, (((size_t)page * Hkv + h) * ps + t) * d + c);
+      acc = __fadd_rn(acc, x);
+      mn = x < mn ? x : mn;
+      mx = x > mx ? x : mx;
+    }
+    float* s = summ + ((size_t)page * Hkv + h) * 3 * d;
+    s[c] = __fdiv_rn(acc, (float)ps);
+    s[d + c] = mn;
+    s[2 * d + c] = mx;
+  }
+}
+
+// ------------------------------------------------------------------ scores
+// One warp per (sequence, logical page); lane l owns channels l*CPL.. of every head.
+template <int CPL>
+__global__ void score_kernel(const float* __restrict__ ema, const float* __restrict__ summ,
+                             int num_pages, const int32_t* __restrict__ table, int max_pages,
+                             const int32_t* __restrict__ seq_lens, const uint8_t* __restrict__ active,
+                             int B, int Hkv, int ps, float* __restrict__ scores, int* status) {
+  constexpr int d = 32 * CPL;
+  const int lane = threadIdx.x & 31;
+  const long long wid = (long long)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  if (wid >= (long long)B * max_pages) return;
+  const int b = (int)(wid / max_pages), j = (int)(wid - (long long)b * max_pages);
+  if (active && !active[b]) return;
+  float2* out = reinterpret_cast<float2*>(scores + ((size_t)b * max_pages + j) * 2);
+  const long long np = ceil_div_ll(seq_lens[b], ps);
+  if (j >= np) {
+    if (lane == 0) *out = make_float2(-INFINITY, -INFINITY);
+    return;
+  }
+  const int page = table[(size_t)b * max_pages + j];
+  if (page < 0 || page >= num_pages) {
+    if (lane == 0) set_status(status, KV_EBADPAGE);
+    return;
+  }
+  float af = 0.0f, as = 0.0f;
+  for (int h = 0; h < Hkv; ++h) {
+    const float* uf = ema + (((size_t)b * 2 + 0) * Hkv + h) * d + lane * CPL;
+    const float* us = ema + (((size_t)b * 2 + 1) * Hkv + h) * d + lane * CPL;
+    const float* sm = summ + ((size_t)page * Hkv + h) * 3 * d + lane * CPL;
+#pragma unroll
+    for (int i = 0; i < CPL; ++i) {
+      const float mu = sm[i], mn = sm[d + i], mx = sm[2 * d + i];
+      {
+        const float u = uf[i];
+        const float ta = __fmul_rn(u, mn), tb = __fmul_rn(u, mx);
+        af = __fadd_rn(af, __fadd_rn(__fmul_rn(u, mu), ta > tb ? ta : tb));
+      }
+      {
+        const float u = us[i];
+        const float ta = __fmul_rn(u, mn), tb = __fmul_rn(u, mx);
+        as = __fadd_rn(as, __fadd_rn(__fmul_rn(u, mu), ta > tb ? ta : tb));
+      }
+    }
+  }
+#pragma unroll
+  for (int s = 16; s >= 1; s >>= 1) {
+    af = __fadd_rn(af, __shfl_xor_sync(FULL, af, s));
+    as = __fadd_rn(as, __shfl_xor_sync(FULL, as, s));
+  }
+  if (lane == 0) *out = make_float2(af, as);
+}
+
+// ------------------------------------------------------------------ selection
+constexpr int kSelThreads = 1024;
+constexpr int kMaxSelectPages = 8192;
+
+__device__ __forceinline__ int block_sum_int(int v, int* sm) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
+  for (int o = 16; o; o >>= 1) v += __shfl_xor_sync(FULL, v, o);
+  __syncthreads();
+  if (lane == 0) sm[warp] = v;
+  __syncthreads();
+  int t = 0;
+  for (int w = 0; w < nw; ++w) t += sm[w];
+  __syncthreads();
+  return t;
+}
+
+// rank of candidate j among candidates by key (larger first, ties: lower index)
+__device__ __forceinline__ int rank_of(const float* key, const uint8_t* is_cand, int n, int j) {
+  const float kj = key[j];
+  int r = 0;
+  for (int i = 0; i < n; ++i) r += is_cand[i] && (key[i] > kj || (key[i] == kj && i < j));
+  return r;
+}
+
+struct SelectArgs {
+  const float* scores;
+  const int32_t* seq_lens;
+  const uint8_t* active;
+  int32_t* budget;
+  int B, max_pages, ps, n_first, n_last, mode;
+  float delta, ws_frac;
+  uint8_t* keep;
+  uint8_t* grow;
+  int32_t* drift;
+  int32_t* wants;  // [B] workspace
+  int* status;
+};
+
+// Phase 1: one block per sequence: ranks, drift, the compaction keep set.
+__global__ void __launch_bounds__(kSelThreads) select_rank_kernel(const SelectArgs a) {
+  extern __shared__ float sel_sm[];
+  __shared__ int red[32];
+  const int b = blockIdx.x;
+  const int n = (int)ceil_div_ll(a.seq_lens[b], a.ps);
+  uint8_t* keep = a.keep + (size_t)b * a.max_pages;
+  const bool act = a.active ? a.active[b] != 0 : true;
+  if (threadIdx.x == 0) {
+    a.wants[b] = 0;
+    a.grow[b] = 0;
+    if (a.drift) a.drift[b] = 0;
+  }
+  if (!act || n > a.max_pages) {
+    if (n > a.max_pages && threadIdx.x == 0) set_status(a.status, KV_EINVAL);
+    for (int j = threadIdx.x; j < a.max_pages; j += blockDim.x) keep[j] = j < n;
+    return;
+  }
+  float* sf = sel_sm;
+  float* ss = sf + n;
+  float* rr = ss + n;
+  uint8_t* cand = reinterpret_cast<uint8_t*>(rr + n);
+  int my_forced = 0;
+  for (int j = threadIdx.x; j < n; j += blockDim.x) {
+    const float2 s = reinterpret_cast<const float2*>(a.scores + (size_t)b * a.max_pages * 2)[j];
+    sf[j] = s.x;
+    ss[j] = s.y;
+    rr[j] = __fadd_rn(s.x, s.y);
+    const bool forced = j < a.n_first || j >= n - a.n_last;
+    cand[j] = !forced;
+    my_forced += forced;
+  }
+  __syncthreads();
+  const int nf = block_sum_int(my_forced, red);
+  const int nc = n - nf;
+  int k;
+  int wants = 0;
+  if (a.mode == KV_SELECT_TOPK) {
+    k = a.budget[b] - nf;
+  } else {
+    k = n - 1 - nf;
+    if (nc == 0) {
+      wants = 1;
+    } else {
+      int w = (int)ceilf(__fmul_rn(a.ws_frac, (float)nc));
+      w = max(1, min(w, nc));
+      int my_d = 0;
+      for (int j = threadIdx.x; j < n; j += blockDim.x) {
+        if (!cand[j]) continue;
+        const bool in_f = rank_of(sf, cand, n, j) < w;
+        const bool in_s = rank_of(ss, cand, n, j) < w;
+        my_d += in_f && !in_s;
+      }
+      const int D = block_sum_int(my_d, red);
+      wants = (float)D > __fmul_rn(a.delta, (float)w);
+      if (threadIdx.x == 0 && a.drift) a.drift[b] = D;
+    }
+  }
+  if (k < 0) k = 0;
+  for (int j = threadIdx.x; j < a.max_pages; j += blockDim.x) {
+    uint8_t kp = 0;
+    if (j < n) kp = cand[j] ? (rank_of(rr, cand, n, j) < k) : 1;
+    keep[j] = kp;
+  }
+  if (threadIdx.x == 0) a.wants[b] = wants;
+}
+
+// Phase 2 (boundary mode): grant grows in ascending b while free pages last.
+__global__ void __launch_bounds__(1024) select_grant_kernel(const SelectArgs a,
+                                                            const int32_t* __restrict__ free_top) {
+  __shared__ int sm[32];
+  __shared__ int s_carry;
+  const int free_count = *free_top;
+  if (threadIdx.x == 0) s_carry = 0;
+  __syncthreads();
+  for (int base = 0; base < a.B; base += blockDim.x) {
+    const int b = base + threadIdx.x;
+    const int w = b < a.B ? a.wants[b] : 0;
+    // inclusive scan of w across the block
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    int x = w;
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(FULL, x, o);
+      if (lane >= o) x += y;
+    }
+    if (lane == 31) sm[warp] = x;
+    __syncthreads();
+    int before = 0;
+    for (int i = 0; i < warp; ++i) before += sm[i];
+    const int carry = s_carry;
+    const int excl = carry + before + x - w;
+    if (b < a.B && w && excl < free_count) {
+      a.grow[b] = 1;
+      a.budget[b] += 1;
+      const int n = (int)ceil_div_ll(a.seq_lens[b], a.ps);
+      uint8_t* keep = a.keep + (size_t)b * a.max_pages;
+      for (int j = 0; j < n && j < a.max_pages; ++j) keep[j] = 1;
+    }
+    __syncthreads();
+    if (threadIdx.x == blockDim.x - 1) s_carry = carry + before + x;
+    __syncthreads();
+  }
+}
+
+// ------------------------------------------------------------------ compaction
+struct CompactArgs {
+  int32_t* table;
+  int max_pages;
+  int32_t* seq_lens;
+  const uint8_t* keep;
+  int token_granular;
+  uint8_t* k_pool;
+  uint8_t* v_pool;
+  int num_pages;
+  int32_t* free_list;
+  int32_t* free_top;
+  int B, Hkv, d, ps;
+  // workspace
+  int32_t* new_len;    // [B]
+  int32_t* pop_base;   // [B]
+  int32_t* push_base;  // [B]
+  int32_t* fresh_ids;  // [max_fresh]
+  long long max_fresh;
+  int32_t* ctl;        // [0] abort flag, [1] top after pops
+  int* status;
+};
+
+// keep bit of token t (valid token of b)
+__device__ __forceinline__ bool kept_token(const CompactArgs& a, int b, long long t) {
+  if (a.token_granular) return a.keep[(size_t)b * a.max_pages * a.ps + t] != 0;
+  return a.keep[(size_t)b * a.max_pages + t / a.ps] != 0;
+}
+
+// Per source page j of b: kept count c, whether the kept slots are a prefix.
+__device__ __forceinline__ void page_keep_info(const CompactArgs& a, int b, int j, int L, int* c,
+                                               bool* prefix) {
+  const int lo = j * a.ps, hi = min(L, lo + a.ps);
+  int cnt = 0;
+  bool pre = true, gap = false;
+  for (int t = lo; t < hi; ++t) {
+    const bool k = kept_token(a, b, t);
+    if (k) {
+      if (gap) pre = false;
+      ++cnt;
+    } else {
+      gap = true;
+    }
+  }
+  *c = cnt;
+  *prefix = pre;
+}
+
+// Plan: one warp per sequence computes kept tokens, fresh and freed page
+// counts; one block scans them, checks the free list, copies the popped ids.
+__global__ void __launch_bounds__(1024) compact_plan_kernel(const CompactArgs a) {
+  __shared__ long long sm[32];
+  __shared__ int s_info[4];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
+  // per-sequence counts into the workspace (new_len, pop_base <- fresh, push_base <- freed)
+  for (int b = warp; b < a.B; b += nw) {
+    const int L = a.seq_lens[b];
+    const int np = (int)ceil_div_ll(L, a.ps);
+    int kept_before = 0, reused = 0;
+    for (int j0 = 0; j0 < np; j0 += 32) {
+      const int j = j0 + lane;
+      int c = 0;
+      bool pre = true;
+      if (j < np) page_keep_info(a, b, j, L, &c, &pre);
+      for (int o = 16; o; o >>= 1) c += __shfl_xor_sync(FULL, c, o);
+      kept_before += c;
+    }
+    const int K = kept_before;
+    kept_before = 0;
+    for (int j0 = 0; j0 < np; j0 += 32) {
+      const int j = j0 + lane;
+      int c = 0;
+      bool pre = true;
+      if (j < np) page_keep_info(a, b, j, L, &c, &pre);
+      int x = c;
+      for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(FULL, x, o);
+        if (lane >= o) x += y;
+      }
+      const int kb = kept_before + x - c;
+      const bool reuse = j < np && c > 0 && pre && (kb % a.ps == 0) && (c == a.ps || kb + c == K);
+      reused += __popc(__ballot_sync(FULL, reuse));
+      kept_before += __shfl_sync(FULL, x, 31);
+    }
+    if (lane == 0) {
+      const int n_new = (int)ceil_div_ll(K, a.ps);
+      a.new_len[b] = K;
+      a.pop_base[b] = n_new - reused;  // fresh pages (scanned below)
+      a.push_base[b] = np - reused;    // freed pages (scanned below)
+    }
+  }
+  __syncthreads();
+  // exclusive scans over b (single block, sequential chunks)
+  if (threadIdx.x == 0) {
+    s_info[0] = 0;
+    s_info[1] = 0;
+  }
+  __syncthreads();
+  for (int base = 0; base < a.B; base += blockDim.x) {
+    const int b = base + threadIdx.x;
+    const int f = b < a.B ? a.pop_base[b] : 0;
+    const int r = b < a.B ? a.push_base[b] : 0;
+    long long xf = f, xr = r;
+    for (int o = 1; o < 32; o <<= 1) {
+      const long long yf = __shfl_up_sync(FULL, xf, o), yr = __shfl_up_sync(FULL, xr, o);
+      if (lane >= o) { xf += yf; xr += yr; }
+    }
+    if (lane == 31) sm[warp] = (xf << 32) | xr;
+    __syncthreads();
+    long long bf = 0, br = 0;
+    for (int i = 0; i < warp; ++i) { bf += sm[i] >> 32; br += sm[i] & 0xffffffffll; }
+    const int cf = s_info[0], cr = s_info[1];
+    if (b < a.B) {
+      a.pop_base[b] = (int)(cf + bf + xf - f);
+      a.push_base[b] = (int)(cr + br + xr - r);
+    }
+    __syncthreads();
+    if (threadIdx.x == blockDim.x - 1) {
+      s_info[0] = (int)(cf + bf + xf);
+      s_info[1] = (int)(cr + br + xr);
+    }
+    __syncthreads();
+  }
+  const int pops = s_info[0], pushes = s_info[1];
+  const int top = *a.free_top;
+  const bool fail = pops > top || pops > a.max_fresh;
+  if (fail) {
+    if (threadIdx.x == 0) {
+      a.ctl[0] = 1;
+      set_status(a.status, pops > top ? KV_ENOSPACE : KV_EWORKSPACE);
+    }
+    return;
+  }
+  for (int i = threadIdx.x; i < pops; i += blockDim.x) a.fresh_ids[i] = a.free_list[top - 1 - i];
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    a.ctl[0] = 0;
+    a.ctl[1] = top - pops;
+    *a.free_top = top - pops + pushes;
+  }
+}
+
+// Apply: one block per sequence rewrites its row, gathers tokens into fresh
+// pages, pushes its freed pages.
+constexpr int kApplyThreads = 256;
+
+__global__ void __launch_bounds__(kApplyThreads) compact_apply_kernel(const CompactArgs a) {
+  extern __shared__ int32_t cs[];
+  __shared__ int sm[kApplyThreads / 32];
+  __shared__ int s_carry[3];
+  if (a.ctl[0]) return;
+  const int b = blockIdx.x;
+  const int L = a.seq_lens[b];
+  const int np = (int)ceil_div_ll(L, a.ps);
+  const int K = a.new_len[b];
+  const int n_new = (int)ceil_div_ll(K, a.ps);
+  int32_t* old_row = cs;                // [max_pages]
+  int32_t* dest_src = cs + a.max_pages; // [max_pages] old page j reused by dest m, or -1
+  int32_t* kb_arr = dest_src + a.max_pages;  // [max_pages] kept tokens before page j
+  const int32_t* row = a.table + (size_t)b * a.max_pages;
+  for (int j = threadIdx.x; j < a.max_pages; j += blockDim.x) {
+    old_row[j] = j < np ? row[j] : -1;
+    dest_src[j] = -1;
+  }
+  if (threadIdx.x == 0) { s_carry[0] = 0; s_carry[1] = 0; s_carry[2] = 0; }
+  __syncthreads();
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  // pass over source pages: kept-before, reuse, freed ranks
+  for (int base = 0; base < np; base += blockDim.x) {
+    const int j = base + threadIdx.x;
+    int c = 0;
+    bool pre = true;
+    if (j < np) page_keep_info(a, b, j, L, &c, &pre);
+    int x = c;
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(FULL, x, o);
+      if (lane >= o) x += y;
+    }
+    if (lane == 31) sm[warp] = x;
+    __syncthreads();
+    int before = 0;
+    for (int i = 0; i < warp; ++i) before += sm[i];
+    const int carry = s_carry[0];
+    const int kb = carry + before + x - c;
+    const bool reuse = j < np && c > 0 && pre && (kb % a.ps == 0) && (c == a.ps || kb + c == K);
+    if (j < np) {
+      kb_arr[j] = kb;
+      if (reuse) dest_src[kb / a.ps] = j;
+    }
+    __syncthreads();
+    if (threadIdx.x == blockDim.x - 1) s_carry[0] = carry + before + x;
+    __syncthreads();
+  }
+  // freed pages (old pages not reused), pushed in j order
+  const int top_after_pops = a.ctl[1];
+  for (int base = 0; base < np; base += blockDim.x) {
+    const int j = base + threadIdx.x;
+    // page j is reused iff dest_src[kb_arr[j] / ps] == j
+    bool freed = false;
+    if (j < np) {
+      const int m = kb_arr[j] / a.ps;
+      freed = !(m < a.max_pages && dest_src[m] == j && (kb_arr[j] % a.ps) == 0);
+    }
+    const unsigned bal = __ballot_sync(FULL, freed);
+    const int x = __popc(bal & ((1u << lane) - 1u));
+    if (lane == 0) sm[warp] = __popc(bal);
+    __syncthreads();
+    int before = 0;
+    for (int i = 0; i < warp; ++i) before += sm[i];
+    const int carry = s_carry[1];
+    if (freed) {
+      const int page = old_row[j];
+      a.free_list[top_after_pops + a.push_base[b] + carry + before + x] = page;
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      int tot = 0;
+      for (int i = 0; i < (int)(blockDim.x >> 5); ++i) tot += sm[i];
+      s_carry[1] = carry + tot;
+    }
+    __syncthreads();
+  }
+  // new row: reused pages in place, fresh pages in order of m
+  int32_t* out_row = a.table + (size_t)b * a.max_pages;
+  int32_t* new_row = kb_arr;  // reuse: kb_arr no longer needed after the pass above
+  __syncthreads();
+  for (int base = 0; base < a.max_pages; base += blockDim.x) {
+    const int m = base + threadIdx.x;
+    const bool fresh = m < n_new && dest_src[m] < 0;
+    const unsigned bal = __ballot_sync(FULL, fresh);
+    const int x = __popc(bal & ((1u << lane) - 1u));
+    if (lane == 0) sm[warp] = __popc(bal);
+    __syncthreads();
+    int before = 0;
+    for (int i = 0; i < warp; ++i) before += sm[i];
+    const int carry = s_carry[2];
+    if (m < a.max_pages) {
+      int page = -1;
+      if (m < n_new) page = fresh ? a.fresh_ids[a.pop_base[b] + carry + before + x] : old_row[dest_src[m]];
+      new_row[m] = page;
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      int tot = 0;
+      for (int i = 0; i < (int)(blockDim.x >> 5); ++i) tot += sm[i];
+      s_carry[2] = carry + tot;
+    }
+    __syncthreads();
+  }
+  // gather tokens that land in fresh pages (token-granular masks only)
+  if (a.token_granular) {
+    const size_t row_bytes = (size_t)a.d * 2;            // one (token, head) row
+    const size_t head_stride = (size_t)a.ps * row_bytes;  // one (page, head) tile
+    const size_t page_stride = head_stride * a.Hkv;
+    const int vec_per_row = (int)(row_bytes / 16);
+    // walk kept tokens in order with a running rank
+    if (threadIdx.x == 0) s_carry[0] = 0;
+    __syncthreads();
+    for (int base = 0; base < L; base += blockDim.x) {
+      const int t = base + threadIdx.x;
+      const bool k = t < L && kept_token(a, b, t);
+      const unsigned bal = __ballot_sync(FULL, k);
+      const int x = __popc(bal & ((1u << lane) - 1u));
+      if (lane == 0) sm[warp] = __popc(bal);
+      __syncthreads();
+      int before = 0;
+      for (int i = 0; i < warp; ++i) before += sm[i];
+      const int carry = s_carry[0];
+      if (k) {
+        const int r = carry + before + x;
+        const int m = r / a.ps, slot = r % a.ps;
+        if (dest_src[m] < 0) {
+          const int src_page = old_row[t / a.ps];
+          const int dst_page = new_row[m];
+          if (src_page >= 0 && src_page < a.num_pages && dst_page >= 0 && dst_page < a.num_pages) {
+            for (int h = 0; h < a.Hkv; ++h) {
+              const size_t so = (size_t)src_page * page_stride + h * head_stride + (size_t)(t % a.ps) * row_bytes;
+              const size_t dof = (size_t)dst_page * page_stride + h * head_stride + (size_t)slot * row_bytes;
+              const uint4* ks = reinterpret_cast<const uint4*>(a.k_pool + so);
+              const uint4* vs = reinterpret_cast<const uint4*>(a.v_pool + so);
+              uint4* kd = reinterpret_cast<uint4*>(a.k_pool + dof);
+              uint4* vd = reinterpret_cast<uint4*>(a.v_pool + dof);
+              for (int v = 0; v < vec_per_row; ++v) {
+                kd[v] = ks[v];
+                vd[v] = vs[v];
+              }
+            }
+          } else {
+            set_status(a.status, KV_EBADPAGE);
+          }
+        }
+      }
+      __syncthreads();
+      if (threadIdx.x == 0) {
+        int tot = 0;
+        for (int i = 0; i < (int)(blockDim.x >> 5); ++i) tot += sm[i];
+        s_carry[0] = carry + tot;
+      }
+      __syncthreads();
+    }
+  }
+  __syncthreads();
+  for (int m = threadIdx.x; m < a.max_pages; m += blockDim.x) out_row[m] = new_row[m];
+  if (threadIdx.x == 0) a.seq_lens[b] = K;
+}
+
+// ------------------------------------------------------------------ append
+struct AppendArgs {
+  const uint8_t* k_new;
+  const uint8_t* v_new;
+  uint8_t* k_pool;
+  uint8_t* v_pool;
+  int num_pages;
+  int32_t* table;
+  int max_pages;
+  int32_t* seq_lens;
+  int32_t* free_list;
+  int32_t* free_top;
+  int B, Hkv, d, ps;
+  int2* dest;    // [B] (page, slot) workspace
+  int32_t* ctl;  // [0] abort
+  int* status;
+};
+
+__global__ void __launch_bounds__(1024) append_plan_kernel(const AppendArgs a) {
+  __shared__ int sm[32];
+  __shared__ int s_err[3];
+  __shared__ int s_carry;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
+  if (threadIdx.x == 0) { s_err[0] = s_err[1] = 0; s_carry = 0; }
+  __syncthreads();
+  // pass A: rows full, bad page ids already in use, number of pops
+  int my_need = 0;
+  for (int b = threadIdx.x; b < a.B; b += blockDim.x) {
+    const int L = a.seq_lens[b];
+    if (L < 0) {
+      s_err[1] = 1;
+    } else if (L % a.ps == 0) {
+      if (L / a.ps >= a.max_pages) s_err[0] = 1;
+      ++my_need;
+    } else {
+      const int p = a.table[(size_t)b * a.max_pages + L / a.ps];
+      if (p < 0 || p >= a.num_pages) s_err[1] = 1;
+    }
+  }
+  int need = my_need;
+  for (int o = 16; o; o >>= 1) need += __shfl_xor_sync(FULL, need, o);
+  if (lane == 0) sm[warp] = need;
+  __syncthreads();
+  int total = 0;
+  for (int i = 0; i < nw; ++i) total += sm[i];
+  const int top = *a.free_top;
+  // pass B: ids that would be popped must be pool pages
+  if (total <= top)
+    for (int i = threadIdx.x; i < total; i += blockDim.x) {
+      const int p = a.free_list[top - 1 - i];
+      if (p < 0 || p >= a.num_pages) s_err[1] = 1;
+    }
+  __syncthreads();
+  const int err = s_err[0] ? KV_EFULL : (s_err[1] ? KV_EBADPAGE : (total > top ? KV_ENOSPACE : 0));
+  if (err) {
+    if (threadIdx.x == 0) {
+      a.ctl[0] = 1;
+      set_status(a.status, err);
+    }
+    return;
+  }
+  // pass C: pops in ascending b, table and length updates
+  for (int base = 0; base < a.B; base += blockDim.x) {
+    const int b = base + threadIdx.x;
+    const int L = b < a.B ? a.seq_lens[b] : 1;
+    const bool nd = b < a.B && L % a.ps == 0;
+    const unsigned bal = __ballot_sync(FULL, nd);
+    const int x = __popc(bal & ((1u << lane) - 1u));
+    __syncthreads();
+    if (lane == 0) sm[warp] = __popc(bal);
+    __syncthreads();
+    int before = 0;
+    for (int i = 0; i < warp; ++i) before += sm[i];
+    const int carry = s_carry;
+    if (b < a.B) {
+      int32_t* slot = &a.table[(size_t)b * a.max_pages + L / a.ps];
+      if (nd) *slot = a.free_list[top - 1 - (carry + before + x)];
+      a.dest[b] = make_int2(*slot, L % a.ps);
+      a.seq_lens[b] = L + 1;
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      int tot = 0;
+      for (int i = 0; i < nw; ++i) tot += sm[i];
+      s_carry = carry + tot;
+    }
+    __syncthreads();
+  }
+  if (threadIdx.x == 0) {
+    a.ctl[0] = 0;
+    *a.free_top = top - total;
+  }
+}
+
+// Copy the new token's K and V rows (all heads) into place; 16 bytes per thread.
+__global__ void append_copy_kernel(const AppendArgs a) {
+  if (a.ctl[0]) return;
+  const int b = blockIdx.x;
+  const int2 dst = a.dest[b];
+  const size_t row_bytes = (size_t)a.d * 2;
+  const int vec = (int)(row_bytes / 16);
+  for (int i = threadIdx.x; i < a.Hkv * vec; i += blockDim.x) {
+    const int h = i / vec, v = i - h * vec;
+    const size_t so = ((size_t)b * a.Hkv + h) * row_bytes + (size_t)v * 16;
+    const size_t dof = (((size_t)dst.x * a.Hkv + h) * a.ps + dst.y) * row_bytes + (size_t)v * 16;
+    *reinterpret_cast<uint4*>(a.k_pool + dof) = *reinterpret_cast<const uint4*>(a.k_new + so);
+    *reinterpret_cast<uint4*>(a.v_pool + dof) = *reinterpret_cast<const uint4*>(a.v_new + so);
+  }
+}
+
+bool dtype_ok(int dtype) { return dtype == KV_F16 || dtype == KV_BF16; }
+
+size_t ws_take(size_t* off, size_t bytes) {
+  size_t o = *off;
+  *off = align_up(*off + bytes, 256);
+  return o;
+}
+
+}  // namespace
+}  // namespace kvb
+
+using namespace kvb;
+
+extern "C" {
+
+int kv_update_query_summaries(const void* q, int B, int Hq, int Hkv, int d, int dtype, float a_fast,
+                              float a_slow, int first, float* ema, void* stream) {
+  if (B < 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv || d <= 0 || !dtype_ok(dtype)) return KV_EINVAL;
+  if (B == 0) return KV_OK;
+  if (!q || !ema) return KV_EINVAL;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const int threads = d < 128 ? d : 128;
+  if (dtype == KV_BF16)
+    ema_kernel<BF16><<<B * Hkv, threads, 0, s>>>(static_cast<const uint16_t*>(q), Hq, Hkv, d, a_fast,
+                                                 a_slow, first, ema);
+  else
+    ema_kernel<F16><<<B * Hkv, threads, 0, s>>>(static_cast<const uint16_t*>(q), Hq, Hkv, d, a_fast,
+                                                a_slow, first, ema);
+  return cudaGetLastError() == cudaSuccess ? KV_OK : KV_ECUDA;
+}
+
+int kv_mark_active(const int32_t* seq_lens, const int32_t* budget, int B, int page_size, int mode,
+                   uint8_t* active, void* stream) {
+  if (B < 0 || page_size <= 0 || (mode != 0 && mode != 1)) return KV_EINVAL;
+  if (B == 0) return KV_OK;
+  if (!seq_lens || !budget || !active) return KV_EINVAL;
+  mark_kernel<<<ceil_div(B, 256), 256, 0, static_cast<cudaStream_t>(stream)>>>(seq_lens, budget, B,
+                                                                              page_size, mode, active);
+  return cudaGetLastError() == cudaSuccess ? KV_OK : KV_ECUDA;
+}
+
+static int launch_summaries(const void* k_pool, int num_pages, const int32_t* page_ids, int n,
+                            const int32_t* table, int max_pages, const int32_t* seq_lens,
+                            const uint8_t* active, int Hkv, int page_size, int d, int dtype,
+                            float* summ, void* ws, size_t ws_bytes, void* stream) {
+  if (n < 0 || Hkv <= 0 || page_size <= 0 || d <= 0 || num_pages < 0 || !dtype_ok(dtype))
+    return KV_EINVAL;
+  if (n == 0) return KV_OK;
+  if (!k_pool || !summ || !ws || ws_bytes < kHeaderBytes) return KV_EINVAL;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const int threads = d < 128 ? d : 128;
+  int* status = static_cast<int*>(ws);
+  const long long blocks = (long long)n * Hkv;
+  if (blocks > 0x7fffffffll) return KV_EINVAL;
+  if (dtype == KV_BF16)
+    summary_kernel<BF16><<<(unsigned)blocks, threads, 0, s>>>(
+        static_cast<const uint16_t*>(k_pool), num_pages, page_ids, n, table, max_pages, seq_lens,
+        active, Hkv, page_size, d, summ, status);
+  else
+    summary_kernel<F16><<<(unsigned)blocks, threads, 0, s>>>(
+        static_cast<const uint16_t*>(k_pool), num_pages, page_ids, n, table, max_pages, seq_lens,
+        active, Hkv, page_size, d, summ, status);
+  return cudaGetLastError() == cudaSuccess ? KV_OK : KV_ECUDA;
+}
+
+int kv_page_summaries(const void* k_pool, int num_pages, const int32_t* page_ids, int n, int Hkv,
+                      int page_size, int d, int dtype, float* summ, void* ws, size_t ws_bytes,
+                      void* stream) {
+  if (n > 0 && !page_ids) return KV_EINVAL;
+  return launch_summaries(k_pool, num_pages, page_ids, n, nullptr, 0, nullptr, nullptr, Hkv,
+                          page_size, d, dtype, summ, ws, ws_bytes, stream);
+}
+
+int kv_summarize_last_pages(const void* k_pool, int num_pages, const int32_t* block_table,
+                            int max_pages, const int32_t* seq_lens, const uint8_t* active, int B,
+                            int Hkv, int page_size, int d, int dtype, float* summ, void* ws,
+                            size_t ws_bytes, void* stream) {
+  if (B > 0 && (!block_table || !seq_lens)) return KV_EINVAL;
+  if (max_pages < 0) return KV_EINVAL;
+  return launch_summaries(k_pool, num_pages, nullptr, B, block_table, max_pages, seq_lens, active,
+                          Hkv, page_size, d, dtype, summ, ws, ws_bytes, stream);
+}
+
+int kv_score_pages(const float* query_summaries, const float* page_key_summaries, int num_pages,
+                   const int32_t* block_table, int max_pages, const int32_t* seq_lens,
+                   const uint8_t* active, int B, int Hkv, int d, int page_size, float* scores,
+                   void* ws, size_t ws_bytes, void* stream) {
+  if (B < 0 || Hkv <= 0 || page_size <= 0 || max_pages < 0 || (d != 64 && d != 128)) return KV_EINVAL;
+  if (B == 0 || max_pages == 0) return KV_OK;
+  if (!query_summaries || !page_key_summaries || !block_table || !seq_lens || !scores || !ws ||
+      ws_bytes < kHeaderBytes)
+    return KV_EINVAL;
+  const long long warps = (long long)B * max_pages;
+  const int wpb = 8;
+  const long long blocks = ceil_div_ll(warps, wpb);
+  if (blocks > 0x7fffffffll) return KV_EINVAL;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  int* status = static_cast<int*>(ws);
+  if (d == 128)
+    score_kernel<4><<<(unsigned)blocks, wpb * 32, 0, s>>>(query_summaries, page_key_summaries,
+                                                          num_pages, block_table, max_pages, seq_lens,
+                                                          active, B, Hkv, page_size, scores, status);
+  else
+    score_kernel<2><<<(unsigned)blocks, wpb * 32, 0, s>>>(query_summaries, page_key_summaries,
+                                                          num_pages, block_table, max_pages, seq_lens,
+                                                          active, B, Hkv, page_size, scores, status);
+  return cudaGetLastError() == cudaSuccess ? KV_OK : KV_ECUDA;
+}
+
+size_t kv_select_workspace_size(int B, int max_pages) {
+  (void)max_pages;
+  size_t off = kHeaderBytes;
+  ws_take(&off, (size_t)(B > 0 ? B : 1) * 4);
+  return off;
+}
+
+int kv_select_pages(const float* scores, const int32_t* seq_lens, const uint8_t* active,
+                    int32_t* budget, int B, int max_pages, int page_size, int n_first, int n_last,
+                    float delta, float ws_frac, int mode, const int32_t* free_top,
+                    uint8_t* keep_mask, uint8_t* grow, int32_t* drift, void* ws, size_t ws_bytes,
+                    void* stream) {
+  if (B < 0 || max_pages < 0 || page_size <= 0 || n_first < 0 || n_last < 0) return KV_EINVAL;
+  if (mode != KV_SELECT_TOPK && mode != KV_SELECT_BOUNDARY) return KV_EINVAL;
+  if (max_pages > kMaxSelectPages) return KV_EINVAL;
+  if (B == 0) return KV_OK;
+  if (!scores || !seq_lens || !budget || !keep_mask || !grow || !ws) return KV_EINVAL;
+  if (mode == KV_SELECT_BOUNDARY && !free_top) return KV_EINVAL;
+  if (ws_bytes < kv_select_workspace_size(B, max_pages)) return KV_EWORKSPACE;
+  SelectArgs a{};
+  a.scores = scores;
+  a.seq_lens = seq_lens;
+  a.active = active;
+  a.budget = budget;
+  a.B = B;
+  a.max_pages = max_pages;
+  a.ps = page_size;
+  a.n_first = n_first;
+  a.n_last = n_last;
+  a.mode = mode;
+  a.delta = delta;
+  a.ws_frac = ws_frac;
+  a.keep = keep_mask;
+  a.grow = grow;
+  a.drift = drift;
+  a.status = static_cast<int*>(ws);
+  a.wants = reinterpret_cast<int32_t*>(static_cast<uint8_t*>(ws) + kHeaderBytes);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const size_t smem = (size_t)max_pages * (3 * sizeof(float) + 1) + 16;
+  if (cudaFuncSetAttribute(select_rank_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           (int)((size_t)kMaxSelectPages * 13 + 16)) != cudaSuccess)
+    return KV_ECUDA;
+  select_rank_kernel<<<B, kSelThreads, smem, s>>>(a);
+  if (cudaGetLastError() != cudaSuccess) return KV_ECUDA;
+  if (mode == KV_SELECT_BOUNDARY) {
+    select_grant_kernel<<<1, 1024, 0, s>>>(a, free_top);
+    if (cudaGetLastError() != cudaSuccess) return KV_ECUDA;
+  }
+  return KV_OK;
+}
+
+static void compact_layout(int B, int max_pages, size_t* off_new_len, size_t* off_pop,
+                           size_t* off_push, size_t* off_ctl, size_t* off_fresh, long long* max_fresh,
+                           size_t* total) {
+  size_t off = kHeaderBytes;
+  const size_t nb = (size_t)(B > 0 ? B : 1);
+  *off_new_len = ws_take(&off, nb * 4);
+  *off_pop = ws_take(&off, nb * 4);
+  *off_push = ws_take(&off, nb * 4);
+  *off_ctl = ws_take(&off, 16);
+  *max_fresh = (long long)nb * (max_pages > 0 ? max_pages : 1);
+  *off_fresh = ws_take(&off, (size_t)*max_fresh * 4);
+  *total = off;
+}
+
+size_t kv_compact_workspace_size(int B, int max_pages, int page_size, int token_granular) {
+  (void)page_size;
+  (void)token_granular;
+  size_t a, b, c, d, e, t;
+  long long mf;
+  compact_layout(B, max_pages, &a, &b, &c, &d, &e, &mf, &t);
+  return t;
+}
+
+int kv_compact(int32_t* block_table, int max_pages, int32_t* seq_lens, const uint8_t* keep_mask,
+               int token_granular, void* k_pool, void* v_pool, int num_pages, int32_t* free_list,
+               int32_t* free_top, int B, int Hkv, int d, int page_size, int dtype, void* ws,
+               size_t ws_bytes, void* stream) {
+  if (B < 0 || max_pages < 0 || Hkv <= 0 || page_size <= 0 || (d % 8) || d <= 0 || !dtype_ok(dtype))
+    return KV_EINVAL;
+  if (B == 0) return KV_OK;
+  if (!block_table || !seq_lens || !keep_mask || !free_list || !free_top || !ws) return KV_EINVAL;
+  if (token_granular && (!k_pool || !v_pool || ((uintptr_t)k_pool & 15) || ((uintptr_t)v_pool & 15)))
+    return KV_EINVAL;
+  const size_t smem = (size_t)3 * max_pages * 4;
+  if (smem > 200 * 1024) return KV_EINVAL;
+  size_t o_len, o_pop, o_push, o_ctl, o_fresh, total;
+  long long max_fresh;
+  compact_layout(B, max_pages, &o_len, &o_pop, &o_push, &o_ctl, &o_fresh, &max_fresh, &total);
+  if (ws_bytes < total) return KV_EWORKSPACE;
+  uint8_t* w = static_cast<uint8_t*>(ws);
+  CompactArgs a{};
+  a.table = block_table;
+  a.max_pages = max_pages;
+  a.seq_lens = seq_lens;
+  a.keep = keep_mask;
+  a.token_granular = token_granular ? 1 : 0;
+  a.k_pool = static_cast<uint8_t*>(k_pool);
+  a.v_pool = static_cast<uint8_t*>(v_pool);
+  a.num_pages = num_pages;
+  a.free_list = free_list;
+  a.free_top = free_top;
+  a.B = B;
+  a.Hkv = Hkv;
+  a.d = d;
+  a.ps = page_size;
+  a.new_len = reinterpret_cast<int32_t*>(w + o_len);
+  a.pop_base = reinterpret_cast<int32_t*>(w + o_pop);
+  a.push_base = reinterpret_cast<int32_t*>(w + o_push);
+  a.ctl = reinterpret_cast<int32_t*>(w + o_ctl);
+  a.fresh_ids = reinterpret_cast<int32_t*>(w + o_fresh);
+  a.max_fresh = max_fresh;
+  a.status = reinterpret_cast<int*>(w);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  compact_plan_kernel<<<1, 1024, 0, s>>>(a);
+  if (cudaGetLastError() != cudaSuccess) return KV_ECUDA;
+  if (smem > 48 * 1024 &&
+      cudaFuncSetAttribute(compact_apply_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           (int)smem) != cudaSuccess)
+    return KV_ECUDA;
+  compact_apply_kernel<<<B, kApplyThreads, smem, s>>>(a);
+  return cudaGetLastError() == cudaSuccess ? KV_OK : KV_ECUDA;
+}
+
+size_t kv_append_workspace_size(int B) {
+  size_t off = kHeaderBytes;
+  ws_take(&off, (size_t)(B > 0 ? B : 1) * 8);
+  ws_take(&off, 16);
+  return off;
+}
+
+int kv_append(const void* k_new, const void* v_new, void* k_pool, void* v_pool, int num_pages,
+              int32_t* block_table, int max_pages, int32_t* seq_lens, int32_t* free_list,
+              int32_t* free_top, int B, int Hkv, int d, int page_size, int dtype, void* ws,
+              size_t ws_bytes, void* stream) {
+  if (B < 0 || max_pages < 0 || Hkv <= 0 || page_size <= 0 || d <= 0 || (d % 8) || !dtype_ok(dtype))
+    return KV_EINVAL;
+  if (B == 0) return KV_OK;
+  if (!k_new || !v_new || !k_pool || !v_pool || !block_table || !seq_lens || !free_list ||
+      !free_top || !ws)
+    return KV_EINVAL;
+  if (((uintptr_t)k_new | (uintptr_t)v_new | (uintptr_t)k_pool | (uintptr_t)v_pool) & 15)
+    return KV_EINVAL;
+  if (ws_bytes < kv_append_workspace_size(B)) return KV_EWORKSPACE;
+  uint8_t* w = static_cast<uint8_t*>(ws);
+  size_t off = kHeaderBytes;
+  const size_t o_dest = ws_take(&off, (size_t)B * 8);
+  const size_t o_ctl = ws_take(&off, 16);
+  AppendArgs a{};
+  a.k_new = static_cast<const uint8_t*>(k_new);
+  a.v_new = static_cast<const uint8_t*>(v_new);
+  a.k_pool = static_cast<uint8_t*>(k_pool);
+  a.v_pool = static_cast<uint8_t*>(v_pool);
+  a.num_pages = num_pages;
+  a.table = block_table;
+  a.max_pages = max_pages;
+  a.seq_lens = seq_lens;
+  a.free_list = free_list;
+  a.free_top = free_top;
+  a.B = B;
+  a.Hkv = Hkv;
+  a.d = d;
+  a.ps = page_size;
+  a.dest = reinterpret_cast<int2*>(w + o_dest);
+  a.ctl = reinterpret_cast<int32_t*>(w + o_ctl);
+  a.status = reinterpret_cast<int*>(w);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  append_plan_kernel<<<1, 1024, 0, s>>>(a);
+  if (cudaGetLastError() != cudaSuccess) return KV_ECUDA;
+  append_copy_kernel<<<B, 128, 0, s>>>(a);
+  return cudaGetLastError() == cudaSuccess ? KV_OK : KV_ECUDA;
+}
+
+}  // extern "C"

@@ -1,0 +1,303 @@
+"""Python binding of the C ABI in include/kv.h (ctypes).
+
+Argument marshalling only: every function here forwards to the CUDA library
+libkv.so with the same name; all computation happens in its kernels.  Tensors
+are torch tensors (device memory and streams come from torch); raw integers
+are accepted wherever a pointer is expected.  A missing or unloadable
+library raises -- there is no fallback path.
+"""
+from __future__ import annotations
+
+import ctypes as C
+import os
+import re
+import threading
+from typing import Optional
+
+import torch
+
+from . import build as _build
+
+KV_OK, KV_EINVAL, KV_EBADPAGE, KV_ENOSPACE, KV_EWORKSPACE, KV_ECUDA, KV_EFULL, KV_ETIMEOUT = (
+    0, -1, -2, -3, -4, -5, -6, -7)
+KV_F16, KV_BF16 = 0, 1
+KV_SELECT_TOPK, KV_SELECT_BOUNDARY = 0, 1
+
+HEADER = os.path.join(_build.INCLUDE, "kv.h")
+_lock = threading.Lock()
+_lib = None
+
+
+class KVError(RuntimeError):
+    def __init__(self, code: int, what: str = ""):
+        msg = status_string(code) if _lib is not None else str(code)
+        super().__init__(f"{what}: {msg} ({code})" if what else f"{msg} ({code})")
+        self.code = code
+
+
+def declared_functions() -> list:
+    """Names of the functions include/kv.h declares."""
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(kv_[a-z0-9_]+)\s*\(", text)))
+
+
+def lib():
+    global _lib
+    with _lock:
+        if _lib is None:
+            path = _build.LIB
+            if _build.stale():
+                _build.build()
+            if not os.path.exists(path):
+                raise ImportError(f"CUDA library {path} is missing; run paged_kv_cache_492_b300.build")
+            _lib = C.CDLL(path)
+            _declare(_lib)
+    return _lib
+
+
+P, I, SZ, F = C.c_void_p, C.c_int, C.c_size_t, C.c_float
+
+_SIGS = {
+    "kv_status_string": ([I], C.c_char_p),
+    "kv_status_workspace_size": ([], SZ),
+    "kv_workspace_reset": ([P, P], I),
+    "kv_get_status": ([P, P], I),
+    "kv_decode_num_workers": ([I, I, I, I, I], I),
+    "kv_decode_workspace_size": ([I, I, I, I, I, I, I], SZ),
+    "kv_decode": ([P, P, P, I, P, I, P, I, I, I, I, I, I, F, I, P, P, P, SZ, P], I),
+    "kv_decode_hostio_workspace_size": ([I, I, I, I, I, I, I], SZ),
+    "kv_decode_hostio": ([P, P, P, I, P, I, P, I, I, I, I, I, I, F, I, P, P, P, SZ, P], I),
+    "kv_workqueue_workspace_size": ([I], SZ),
+    "kv_profile_next_decode": ([P, P], I),
+    "kv_build_workqueue": ([P, I, I, I, I, I, I, P, I, P, I, P, P, P, P, P], I),
+    "kv_update_query_summaries": ([P, I, I, I, I, I, F, F, I, P, P], I),
+    "kv_mark_active": ([P, P, I, I, I, P, P], I),
+    "kv_page_summaries": ([P, I, P, I, I, I, I, I, P, P, SZ, P], I),
+    "kv_summarize_last_pages": ([P, I, P, I, P, P, I, I, I, I, I, P, P, SZ, P], I),
+    "kv_score_pages": ([P, P, I, P, I, P, P, I, I, I, I, P, P, SZ, P], I),
+    "kv_select_workspace_size": ([I, I], SZ),
+    "kv_select_pages": ([P, P, P, P, I, I, I, I, I, F, F, I, P, P, P, P, P, SZ, P], I),
+    "kv_compact_workspace_size": ([I, I, I, I], SZ),
+    "kv_compact": ([P, I, P, P, I, P, P, I, P, P, I, I, I, I, I, P, SZ, P], I),
+    "kv_append_workspace_size": ([I], SZ),
+    "kv_append": ([P, P, P, P, I, P, I, P, P, P, I, I, I, I, I, P, SZ, P], I),
+}
+
+
+def _declare(L):
+    for name, (args, res) in _SIGS.items():
+        fn = getattr(L, name, None)
+        if fn is None:
+            continue
+        fn.argtypes = args
+        fn.restype = res
+
+
+def _p(x):
+    if x is None:
+        return None
+    if isinstance(x, int):
+        return x
+    if isinstance(x, torch.Tensor):
+        return x.data_ptr()
+    raise TypeError(f"expected a tensor or an address, got {type(x)}")
+
+
+def _s(stream):
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def _check(rc, what):
+    if rc != KV_OK:
+        raise KVError(rc, what)
+
+
+def dtype_code(t) -> int:
+    dt = t.dtype if isinstance(t, torch.Tensor) else t
+    if dt == torch.float16:
+        return KV_F16
+    if dt == torch.bfloat16:
+        return KV_BF16
+    raise TypeError(f"unsupported element type {dt}")
+
+
+def status_string(code: int) -> str:
+    return lib().kv_status_string(int(code)).decode()
+
+
+# ---------------------------------------------------------------- workspace
+def alloc_workspace(nbytes: int, device="cuda") -> torch.Tensor:
+    """Zeroed device buffer usable as a workspace (torch allocations are
+    at least 256-byte aligned)."""
+    ws = torch.zeros(max(int(nbytes), 256), dtype=torch.uint8, device=device)
+    assert ws.data_ptr() % 256 == 0
+    return ws
+
+
+def kv_status_workspace_size() -> int:
+    return lib().kv_status_workspace_size()
+
+
+def kv_workspace_reset(ws, stream=None):
+    _check(lib().kv_workspace_reset(_p(ws), _s(stream)), "kv_workspace_reset")
+
+
+def kv_get_status(ws, stream=None) -> int:
+    return lib().kv_get_status(_p(ws), _s(stream))
+
+
+def check_status(ws, stream=None, what="device"):
+    rc = kv_get_status(ws, stream)
+    _check(rc, what)
+
+
+# ---------------------------------------------------------------- decode
+def kv_decode_num_workers(Hq, Hkv, d, page_size=16, dtype=KV_F16) -> int:
+    n = lib().kv_decode_num_workers(Hq, Hkv, d, page_size, dtype)
+    if n < 0:
+        raise KVError(n, "kv_decode_num_workers")
+    return n
+
+
+def kv_decode_workspace_size(B, Hq, Hkv, d, max_pages, page_size=16, pages_per_split=0) -> int:
+    return lib().kv_decode_workspace_size(B, Hq, Hkv, d, max_pages, page_size, pages_per_split)
+
+
+def kv_decode(q, k_pool, v_pool, block_table, seq_lens, scale, out, lse, ws,
+              pages_per_split=0, stream=None, *, num_pages=None, dtype=None):
+    """q [B,Hq,d], pools [P,Hkv,16,d] (f16/bf16), block_table [B,maxP] int32,
+    seq_lens [B] int32, out [B,Hq,d] f32, lse [B,Hq] f32, ws from
+    alloc_workspace(kv_decode_workspace_size(...))."""
+    B, Hq, d = q.shape
+    P_, Hkv, ps, _ = k_pool.shape
+    rc = lib().kv_decode(_p(q), _p(k_pool), _p(v_pool), int(num_pages if num_pages is not None else P_),
+                         _p(block_table), block_table.shape[1], _p(seq_lens), B, ps, Hq, Hkv, d,
+                         dtype_code(q) if dtype is None else dtype, float(scale),
+                         int(pages_per_split), _p(out), _p(lse), _p(ws), ws.numel(), _s(stream))
+    _check(rc, "kv_decode")
+
+
+def kv_decode_hostio_workspace_size(B, Hq, Hkv, d, max_pages, page_size=16, pages_per_split=0):
+    return lib().kv_decode_hostio_workspace_size(B, Hq, Hkv, d, max_pages, page_size,
+                                                 pages_per_split)
+
+
+def kv_decode_hostio(h_q, k_pool, v_pool, h_block_table, h_seq_lens, scale, h_out, h_lse, ws,
+                     pages_per_split=0, stream=None):
+    """Like kv_decode with q, block_table, seq_lens, out and lse in (pinned) host memory."""
+    B, Hq, d = h_q.shape
+    P_, Hkv, ps, _ = k_pool.shape
+    rc = lib().kv_decode_hostio(_p(h_q), _p(k_pool), _p(v_pool), P_, _p(h_block_table),
+                                h_block_table.shape[1], _p(h_seq_lens), B, ps, Hq, Hkv, d,
+                                dtype_code(k_pool), float(scale), int(pages_per_split), _p(h_out),
+                                _p(h_lse), _p(ws), ws.numel(), _s(stream))
+    _check(rc, "kv_decode_hostio")
+
+
+def kv_profile_next_decode(event_before, event_after):
+    """Arm CUDA events (torch.cuda.Event) around the next decode's attention kernel."""
+    ev0 = event_before.cuda_event if event_before is not None else None
+    ev1 = event_after.cuda_event if event_after is not None else None
+    _check(lib().kv_profile_next_decode(ev0, ev1), "kv_profile_next_decode")
+
+
+def kv_workqueue_workspace_size(B) -> int:
+    return lib().kv_workqueue_workspace_size(B)
+
+
+def kv_build_workqueue(seq_lens, Hkv, page_size, max_pages, pages_per_split, n_workers, tasks,
+                       chunk_begin, seq_group_begin, seq_nsplit, meta, ws, stream=None):
+    rc = lib().kv_build_workqueue(_p(seq_lens), seq_lens.numel(), Hkv, page_size, max_pages,
+                                  pages_per_split, n_workers, _p(tasks), tasks.shape[0],
+                                  _p(chunk_begin), chunk_begin.numel(), _p(seq_group_begin),
+                                  _p(seq_nsplit), _p(meta), _p(ws), _s(stream))
+    _check(rc, "kv_build_workqueue")
+
+
+# ---------------------------------------------------------------- budgeting
+def kv_update_query_summaries(q, Hkv, a_fast, a_slow, first, ema, stream=None):
+    B, Hq, d = q.shape
+    rc = lib().kv_update_query_summaries(_p(q), B, Hq, Hkv, d, dtype_code(q), float(a_fast),
+                                         float(a_slow), int(bool(first)), _p(ema), _s(stream))
+    _check(rc, "kv_update_query_summaries")
+
+
+def kv_mark_active(seq_lens, budget, page_size, mode, active, stream=None):
+    rc = lib().kv_mark_active(_p(seq_lens), _p(budget), seq_lens.numel(), page_size, int(mode),
+                              _p(active), _s(stream))
+    _check(rc, "kv_mark_active")
+
+
+def kv_page_summaries(k_pool, page_ids, summ, ws, stream=None):
+    P_, Hkv, ps, d = k_pool.shape
+    rc = lib().kv_page_summaries(_p(k_pool), P_, _p(page_ids), page_ids.numel(), Hkv, ps, d,
+                                 dtype_code(k_pool), _p(summ), _p(ws), ws.numel(), _s(stream))
+    _check(rc, "kv_page_summaries")
+
+
+def kv_summarize_last_pages(k_pool, block_table, seq_lens, active, summ, ws, stream=None):
+    P_, Hkv, ps, d = k_pool.shape
+    B, maxp = block_table.shape
+    rc = lib().kv_summarize_last_pages(_p(k_pool), P_, _p(block_table), maxp, _p(seq_lens),
+                                       _p(active), B, Hkv, ps, d, dtype_code(k_pool), _p(summ),
+                                       _p(ws), ws.numel(), _s(stream))
+    _check(rc, "kv_summarize_last_pages")
+
+
+def kv_score_pages(query_summaries, page_key_summaries, block_table, seq_lens, active, scores, ws,
+                   page_size=16, stream=None):
+    B, _, Hkv, d = query_summaries.shape
+    P_ = page_key_summaries.shape[0]
+    maxp = block_table.shape[1]
+    rc = lib().kv_score_pages(_p(query_summaries), _p(page_key_summaries), P_, _p(block_table),
+                              maxp, _p(seq_lens), _p(active), B, Hkv, d, page_size, _p(scores),
+                              _p(ws), ws.numel(), _s(stream))
+    _check(rc, "kv_score_pages")
+
+
+def kv_select_workspace_size(B, max_pages) -> int:
+    return lib().kv_select_workspace_size(B, max_pages)
+
+
+def kv_select_pages(scores, seq_lens, active, budget, n_first, n_last, delta, ws_frac, mode,
+                    free_top, keep_mask, grow, drift, ws, page_size=16, stream=None):
+    B, maxp, _ = scores.shape
+    rc = lib().kv_select_pages(_p(scores), _p(seq_lens), _p(active), _p(budget), B, maxp,
+                               page_size, int(n_first), int(n_last), float(delta), float(ws_frac),
+                               int(mode), _p(free_top), _p(keep_mask), _p(grow), _p(drift),
+                               _p(ws), ws.numel(), _s(stream))
+    _check(rc, "kv_select_pages")
+
+
+def kv_compact_workspace_size(B, max_pages, page_size=16, token_granular=False) -> int:
+    return lib().kv_compact_workspace_size(B, max_pages, page_size, int(bool(token_granular)))
+
+
+def kv_compact(block_table, seq_lens, keep_mask, token_granular, k_pool, v_pool, free_list,
+               free_top, ws, stream=None):
+    B, maxp = block_table.shape
+    P_, Hkv, ps, d = k_pool.shape
+    rc = lib().kv_compact(_p(block_table), maxp, _p(seq_lens), _p(keep_mask),
+                          int(bool(token_granular)), _p(k_pool), _p(v_pool), P_, _p(free_list),
+                          _p(free_top), B, Hkv, d, ps, dtype_code(k_pool), _p(ws), ws.numel(),
+                          _s(stream))
+    _check(rc, "kv_compact")
+
+
+def kv_append_workspace_size(B) -> int:
+    return lib().kv_append_workspace_size(B)
+
+
+def kv_append(k_new, v_new, k_pool, v_pool, block_table, seq_lens, free_list, free_top, ws,
+              stream=None):
+    B, Hkv, d = k_new.shape
+    P_, _, ps, _ = k_pool.shape
+    rc = lib().kv_append(_p(k_new), _p(v_new), _p(k_pool), _p(v_pool), P_, _p(block_table),
+                         block_table.shape[1], _p(seq_lens), _p(free_list), _p(free_top), B, Hkv,
+                         d, ps, dtype_code(k_pool), _p(ws), ws.numel(), _s(stream))
+    _check(rc, "kv_append")
