@@ -348,3 +348,28 @@ def build_variant(src_text: str, out_path: str) -> str:
 def source() -> str:
     with open(_SRC) as f:
         return f.read()
+
+
+def compact_inplace(table, seq_lens, keep, token_granular, k_pool, v_pool, free_list, free_top_arr,
+                    Hkv, d, ps):
+    """or_compact on the caller's arrays (all C-contiguous, right dtypes);
+    free_top_arr is a 1-element int32 array.  Returns the status."""
+    for a, dt in ((table, np.int32), (seq_lens, np.int32), (keep, np.uint8), (k_pool, np.uint16),
+                  (v_pool, np.uint16), (free_list, np.int32), (free_top_arr, np.int32)):
+        assert a.dtype == dt and a.flags.c_contiguous
+    B, maxp = table.shape
+    return lib().or_compact(_p(table), maxp, _p(seq_lens), _p(keep), int(token_granular),
+                            _p(k_pool), _p(v_pool), k_pool.shape[0], _p(free_list),
+                            _p(free_top_arr), B, Hkv, d, ps)
+
+
+def append_inplace(k_new, v_new, k_pool, v_pool, table, seq_lens, free_list, free_top_arr,
+                   Hkv, d, ps):
+    """or_append on the caller's arrays.  Returns the status."""
+    for a, dt in ((table, np.int32), (seq_lens, np.int32), (k_pool, np.uint16),
+                  (v_pool, np.uint16), (free_list, np.int32), (free_top_arr, np.int32)):
+        assert a.dtype == dt and a.flags.c_contiguous
+    B, maxp = table.shape
+    return lib().or_append(_p(_c(k_new, np.uint16)), _p(_c(v_new, np.uint16)), _p(k_pool),
+                           _p(v_pool), k_pool.shape[0], _p(table), maxp, _p(seq_lens),
+                           _p(free_list), _p(free_top_arr), B, Hkv, d, ps)

@@ -1,0 +1,120 @@
+"""GrowPage-style budgeted decode step, as a sequence of C-ABI calls.
+
+GrowPage (mlsanity.com, "GrowPage: On-Demand KV Budgeting ...", Abstract):
+dual-timescale query summaries; at every capacity boundary either compress
+the KV states inside the current allocation or take one more physical page
+when the recent attention working set has moved beyond the long-term one.
+This module only orders the library's kernels on one stream; it does no
+arithmetic itself.
+
+Per-step order (this library's reading):
+  1. query EMAs with q_t (step 0: initialised from q_0 by `fit`);
+  2. capacity boundary = last page full and the sequence holds its budget:
+     summarise the page that just filled, score the resident pages, select
+     (grow by one page, or keep the forced pages plus the best n-1-|F|),
+     compact the block table (page granular: no K/V moves);
+  3. append the token's K/V (pops a page when the last one is full);
+  4. decode over the resident tokens.
+`fit` is the start: every sequence above its budget is cut to it with the
+same top-k rule before the first step.
+"""
+from __future__ import annotations
+
+import dataclasses
+
+import torch
+
+from . import kv
+
+
+@dataclasses.dataclass
+class BudgetConfig:
+    a_fast: float = 0.9
+    a_slow: float = 0.999
+    n_first: int = 2
+    n_last: int = 2
+    delta: float = 0.5
+    ws_frac: float = 0.5
+
+
+class BudgetedDecoder:
+    """Device state of a batch decoding under per-sequence page budgets.
+
+    k_pool, v_pool [P, Hkv, 16, d] (f16/bf16), block_table [B, maxP] int32,
+    seq_lens [B] int32, free_list [P] int32 + free_top [1] int32 (stack),
+    budget [B] int32.  All tensors live on one device and are updated in
+    place by the kernels."""
+
+    def __init__(self, k_pool, v_pool, block_table, seq_lens, free_list, free_top, budget,
+                 Hq: int, cfg: BudgetConfig, stream=None):
+        self.k_pool, self.v_pool = k_pool, v_pool
+        self.table, self.lens = block_table, seq_lens
+        self.free_list, self.free_top = free_list, free_top
+        self.budget = budget
+        self.cfg = cfg
+        self.stream = stream
+        dev = k_pool.device
+        P, Hkv, ps, d = k_pool.shape
+        B, maxp = block_table.shape
+        self.B, self.Hq, self.Hkv, self.d, self.ps, self.maxp, self.P = B, Hq, Hkv, d, ps, maxp, P
+        self.ema = torch.zeros((B, 2, Hkv, d), dtype=torch.float32, device=dev)
+        self.summ = torch.zeros((P, Hkv, 3, d), dtype=torch.float32, device=dev)
+        self.scores = torch.zeros((B, maxp, 2), dtype=torch.float32, device=dev)
+        self.active = torch.zeros(B, dtype=torch.uint8, device=dev)
+        self.keep = torch.zeros((B, maxp), dtype=torch.uint8, device=dev)
+        self.grow = torch.zeros(B, dtype=torch.uint8, device=dev)
+        self.drift = torch.zeros(B, dtype=torch.int32, device=dev)
+        self.out = torch.empty((B, Hq, d), dtype=torch.float32, device=dev)
+        self.lse = torch.empty((B, Hq), dtype=torch.float32, device=dev)
+        ws = max(kv.kv_decode_workspace_size(B, Hq, Hkv, d, maxp),
+                 kv.kv_select_workspace_size(B, maxp),
+                 kv.kv_compact_workspace_size(B, maxp),
+                 kv.kv_append_workspace_size(B))
+        self.ws = kv.alloc_workspace(ws, dev)
+        self.scale = 1.0 / (d ** 0.5)
+
+    # -- pieces ---------------------------------------------------------
+    def summarize_pages(self, page_ids):
+        kv.kv_page_summaries(self.k_pool, page_ids, self.summ, self.ws, stream=self.stream)
+
+    def update_summaries(self, q, first):
+        kv.kv_update_query_summaries(q, self.Hkv, self.cfg.a_fast, self.cfg.a_slow, first,
+                                     self.ema, stream=self.stream)
+
+    def fit(self, q0):
+        """Start of decoding: EMAs from q0, then cut every sequence that holds
+        more pages than its budget down to it (forced first/last pages kept)."""
+        c = self.cfg
+        self.update_summaries(q0, True)
+        kv.kv_mark_active(self.lens, self.budget, self.ps, 0, self.active, stream=self.stream)
+        kv.kv_score_pages(self.ema, self.summ, self.table, self.lens, self.active, self.scores,
+                          self.ws, stream=self.stream)
+        kv.kv_select_pages(self.scores, self.lens, self.active, self.budget, c.n_first, c.n_last,
+                           c.delta, c.ws_frac, kv.KV_SELECT_TOPK, self.free_top, self.keep,
+                           self.grow, self.drift, self.ws, stream=self.stream)
+        kv.kv_compact(self.table, self.lens, self.keep, False, self.k_pool, self.v_pool,
+                      self.free_list, self.free_top, self.ws, stream=self.stream)
+
+    def boundary(self):
+        """Compress-or-grow for the sequences at a capacity boundary."""
+        c = self.cfg
+        kv.kv_mark_active(self.lens, self.budget, self.ps, 1, self.active, stream=self.stream)
+        kv.kv_summarize_last_pages(self.k_pool, self.table, self.lens, self.active, self.summ,
+                                   self.ws, stream=self.stream)
+        kv.kv_score_pages(self.ema, self.summ, self.table, self.lens, self.active, self.scores,
+                          self.ws, stream=self.stream)
+        kv.kv_select_pages(self.scores, self.lens, self.active, self.budget, c.n_first, c.n_last,
+                           c.delta, c.ws_frac, kv.KV_SELECT_BOUNDARY, self.free_top, self.keep,
+                           self.grow, self.drift, self.ws, stream=self.stream)
+        kv.kv_compact(self.table, self.lens, self.keep, False, self.k_pool, self.v_pool,
+                      self.free_list, self.free_top, self.ws, stream=self.stream)
+
+    def step(self, q, k_new, v_new, t: int):
+        """One decode step for token t (q [B, Hq, d], k_new/v_new [B, Hkv, d])."""
+        if t > 0:
+            self.update_summaries(q, False)
+        self.boundary()
+        kv.kv_append(k_new, v_new, self.k_pool, self.v_pool, self.table, self.lens,
+                     self.free_list, self.free_top, self.ws, stream=self.stream)
+        kv.kv_decode(q, self.k_pool, self.v_pool, self.table, self.lens, self.scale, self.out,
+                     self.lse, self.ws, stream=self.stream)

@@ -160,6 +160,8 @@ int kv_build_workqueue(const int32_t* seq_lens, int B, int Hkv, int page_size, i
   a.seq_group_begin = seq_group_begin;
   a.seq_nsplit = seq_nsplit;
   a.seq_page_off = reinterpret_cast<long long*>(static_cast<uint8_t*>(ws) + kHeaderBytes);
+  a.scratch_np = reinterpret_cast<int32_t*>(static_cast<uint8_t*>(ws) + kHeaderBytes +
+                                            align_up((size_t)(B > 0 ? B : 1) * 8, 256));
   a.meta = meta;
   a.status = static_cast<int*>(ws);
   return launch_build_workqueue(a, static_cast<cudaStream_t>(stream)) == cudaSuccess ? KV_OK
@@ -171,6 +173,9 @@ int kv_profile_next_decode(void* event_before, void* event_after) {
   return KV_OK;
 }
 
-size_t kv_workqueue_workspace_size(int B) { return kHeaderBytes + align_up((size_t)(B > 0 ? B : 1) * 8, 256); }
+size_t kv_workqueue_workspace_size(int B) {
+  const size_t nb = (size_t)(B > 0 ? B : 1);
+  return kHeaderBytes + align_up(nb * 8, 256) + align_up(nb * 4, 256);
+}
 
 }  // extern "C"

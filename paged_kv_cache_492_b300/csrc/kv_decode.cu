@@ -442,10 +442,16 @@ __global__ void __launch_bounds__(32 * 9, 1) decode_kernel(const DecodeParams p)
   }
 }
 
-// Combine the splits of each (sequence, query head):
+// Combine the splits of each (sequence, KV head), all G query heads at once:
 //   lse = ln sum_s exp(lse_s),  out = sum_s exp(lse_s - lse) out_s.
-// Sequences with one split were written by the decode kernel; empty (or
-// invalid) sequences get out = 0, lse = -inf.
+// One CTA per (sequence, KV head).  Sequences with one split were written by
+// the decode kernel and empty ones by the workqueue builder; both are skipped.
+// Threads are (split group, float4 of the G x d outputs): each sums every
+// NSG-th split with independent loads, then the groups are added in shared
+// memory.  The per-split weights are computed once into shared memory.
+constexpr int kMergeThreads = 512;
+constexpr int kMergeMaxWeights = 4096;  // G * splits held in shared memory
+
 struct MergeParams {
   const int32_t* seq_lens;
   const int32_t* seq_group_begin;
@@ -457,43 +463,68 @@ struct MergeParams {
   int Hq, Hkv, G, d;
 };
 
-__global__ void __launch_bounds__(128) merge_kernel(const MergeParams p) {
+__global__ void __launch_bounds__(kMergeThreads) merge_kernel(const MergeParams p) {
+  __shared__ float w_sm[kMergeMaxWeights];
+  __shared__ float lse_sm[8];
+  __shared__ float4 red[kMergeThreads];
   pdl_wait();
   const int row = blockIdx.x;
-  const int b = row / p.Hq, hq = row - b * p.Hq;
-  const int h = hq / p.G, g = hq - h * p.G;
-  float* o = p.out + (size_t)row * p.d;
+  const int b = row / p.Hkv, h = row - b * p.Hkv;
   const int ns = p.seq_nsplit[b];
-  if (p.seq_lens[b] <= 0 || ns == 0) {
-    for (int c = threadIdx.x; c < p.d; c += blockDim.x) o[c] = 0.f;
-    if (threadIdx.x == 0) p.lse[row] = -INFINITY;
-    return;
-  }
-  if (ns == 1) return;
+  if (p.seq_lens[b] <= 0 || ns <= 1) return;
+  const int G = p.G, d = p.d;
   const size_t base = p.seq_group_begin[b];
-  auto lse_of = [&](int s) { return p.part_lse[((base + s) * p.Hkv + h) * p.G + g]; };
-  __shared__ float red[4];
-  float mx = -INFINITY;
-  for (int s = threadIdx.x; s < ns; s += blockDim.x) mx = fmaxf(mx, lse_of(s));
-  for (int off = 16; off; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(FULL, mx, off));
-  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = mx;
-  __syncthreads();
-  mx = fmaxf(fmaxf(red[0], red[1]), fmaxf(red[2], red[3]));
-  __syncthreads();
-  float sum = 0.f;
-  for (int s = threadIdx.x; s < ns; s += blockDim.x) sum += expf(lse_of(s) - mx);
-  for (int off = 16; off; off >>= 1) sum += __shfl_xor_sync(FULL, sum, off);
-  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = sum;
-  __syncthreads();
-  sum = red[0] + red[1] + red[2] + red[3];
-  const float lse = mx + logf(sum);
-  for (int c = threadIdx.x; c < p.d; c += blockDim.x) {
-    float acc = 0.f;
-    for (int s = 0; s < ns; ++s)
-      acc = fmaf(expf(lse_of(s) - lse), p.part_o[(((base + s) * p.Hkv + h) * p.G + g) * p.d + c], acc);
-    o[c] = acc;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  auto task = [&](int s) { return (base + s) * p.Hkv + h; };
+  // per query head of the group: the merged log-sum-exp
+  if (warp < G) {
+    const int g = warp;
+    float mx = -INFINITY;
+    for (int s = lane; s < ns; s += 32) mx = fmaxf(mx, __ldcg(p.part_lse + task(s) * G + g));
+    for (int o = 16; o; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(FULL, mx, o));
+    float sum = 0.f;
+    for (int s = lane; s < ns; s += 32) sum += expf(__ldcg(p.part_lse + task(s) * G + g) - mx);
+    for (int o = 16; o; o >>= 1) sum += __shfl_xor_sync(FULL, sum, o);
+    const float l = mx + logf(sum);
+    if (lane == 0) {
+      lse_sm[g] = l;
+      p.lse[(size_t)b * p.Hq + (size_t)h * G + g] = l;
+    }
   }
-  if (threadIdx.x == 0) p.lse[row] = lse;
+  __syncthreads();
+  const bool cached = ns * G <= kMergeMaxWeights;
+  if (cached)
+    for (int i = threadIdx.x; i < ns * G; i += blockDim.x) {
+      const int s = i / G, g = i - s * G;
+      w_sm[i] = expf(__ldcg(p.part_lse + task(s) * G + g) - lse_sm[g]);
+    }
+  __syncthreads();
+  const int F4 = G * d / 4;              // float4s per split
+  const int NSG = blockDim.x / F4;       // split groups
+  const int f = threadIdx.x % F4, sg = threadIdx.x / F4;
+  const int g = f / (d / 4);
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  if (sg < NSG) {
+#pragma unroll 4
+    for (int s = sg; s < ns; s += NSG) {
+      const float w = cached ? w_sm[s * G + g]
+                             : expf(__ldcg(p.part_lse + task(s) * G + g) - lse_sm[g]);
+      const float4 v = __ldcg(reinterpret_cast<const float4*>(p.part_o + task(s) * G * d) + f);
+      acc.x = fmaf(w, v.x, acc.x);
+      acc.y = fmaf(w, v.y, acc.y);
+      acc.z = fmaf(w, v.z, acc.z);
+      acc.w = fmaf(w, v.w, acc.w);
+    }
+  }
+  red[threadIdx.x] = acc;
+  __syncthreads();
+  if (sg == 0) {
+    for (int k = 1; k < NSG; ++k) {
+      const float4 v = red[k * F4 + f];
+      acc.x += v.x; acc.y += v.y; acc.z += v.z; acc.w += v.w;
+    }
+    reinterpret_cast<float4*>(p.out + ((size_t)b * p.Hq + (size_t)h * G) * d)[f] = acc;
+  }
 }
 
 using DecodeFn = void (*)(const DecodeParams);
@@ -611,6 +642,7 @@ DecodeLayout decode_layout(int B, int Hq, int Hkv, int d, int max_pages, int pag
   L.seq_group_begin = take((size_t)B * 4);
   L.seq_nsplit = take((size_t)B * 4);
   L.seq_page_off = take((size_t)B * 8);
+  L.scratch_np = take((size_t)B * 4);
   L.meta = take(64);
   L.part_o = take((size_t)L.max_tasks * G * d * 4);
   L.part_lse = take((size_t)L.max_tasks * G * 4);
@@ -656,8 +688,13 @@ int decode_launch(const void* q, const void* k_pool, const void* v_pool, int num
   wa.seq_group_begin = reinterpret_cast<int32_t*>(w + L.seq_group_begin);
   wa.seq_nsplit = reinterpret_cast<int32_t*>(w + L.seq_nsplit);
   wa.seq_page_off = reinterpret_cast<long long*>(w + L.seq_page_off);
+  wa.scratch_np = reinterpret_cast<int32_t*>(w + L.scratch_np);
   wa.meta = reinterpret_cast<int32_t*>(w + L.meta);
   wa.status = status;
+  wa.out = out;
+  wa.lse = lse;
+  wa.Hq = Hq;
+  wa.d = d;
   if (launch_build_workqueue(wa, stream) != cudaSuccess) return KV_ECUDA;
 
   DecodeParams dp{};
@@ -715,8 +752,8 @@ int decode_launch(const void* q, const void* k_pool, const void* v_pool, int num
   mp.G = Hq / Hkv;
   mp.d = d;
   cudaLaunchConfig_t mcfg{};
-  mcfg.gridDim = dim3((unsigned)((long long)B * Hq));
-  mcfg.blockDim = dim3(128);
+  mcfg.gridDim = dim3((unsigned)((long long)B * Hkv));
+  mcfg.blockDim = dim3(kMergeThreads);
   mcfg.stream = stream;
   mcfg.attrs = attr;
   mcfg.numAttrs = 1;

@@ -10,6 +10,9 @@
 
 namespace kvb {
 
+// Batches up to this many sequences keep the builder's arrays in shared memory.
+constexpr int kSmemSeqs = 2048;
+
 struct WorkqueueArgs {
   const int32_t* seq_lens;
   int B, Hkv, page_size, max_pages;
@@ -22,11 +25,18 @@ struct WorkqueueArgs {
   long long max_chunks;
   int32_t* seq_group_begin;  // [B]
   int32_t* seq_nsplit;       // [B]
-  long long* seq_page_off;   // [B] scratch
+  long long* seq_page_off;   // [B] scratch (used when B > kSmemSeqs)
+  int32_t* scratch_np;       // [B] scratch (used when B > kSmemSeqs)
   int32_t* meta;             // [5]
   int* status;
+  // decode call only (NULL otherwise)
+  int32_t* row_done;  // [B * Hkv] split-merge completion counters, zeroed here
+  float* out;         // [B][Hq][d]: rows of empty sequences set to 0
+  float* lse;         // [B][Hq]:    rows of empty sequences set to -inf
+  int Hq, d;
 };
 
+size_t workqueue_smem_bytes(int B);
 cudaError_t launch_build_workqueue(const WorkqueueArgs& a, cudaStream_t stream);
 
 // Smallest automatic split (pages): keeps merge traffic small on tiny batches.
@@ -34,8 +44,8 @@ constexpr int kMinChunk = 8;
 
 // Decode workspace layout (offsets from the start of the workspace).
 struct DecodeLayout {
-  size_t tasks, chunk_begin, seq_group_begin, seq_nsplit, seq_page_off, meta, part_o, part_lse,
-      total;
+  size_t tasks, chunk_begin, seq_group_begin, seq_nsplit, seq_page_off, scratch_np, row_done,
+      meta, part_o, part_lse, total;
   long long max_tasks, max_chunks;
 };
 DecodeLayout decode_layout(int B, int Hq, int Hkv, int d, int max_pages, int page_size,

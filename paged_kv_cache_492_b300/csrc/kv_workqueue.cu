@@ -1,7 +1,7 @@
 // Device-side builder of the decode workqueue: the non-empty
 // (sequence, KV-head, split) tasks of one decode step (PersistentKV,
-// aissential.tech -- Summary and Method: "compact workqueue ... executes only
-// non-empty tasks").
+// aissential.tech -- Summary and Method: a compact workqueue that executes
+// only non-empty tasks).
 //
 // Split rule (this library's): the batch's non-empty pages are laid end to
 // end (sequence offsets O_b), the range is cut into chunks of `chunk` pages
@@ -9,6 +9,13 @@
 // (ceil(W / workers), at least min_chunk) every decode worker streams the same
 // number of pages whatever the length mix, and a sequence is split only where
 // a worker boundary falls inside it.
+//
+// One CTA builds the whole queue.  Per-sequence arrays live in shared memory
+// for batches up to kSmemSeqs sequences (global scratch beyond), so the build
+// costs one read of seq_lens plus a few block-wide scans.  For a decode call it
+// also zeroes the per-(sequence, KV head) completion counters the decode
+// kernel's split merge uses, and writes out = 0 / lse = -inf for sequences
+// with no tokens (the decode kernel never visits them).
 #include "kv_internal.h"
 
 namespace kvb {
@@ -45,12 +52,13 @@ __device__ long long block_exclusive_scan(long long v, long long* out_excl, long
   return total;
 }
 
-// Largest b with sgb[b] <= gi (that sequence owns group gi; see builder).
-__device__ int owner_of_group(const int32_t* sgb, int B, long long gi) {
+// Largest b with gbeg[b] <= gi: the sequence that owns group gi (sequences
+// without splits share their successor's begin and are skipped over).
+__device__ int owner_of_group(const int32_t* gbeg, int B, long long gi) {
   int lo = 0, hi = B - 1;
   while (lo < hi) {
     int mid = (lo + hi + 1) >> 1;
-    if (sgb[mid] <= gi) lo = mid; else hi = mid - 1;
+    if (gbeg[mid] <= gi) lo = mid; else hi = mid - 1;
   }
   return lo;
 }
@@ -59,19 +67,30 @@ __global__ void __launch_bounds__(kWqThreads, 1) build_workqueue_kernel(Workqueu
   // The decode kernel that follows may start its prologue now; it waits for
   // this grid to finish before reading the queue.
   pdl_launch_dependents();
+  extern __shared__ long long wq_dyn[];
   __shared__ long long sm[32];
   const int tid = threadIdx.x, nth = blockDim.x;
+  const bool in_smem = a.B <= kSmemSeqs;
+  int32_t* np_arr = in_smem ? reinterpret_cast<int32_t*>(wq_dyn) : a.scratch_np;
+  int32_t* gbeg = in_smem ? np_arr + a.B : a.seq_group_begin;
+  int32_t* nspl = in_smem ? gbeg + a.B : a.seq_nsplit;
+  long long* poff = in_smem ? reinterpret_cast<long long*>(wq_dyn) + ceil_div(3 * a.B, 2) + 1
+                            : a.seq_page_off;
   const int per = ceil_div(a.B, nth);
   const int b0 = min(a.B, tid * per), b1 = min(a.B, b0 + per);
 
-  // pass 1: pages per sequence, page offsets
+  // pass 1: pages per sequence (0 for an invalid length), page offsets
   long long my_pages = 0;
   bool bad = false;
   for (int b = b0; b < b1; ++b) {
-    int L = a.seq_lens[b];
+    const int L = a.seq_lens[b];
     long long np = L > 0 ? ceil_div_ll(L, a.page_size) : 0;
-    if (L < 0 || np > a.max_pages) bad = true;
-    my_pages += (L < 0 || np > a.max_pages) ? 0 : np;
+    if (L < 0 || np > a.max_pages) {
+      bad = true;
+      np = 0;
+    }
+    np_arr[b] = (int32_t)np;
+    my_pages += np;
   }
   if (bad) set_status(a.status, KV_EINVAL);
   long long page_off;
@@ -86,10 +105,11 @@ __global__ void __launch_bounds__(kWqThreads, 1) build_workqueue_kernel(Workqueu
   {
     long long O = page_off;
     for (int b = b0; b < b1; ++b) {
-      int L = a.seq_lens[b];
-      long long np = L > 0 ? ceil_div_ll(L, a.page_size) : 0;
-      if (L < 0 || np > a.max_pages) np = 0;
-      if (np > 0) my_groups += (O + np - 1) / chunk - O / chunk + 1;
+      const long long np = np_arr[b];
+      const long long ns = np > 0 ? (O + np - 1) / chunk - O / chunk + 1 : 0;
+      poff[b] = O;
+      nspl[b] = (int32_t)ns;
+      my_groups += ns;
       O += np;
     }
   }
@@ -101,17 +121,29 @@ __global__ void __launch_bounds__(kWqThreads, 1) build_workqueue_kernel(Workqueu
   const bool overflow = T > a.max_tasks || nchunks + 1 > a.max_chunks ||
                         W > 0x7fffffffll || G_total > 0x7fffffffll;
   {
-    long long O = page_off, gofs = group_off;
+    long long g = group_off;
     for (int b = b0; b < b1; ++b) {
-      int L = a.seq_lens[b];
-      long long np = L > 0 ? ceil_div_ll(L, a.page_size) : 0;
-      if (L < 0 || np > a.max_pages) np = 0;
-      long long ns = np > 0 ? (O + np - 1) / chunk - O / chunk + 1 : 0;
-      a.seq_group_begin[b] = overflow ? 0 : (int32_t)gofs;
-      a.seq_nsplit[b] = overflow ? 0 : (int32_t)ns;
-      a.seq_page_off[b] = O;
-      gofs += ns;
-      O += np;
+      const int ns = nspl[b];
+      gbeg[b] = (int32_t)g;
+      if (in_smem) {
+        a.seq_group_begin[b] = overflow ? 0 : (int32_t)g;
+        a.seq_nsplit[b] = overflow ? 0 : ns;
+      } else if (overflow) {
+        gbeg[b] = 0;
+        nspl[b] = 0;
+      }
+      g += ns;
+    }
+  }
+  // decode only: completion counters of the split merge, empty-sequence outputs
+  if (a.row_done)
+    for (long long i = tid; i < (long long)a.B * a.Hkv; i += nth) a.row_done[i] = 0;
+  if (a.out) {
+    const int per_seq = a.Hq * a.d;
+    for (int b = 0; b < a.B; ++b) {
+      if (np_arr[b] != 0 && !overflow) continue;
+      for (int i = tid; i < per_seq; i += nth) a.out[(size_t)b * per_seq + i] = 0.f;
+      for (int i = tid; i < a.Hq; i += nth) a.lse[(size_t)b * a.Hq + i] = -INFINITY;
     }
   }
   __syncthreads();  // sequence arrays visible to the whole block
@@ -128,17 +160,16 @@ __global__ void __launch_bounds__(kWqThreads, 1) build_workqueue_kernel(Workqueu
   for (long long ti = tid; ti < T; ti += nth) {
     const long long gi = ti / a.Hkv;
     const int h = (int)(ti - gi * a.Hkv);
-    const int b = owner_of_group(a.seq_group_begin, a.B, gi);
-    const int s = (int)(gi - a.seq_group_begin[b]);
-    const int L = a.seq_lens[b];
-    const long long np = ceil_div_ll(L, a.page_size);
-    const long long O = a.seq_page_off[b];
+    const int b = owner_of_group(gbeg, a.B, gi);
+    const int s = (int)(gi - gbeg[b]);
+    const long long np = np_arr[b];
+    const long long O = poff[b];
     const long long c = O / chunk + s;
     const long long lo = max(O, c * chunk) - O;
     const long long hi = min(O + np, (c + 1) * chunk) - O;
     int4* rec = reinterpret_cast<int4*>(a.tasks + ti * 8);
-    rec[0] = make_int4(b, h, s, a.seq_nsplit[b]);
-    rec[1] = make_int4((int)lo, (int)hi, (int)c, L);
+    rec[0] = make_int4(b, h, s, nspl[b]);
+    rec[1] = make_int4((int)lo, (int)hi, (int)c, a.seq_lens[b]);
     if (h == 0) {
       // chunk c' starts at this group for every c' in (cidx(gi-1), c]
       long long prev;
@@ -147,10 +178,8 @@ __global__ void __launch_bounds__(kWqThreads, 1) build_workqueue_kernel(Workqueu
       } else if (s > 0) {
         prev = c - 1;
       } else {
-        const int pb = owner_of_group(a.seq_group_begin, a.B, gi - 1);
-        const long long pO = a.seq_page_off[pb];
-        const long long pnp = ceil_div_ll(a.seq_lens[pb], a.page_size);
-        prev = (pO + pnp - 1) / chunk;
+        const int pb = owner_of_group(gbeg, a.B, gi - 1);
+        prev = (poff[pb] + np_arr[pb] - 1) / chunk;
       }
       for (long long cc = prev + 1; cc <= c; ++cc) a.chunk_begin[cc] = (int32_t)gi;
     }
@@ -167,8 +196,12 @@ __global__ void __launch_bounds__(kWqThreads, 1) build_workqueue_kernel(Workqueu
 
 }  // namespace
 
+size_t workqueue_smem_bytes(int B) {
+  return B <= kSmemSeqs ? ((size_t)ceil_div(3 * B, 2) + 1 + B) * 8 : 0;
+}
+
 cudaError_t launch_build_workqueue(const WorkqueueArgs& a, cudaStream_t stream) {
-  build_workqueue_kernel<<<1, kWqThreads, 0, stream>>>(a);
+  build_workqueue_kernel<<<1, kWqThreads, workqueue_smem_bytes(a.B), stream>>>(a);
   return cudaGetLastError();
 }
 

@@ -1,0 +1,326 @@
+"""GPU parity of the budgeting kernels against the oracle: bit-exact for
+every integer decision and every fp32 value that feeds one."""
+import os
+
+import numpy as np
+import pytest
+import torch
+
+from oracle import oracle as O
+from paged_kv_cache_492_b300 import budget as BG
+from paged_kv_cache_492_b300 import kv
+from paged_kv_cache_492_b300 import workloads as W
+from tests.budget_oracle import OracleBudget
+from tests.gpu_util import DeviceDecode, assert_decode_close, bits_to_dev, i32
+
+pytestmark = pytest.mark.gpu
+NCPU = len(os.sched_getaffinity(0))
+DEV = "cuda"
+
+
+def f32(a):
+    return torch.from_numpy(np.ascontiguousarray(a, dtype=np.float32)).to(DEV)
+
+
+def u8(a):
+    return torch.from_numpy(np.ascontiguousarray(a, dtype=np.uint8)).to(DEV)
+
+
+@pytest.mark.parametrize("dtype", [W.F16, W.BF16])
+@pytest.mark.parametrize("G,d", [(4, 128), (4, 64), (1, 128), (8, 64)])
+def test_ema_bit_exact(dtype, G, d):
+    rng = np.random.default_rng(1)
+    B, Hkv = 5, 2
+    Hq = G * Hkv
+    ema_ref = np.zeros((B, 2, Hkv, d), np.float32)
+    ema = torch.zeros((B, 2, Hkv, d), dtype=torch.float32, device=DEV)
+    for t in range(6):
+        q = W.normal_bits(rng, (B, Hq, d), dtype)
+        O.ema_f32(q, B, Hq, Hkv, d, dtype, 0.9, 0.999, t == 0, ema_ref)
+        kv.kv_update_query_summaries(bits_to_dev(q, dtype), Hkv, 0.9, 0.999, t == 0, ema)
+    assert np.array_equal(ema.cpu().numpy(), ema_ref)
+
+
+def test_mark_active_exact():
+    rng = np.random.default_rng(2)
+    lens = rng.integers(0, 5000, size=300).astype(np.int32)
+    lens[::7] = (lens[::7] // 16) * 16
+    bud = rng.integers(0, 300, size=300).astype(np.int32)
+    act = torch.zeros(300, dtype=torch.uint8, device=DEV)
+    for mode in (0, 1):
+        kv.kv_mark_active(i32(lens), i32(bud), 16, mode, act)
+        assert np.array_equal(act.cpu().numpy(), O.mark_active(lens, bud, 16, mode))
+
+
+@pytest.mark.parametrize("dtype", [W.F16, W.BF16])
+def test_page_summaries_bit_exact(dtype):
+    rng = np.random.default_rng(3)
+    P, Hkv, d = 40, 8, 128
+    kp = W.normal_bits(rng, (P, Hkv, 16, d), dtype)
+    ids = rng.permutation(P)[:17].astype(np.int32)
+    ref = np.zeros((P, Hkv, 3, d), np.float32)
+    O.page_summaries_f32(kp, ids, Hkv, 16, d, dtype, ref)
+    summ = torch.zeros((P, Hkv, 3, d), dtype=torch.float32, device=DEV)
+    ws = kv.alloc_workspace(256)
+    kdev = bits_to_dev(kp, dtype)
+    kv.kv_page_summaries(kdev, i32(ids), summ, ws)
+    assert kv.kv_get_status(ws) == 0
+    assert np.array_equal(summ.cpu().numpy(), ref)
+    # last full page of active sequences
+    table = rng.permutation(P)[:24].reshape(3, 8).astype(np.int32)
+    lens = np.array([32, 100, 128], np.int32)
+    act = np.array([1, 1, 0], np.uint8)
+    summ.zero_()
+    kv.kv_summarize_last_pages(kdev, i32(table), i32(lens), u8(act), summ, ws)
+    ref2 = np.zeros_like(ref)
+    O.page_summaries_f32(kp, np.array([table[0, 1], table[1, 5]], np.int32), Hkv, 16, d, dtype, ref2)
+    assert np.array_equal(summ.cpu().numpy(), ref2)
+    # a bad id is reported, nothing read out of bounds
+    kv.kv_page_summaries(kdev, i32([0, P + 3]), summ, ws)
+    assert kv.kv_get_status(ws) == kv.KV_EBADPAGE
+
+
+@pytest.mark.parametrize("d", [128, 64])
+def test_scores_bit_exact(d):
+    rng = np.random.default_rng(4)
+    B, Hkv, P, maxp = 6, 8, 60, 9
+    ema = rng.standard_normal((B, 2, Hkv, d)).astype(np.float32)
+    kp = W.normal_bits(rng, (P, Hkv, 16, d), W.BF16)
+    summ = np.zeros((P, Hkv, 3, d), np.float32)
+    O.page_summaries_f32(kp, np.arange(P, dtype=np.int32), Hkv, 16, d, W.BF16, summ)
+    lens = np.array([0, 1, 16, 17, 140, 144], np.int32)
+    table = np.full((B, maxp), -1, np.int32)
+    perm = rng.permutation(P)
+    pos = 0
+    for b, L in enumerate(lens):
+        n = -(-int(L) // 16)
+        table[b, :n] = perm[pos:pos + n]
+        pos += n
+    act = np.array([1, 1, 1, 0, 1, 1], np.uint8)
+    ref = np.full((B, maxp, 2), 7.0, np.float32)
+    O.score_pages_f32(ema, summ, table, lens, act, Hkv, d, 16, ref)
+    sc = torch.full((B, maxp, 2), 7.0, dtype=torch.float32, device=DEV)
+    ws = kv.alloc_workspace(256)
+    kv.kv_score_pages(f32(ema), f32(summ), i32(table), i32(lens), u8(act), sc, ws)
+    assert kv.kv_get_status(ws) == 0
+    got = sc.cpu().numpy()
+    assert np.array_equal(got, ref)
+    # and the fp32 scores sit within rounding of the fp64 definition
+    r64 = np.zeros((B, maxp, 2))
+    O.score_pages_f64(ema.astype(np.float64), summ.astype(np.float64), table, lens, act, Hkv, d,
+                      16, r64)
+    fin = np.isfinite(ref) & (ref != 7.0)
+    assert np.allclose(got[fin], r64[fin], rtol=1e-4, atol=1e-3)
+
+
+def _run_select(scores, lens, act, budget, mode, free_top, n_first=2, n_last=2, delta=0.5,
+                ws_frac=0.5):
+    B, maxp, _ = scores.shape
+    keep = torch.zeros((B, maxp), dtype=torch.uint8, device=DEV)
+    grow = torch.zeros(B, dtype=torch.uint8, device=DEV)
+    drift = torch.zeros(B, dtype=torch.int32, device=DEV)
+    bud = i32(budget)
+    ws = kv.alloc_workspace(kv.kv_select_workspace_size(B, maxp))
+    kv.kv_select_pages(f32(scores), i32(lens), None if act is None else u8(act), bud, n_first,
+                       n_last, delta, ws_frac, mode, i32([free_top]), keep, grow, drift, ws)
+    assert kv.kv_get_status(ws) == 0
+    return keep.cpu().numpy(), grow.cpu().numpy(), bud.cpu().numpy(), drift.cpu().numpy()
+
+
+@pytest.mark.parametrize("trial", range(6))
+def test_select_bit_exact(trial):
+    rng = np.random.default_rng(10 + trial)
+    B, maxp = 12, 300
+    lens = rng.integers(0, maxp * 16, size=B).astype(np.int32)
+    lens[:4] = (lens[:4] // 16) * 16
+    sc = rng.standard_normal((B, maxp, 2)).astype(np.float32)
+    if trial % 2:
+        sc = np.round(sc * 2) / 2          # many exact ties
+    if trial == 3:
+        sc[:, :, 1] = sc[:, :, 0]          # no drift
+    act = (rng.random(B) < 0.7).astype(np.uint8)
+    budget = rng.integers(0, 200, size=B).astype(np.int32)
+    for mode, free in ((O.SELECT_TOPK, 0), (O.SELECT_BOUNDARY, 2), (O.SELECT_BOUNDARY, 100)):
+        for ws_frac, delta in ((0.5, 0.5), (0.25, 0.3)):
+            ref = O.select_pages(sc, lens, act, budget, 16, 2, 2, delta, mode, free, ws_frac=ws_frac)
+            got = _run_select(sc, lens, act, budget, mode, free, delta=delta, ws_frac=ws_frac)
+            for r, g, name in zip(ref, got, ("keep", "grow", "budget", "drift")):
+                assert np.array_equal(r, g), (name, mode, free)
+
+
+def _compact_case(seed, token_granular, free_top=None):
+    rng = np.random.default_rng(seed)
+    B = 5
+    lens = rng.integers(0, 200, size=B).astype(np.int32)
+    lens[0] = 0
+    x = W.small_decode(seed, B, 8, 2, 64, lens.tolist(), pool_factor=3.0, pad_pages=2)
+    width = x.max_pages * (16 if token_granular else 1)
+    keep = (rng.random((B, width)) < 0.55).astype(np.uint8)
+    top = x.free_top if free_top is None else free_top
+    return x, keep, top
+
+
+@pytest.mark.parametrize("seed,token_granular", [(1, False), (2, False), (3, True), (4, True),
+                                                 (5, True)])
+def test_compact_bit_exact(seed, token_granular):
+    x, keep, top = _compact_case(seed, token_granular)
+    ref = O.compact(x.block_table, x.seq_lens, keep, token_granular, x.k_pool, x.v_pool,
+                    x.free_list, top, x.Hkv, x.d, 16)
+    assert ref[-1] == 0
+    dd = DeviceDecode(x)
+    fl = i32(x.free_list)
+    ft = i32([top])
+    ws = kv.alloc_workspace(kv.kv_compact_workspace_size(x.B, x.max_pages, 16, token_granular))
+    kv.kv_compact(dd.table, dd.lens, u8(keep), token_granular, dd.k, dd.v, fl, ft, ws)
+    assert kv.kv_get_status(ws) == 0
+    t, sl, kp, vp, fl_ref, top_ref, _ = ref
+    assert np.array_equal(dd.table.cpu().numpy(), t)
+    assert np.array_equal(dd.lens.cpu().numpy(), sl)
+    assert int(ft.item()) == top_ref
+    assert np.array_equal(fl.cpu().numpy()[:top_ref], fl_ref[:top_ref])
+    assert np.array_equal(dd.k.view(torch.int16).cpu().numpy().view(np.uint16), kp)
+    assert np.array_equal(dd.v.view(torch.int16).cpu().numpy().view(np.uint16), vp)
+
+
+def test_compact_no_space_changes_nothing():
+    x, keep, _ = _compact_case(7, True)
+    dd = DeviceDecode(x)
+    t0 = dd.table.clone()
+    fl = i32(x.free_list)
+    ft = i32([0])
+    ws = kv.alloc_workspace(kv.kv_compact_workspace_size(x.B, x.max_pages, 16, True))
+    ref = O.compact(x.block_table, x.seq_lens, keep, True, x.k_pool, x.v_pool, x.free_list, 0,
+                    x.Hkv, x.d, 16)
+    kv.kv_compact(dd.table, dd.lens, u8(keep), True, dd.k, dd.v, fl, ft, ws)
+    rc = kv.kv_get_status(ws)
+    if ref[-1] == O.ENOSPACE:
+        assert rc == kv.KV_ENOSPACE and torch.equal(dd.table, t0)
+    else:
+        assert rc == 0
+
+
+def test_append_bit_exact_and_errors():
+    rng = np.random.default_rng(8)
+    x = W.small_decode(9, 6, 8, 2, 128, [16, 5, 32, 0, 47, 48], pool_factor=2.0, pad_pages=2)
+    kn = W.normal_bits(rng, (6, 2, 128), W.F16)
+    vn = W.normal_bits(rng, (6, 2, 128), W.F16)
+    ref = O.append(kn, vn, x.k_pool, x.v_pool, x.block_table, x.seq_lens, x.free_list, x.free_top,
+                   2, 128, 16)
+    assert ref[-1] == 0
+    dd = DeviceDecode(x)
+    fl, ft = i32(x.free_list), i32([x.free_top])
+    ws = kv.alloc_workspace(kv.kv_append_workspace_size(6))
+    kv.kv_append(bits_to_dev(kn, W.F16), bits_to_dev(vn, W.F16), dd.k, dd.v, dd.table, dd.lens, fl,
+                 ft, ws)
+    assert kv.kv_get_status(ws) == 0
+    kp, vp, t, sl, flr, top, _ = ref
+    assert np.array_equal(dd.table.cpu().numpy(), t) and np.array_equal(dd.lens.cpu().numpy(), sl)
+    assert int(ft.item()) == top
+    assert np.array_equal(dd.k.view(torch.int16).cpu().numpy().view(np.uint16), kp)
+    assert np.array_equal(dd.v.view(torch.int16).cpu().numpy().view(np.uint16), vp)
+    # too few free pages: error, no change
+    t0, l0 = dd.table.clone(), dd.lens.clone()
+    kv.kv_append(bits_to_dev(kn, W.F16), bits_to_dev(vn, W.F16), dd.k, dd.v, dd.table, dd.lens, fl,
+                 i32([0]), ws)
+    assert kv.kv_get_status(ws) == kv.KV_ENOSPACE
+    assert torch.equal(dd.table, t0) and torch.equal(dd.lens, l0)
+    # a full row: error, no change
+    full = dd.lens.clone()
+    full[0] = 16 * x.max_pages
+    kv.kv_append(bits_to_dev(kn, W.F16), bits_to_dev(vn, W.F16), dd.k, dd.v, dd.table, full, fl,
+                 ft, ws)
+    assert kv.kv_get_status(ws) == kv.KV_EFULL
+
+
+def test_tiny_selection_pipeline():
+    """Tiny workload: EMAs over 32 prior queries, page summaries, scores and
+    keep-8-of-16, against the oracle bit for bit; then the fp64 definition
+    picks the same 8 pages."""
+    c = W.tiny()
+    x = c["decode"]
+    B, Hq, Hkv, d = x.B, x.Hq, x.Hkv, x.d
+    ema = torch.zeros((B, 2, Hkv, d), dtype=torch.float32, device=DEV)
+    ref = np.zeros((B, 2, Hkv, d), np.float32)
+    ref64 = np.zeros((B, 2, Hkv, d))
+    for t in range(32):
+        q = c["prior_q"][t]
+        kv.kv_update_query_summaries(bits_to_dev(q, W.F16), Hkv, c["a_fast"], c["a_slow"], t == 0, ema)
+        O.ema_f32(q, B, Hq, Hkv, d, W.F16, c["a_fast"], c["a_slow"], t == 0, ref)
+        O.ema_f64(q, B, Hq, Hkv, d, W.F16, c["a_fast"], c["a_slow"], t == 0, ref64)
+    assert np.array_equal(ema.cpu().numpy(), ref)
+    dd = DeviceDecode(x)
+    summ = torch.zeros((x.num_pages, Hkv, 3, d), dtype=torch.float32, device=DEV)
+    ws = kv.alloc_workspace(kv.kv_select_workspace_size(B, 16))
+    kv.kv_page_summaries(dd.k, i32(x.block_table[0]), summ, ws)
+    sref = np.zeros((x.num_pages, Hkv, 3, d), np.float32)
+    O.page_summaries_f32(x.k_pool, x.block_table[0], Hkv, 16, d, W.F16, sref)
+    assert np.array_equal(summ.cpu().numpy(), sref)
+    sc = torch.zeros((B, 16, 2), dtype=torch.float32, device=DEV)
+    kv.kv_score_pages(ema, summ, dd.table, dd.lens, None, sc, ws)
+    scr = np.zeros((B, 16, 2), np.float32)
+    O.score_pages_f32(ref, sref, x.block_table, x.seq_lens, None, Hkv, d, 16, scr)
+    assert np.array_equal(sc.cpu().numpy(), scr)
+    keep, grow, bud, _ = _run_select(scr, x.seq_lens, None, [8], O.SELECT_TOPK, 0, 0, 0)
+    kref, *_ = O.select_pages(scr, x.seq_lens, None, [8], 16, 0, 0, 0.5, O.SELECT_TOPK, 0)
+    assert np.array_equal(keep, kref) and keep.sum() == 8
+    # fp64 definition: same selection (margin at the cut far above fp32 noise)
+    s64 = np.zeros((B, 16, 2))
+    summ64 = np.zeros((x.num_pages, Hkv, 3, d))
+    O.page_summaries_f64(x.k_pool, x.block_table[0], Hkv, 16, d, W.F16, summ64)
+    O.score_pages_f64(ref64, summ64, x.block_table, x.seq_lens, None, Hkv, d, 16, s64)
+    R = s64[0, :, 0] + s64[0, :, 1]
+    order = np.argsort(-R, kind="stable")
+    assert set(order[:8]) == set(np.nonzero(keep[0])[0])
+    margin = R[order[7]] - R[order[8]]
+    assert margin > 1e-3 * np.abs(R).max(), margin
+
+
+def test_budgeted_serving_trajectory():
+    """Batch-64 budgeted decode: the fit, then every step's compress-or-grow,
+    append and block-table state bit-exact against the oracle's trajectory;
+    the decode output within tolerance on sampled steps."""
+    steps = int(os.environ.get("KV_BUDGET_STEPS", "128"))
+    c = W.budgeted_serving(steps=steps)
+    x = c["decode"]
+    cfg = BG.BudgetConfig(a_fast=c["a_fast"], a_slow=c["a_slow"], n_first=c["n_first"],
+                          n_last=c["n_last"], delta=c["delta"])
+    orc = OracleBudget(x, c["budget"], cfg)
+    orc.summarize_all()
+    dd = DeviceDecode(x)
+    dec = BG.BudgetedDecoder(dd.k, dd.v, dd.table, dd.lens, i32(x.free_list), i32([x.free_top]),
+                             i32(c["budget"]), x.Hq, cfg)
+    dec.summarize_pages(i32(np.arange(x.num_pages)))
+    q0, _, _ = W.step_tokens(c["seed"], 0, x.B, x.Hq, x.Hkv, x.d, x.dtype)
+    dec.fit(bits_to_dev(q0, x.dtype))
+    orc.fit(q0)
+
+    def check_state(where):
+        assert kv.kv_get_status(dec.ws) == 0, where
+        assert np.array_equal(dec.table.cpu().numpy(), orc.table), where
+        assert np.array_equal(dec.lens.cpu().numpy(), orc.lens), where
+        assert np.array_equal(dec.budget.cpu().numpy(), orc.budget), where
+        top = int(dec.free_top.item())
+        assert top == int(orc.top[0]), where
+        assert np.array_equal(dec.free_list.cpu().numpy()[:top], orc.free_list[:top]), where
+        assert np.array_equal(dec.ema.cpu().numpy(), orc.ema), where
+
+    check_state("fit")
+    grows = compacts = 0
+    for t in range(steps):
+        q, kn, vn = W.step_tokens(c["seed"], t, x.B, x.Hq, x.Hkv, x.d, x.dtype)
+        dec.step(bits_to_dev(q, x.dtype), bits_to_dev(kn, x.dtype), bits_to_dev(vn, x.dtype), t)
+        orc.step(q, kn, vn, t)
+        check_state(f"step {t}")
+        act = orc.active.astype(bool)
+        assert np.array_equal(dec.active.cpu().numpy(), orc.active)
+        assert np.array_equal(dec.grow.cpu().numpy()[act], orc.grow[act])
+        assert np.array_equal(dec.drift.cpu().numpy()[act], orc.drift[act])
+        grows += int(orc.grow[act].sum())
+        compacts += int(act.sum() - orc.grow[act].sum())
+        if t % 16 == 15 or t == steps - 1:
+            y = orc.decode_inputs(q)
+            ref_out, ref_lse = O.decode(y, nthreads=NCPU)
+            assert_decode_close(y, dec.out.cpu().numpy().astype(np.float64),
+                                dec.lse.cpu().numpy().astype(np.float64), ref_out, ref_lse)
+    print(f"budgeted serving: {steps} steps, {grows} grows, {compacts} compactions")
+    assert grows > 0 and compacts > 0
