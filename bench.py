@@ -1,7 +1,10 @@
-"""Benchmark: one paged GQA decode step (workqueue + split-KV decode + LSE
-merge) on the batch-8 bimodal fp16 workload (Hq=32, Hkv=8, d=128, page 16,
-lengths half U[512, 2048] and half U[16384, 32768], pages scattered in a pool
-of 1.25x the pages used), measured as KV HBM GB/s and tokens/s.
+"""Benchmark: one paged GQA decode step (per-CTA workqueue + split-KV decode +
+LSE merge, one kernel launch) on the batch-8 bimodal fp16 workload (Hq=32,
+Hkv=8, d=128, page 16, lengths half U[512, 2048] and half U[16384, 32768],
+pages scattered in a pool of 1.25x the pages used), measured as KV HBM GB/s
+and tokens/s.  The `budget_step` object times the whole budgeted step (query
+EMAs, page summaries, scoring, selection, compaction, append, decode) on the
+batch-64 bf16 workload with per-sequence page budgets.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
                     [--workload bimodal|uniform|zipf|bucket32k|bucket64k|bucket128k|tiny]
@@ -139,7 +142,7 @@ def time_oracle(x: W.DecodeInputs, steps: int, warmup: int):
     y = oracle_sample(x)
     O.decode(y, nthreads=cores)  # build + page in
     for _ in range(max(0, warmup - 1)):
-        pass
+        O.decode(y, nthreads=cores)
     t = []
     for _ in range(steps):
         t0 = time.perf_counter()
@@ -147,7 +150,7 @@ def time_oracle(x: W.DecodeInputs, steps: int, warmup: int):
         t.append(time.perf_counter() - t0)
     sec = statistics.median(t)
     return {"value": y.algorithmic_bytes() / sec / 1e9, "unit": "GB/s", "cores": cores,
-            "kind": "oracle",
+            "kind": "oracle", "ms_per_step": sec * 1e3,
             "tokens_per_s": x.B / sec * (y.Hkv / x.Hkv),
             "sample": f"all {x.B} sequences, KV heads 0..{y.Hkv - 1} of {x.Hkv} "
                       f"({y.algorithmic_bytes() / 1e6:.1f} MB of K/V+q+table per step), "
@@ -157,10 +160,10 @@ def time_oracle(x: W.DecodeInputs, steps: int, warmup: int):
 def run_reference(args, x, name, rank, world):
     if rank != 0:
         return
-    cpu = time_oracle(x, max(1, args.steps), args.warmup)
+    cpu = time_oracle(x, max(1, args.steps), min(args.warmup, 3))
     line = {"impl": "reference", "metric": METRIC, "value": cpu["value"], "unit": "GB/s",
             "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
-            "ms_per_step": None, "higher_is_better": True, "scaling": "weak",
+            "ms_per_step": cpu["ms_per_step"], "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f64", "data": "synthetic",
             "config": workload_config(x, name),
             "cpu_baseline": cpu,
@@ -201,8 +204,12 @@ def run_ours(args, x, name, rank, world):
     ho = torch.empty((x.B, x.Hq, x.d), dtype=torch.float32).pin_memory()
     hls = torch.empty((x.B, x.Hq), dtype=torch.float32).pin_memory()
 
+    decode = kv.prepare_decode(q, k, v, table, lens, x.scale, out, lse, ws, stream=stream)
+
     def step():
-        kv.kv_decode(q, k, v, table, lens, x.scale, out, lse, ws)
+        rc = decode()
+        if rc:
+            raise kv.KVError(rc, "kv_decode")
 
     for _ in range(max(3, args.warmup)):
         step()
@@ -268,12 +275,12 @@ def run_ours(args, x, name, rank, world):
     value = world * nbytes / t_step / 1e9
     achieved = nbytes / t_kern / 1e9
     traffic = None
-    prof = os.path.join(ROOT, "profiles", f"decode_{name}_traffic.json")
+    prof = os.path.join(ROOT, "profiles", f"decode_{name}_traffic.txt")
     if os.path.exists(prof):
         with open(prof) as f:
-            tj = json.load(f)
-        if tj.get("kernel_source_hash") == kernel_hash():
-            traffic = tj.get("dram_bytes_per_launch")
+            tj = dict(line.split(": ", 1) for line in f.read().splitlines() if ": " in line)
+        if tj.get("kernel_source_hash") == kernel_hash():  # null once the kernel changed
+            traffic = float(tj["dram_bytes_per_launch"])
     h2d = x.q.nbytes + x.block_table.nbytes + x.seq_lens.nbytes
     d2h = x.B * x.Hq * x.d * 4 + x.B * x.Hq * 4
     line = {
@@ -290,14 +297,105 @@ def run_ours(args, x, name, rank, world):
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "traffic": traffic,
                      "kernel": "decode_kernel<128,4,F16>" if x.dtype == W.F16 else "decode_kernel<128,4,BF16>",
+                     "units": f"{int(x.seq_lens.sum())} K/V tokens x 4096 B + q + table entries per launch",
                      "kernel_ms": t_kern * 1e3, "peak_source": f"MEASURED_PEAKS.json hbm_gbs ({peak_kind})"},
-        "gpu_launches": 3 * n,
-        "gpu_launches_note": "per step: workqueue builder, split-KV decode, LSE merge",
+        "gpu_launches": launches_per_step(x.B) * n,
+        "gpu_launches_note": "per step: one decode kernel (workqueue slice, split-KV decode and "
+                             "LSE merge fused); a page-offset pass is added above 1024 sequences",
         "clocks": clocks,
     }
+    if not args.no_budget:
+        line["budget_step"] = measure_budget(dev, peak, peak_kind, args.budget_steps,
+                                             args.budget_warmup)
     if not args.no_cpu_baseline:
         line["cpu_baseline"] = time_oracle(x, 1, 0)
     print(json.dumps(line), flush=True)
+
+
+def launches_per_step(B):
+    return 1 if B <= 1024 else 2
+
+
+def measure_budget(dev, peak, peak_kind, steps, warmup):
+    """Whole budgeted decode step on the batch-64 bf16 workload: fit to the
+    budgets, then `warmup` untimed and `steps` timed steps of EMA update,
+    boundary compress-or-grow, append and decode.  Each step's bytes are the
+    decode's algorithmic bytes over the resident tokens after the append."""
+    import torch
+
+    from paged_kv_cache_492_b300 import budget as BG
+    from paged_kv_cache_492_b300 import kv
+
+    t0 = time.perf_counter()
+    c = W.budgeted_serving()
+    x = c["decode"]
+    assert warmup + steps <= c["steps"], "the workload is 128 steps long"
+    tdt = torch.bfloat16 if x.dtype == W.BF16 else torch.float16
+
+    def dev_bits(a):
+        return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).to(dev).view(tdt)
+
+    k = dev_bits(x.k_pool)
+    v = dev_bits(x.v_pool)
+    i32 = lambda a: torch.from_numpy(np.ascontiguousarray(a, dtype=np.int32)).to(dev)  # noqa: E731
+    cfg = BG.BudgetConfig(a_fast=c["a_fast"], a_slow=c["a_slow"], n_first=c["n_first"],
+                          n_last=c["n_last"], delta=c["delta"])
+    dec = BG.BudgetedDecoder(k, v, i32(x.block_table), i32(x.seq_lens), i32(x.free_list),
+                             i32([x.free_top]), i32(c["budget"]), x.Hq, cfg)
+    dec.summarize_pages(i32(np.arange(x.num_pages)))
+    toks = [tuple(dev_bits(a) for a in W.step_tokens(c["seed"], t, x.B, x.Hq, x.Hkv, x.d, x.dtype))
+            for t in range(warmup + steps)]
+    q0 = dev_bits(W.step_tokens(c["seed"], 0, x.B, x.Hq, x.Hkv, x.d, x.dtype)[0])
+    dec.fit(q0)
+    flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+    for t in range(warmup):
+        dec.step(*toks[t], t)
+    torch.cuda.synchronize()
+    setup_s = time.perf_counter() - t0
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(steps)]
+    evk = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(steps)]
+    for a, b in evk:
+        a.record(stream)
+        b.record(stream)
+    lens_after = []
+    torch.cuda.synchronize()
+    for i in range(steps):
+        t = warmup + i
+        flush.zero_()
+        kv.kv_profile_next_decode(evk[i][0], evk[i][1])
+        ev[i][0].record(stream)
+        dec.step(*toks[t], t)
+        ev[i][1].record(stream)
+        lens_after.append(dec.lens.clone())
+    torch.cuda.synchronize()
+    st = [kv.kv_get_status(dec.ws), kv.kv_get_status(dec.decode_ws)]
+    if any(st):
+        raise SystemExit(f"device error in the budgeted step: {st}")
+    step_ms = [a.elapsed_time(b) for a, b in ev]
+    dec_ms = [a.elapsed_time(b) for a, b in evk]
+    nbytes = []
+    for L in lens_after:
+        Lh = L.cpu().numpy().astype(np.int64)
+        npg = -(-Lh // x.page_size)
+        nbytes.append(int(Lh.sum()) * 2 * x.Hkv * x.d * 2 + x.B * x.Hq * x.d * 2 + 4 * int(npg.sum()))
+    tot_b = float(sum(nbytes))
+    t_step = sum(step_ms) / 1e3
+    t_dec = sum(dec_ms) / 1e3
+    return {
+        "workload": "budgeted_b64_bf16 (Hq=32, Hkv=8, d=128, L~U[2048,16384], budgets U[32,256])",
+        "steps_timed": steps, "warmup_steps": warmup,
+        "ms_per_step": t_step / steps * 1e3, "decode_ms_per_step": t_dec / steps * 1e3,
+        "step_gbs": tot_b / t_step / 1e9, "decode_gbs": tot_b / t_dec / 1e9,
+        "decode_frac_of_peak": tot_b / t_dec / 1e9 / peak, "peak_gbs": peak,
+        "peak_source": f"MEASURED_PEAKS.json hbm_gbs ({peak_kind})",
+        "tokens_per_s": x.B * steps / t_step,
+        "resident_kv_bytes_per_step": tot_b / steps,
+        "l2": "flushed between steps (512 MiB memset outside the timed events)",
+        "setup_s": setup_s,
+    }
 
 
 def kernel_hash():
@@ -318,6 +416,9 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="bimodal", choices=list(WORKLOADS))
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-budget", action="store_true", help="skip the budgeted-step leg")
+    ap.add_argument("--budget-steps", type=int, default=64)
+    ap.add_argument("--budget-warmup", type=int, default=8)
     args = ap.parse_args()
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))

@@ -12,8 +12,9 @@
  *        non-empty (sequence, KV-head, split) tasks.
  *  [GP]  mlsanity.com, "GrowPage: On-Demand KV Budgeting for Efficient LLM
  *        Reasoning Serving" -- Abstract; aitrending.vip GrowPage summary --
- *        Technical Details: dual-timescale query summaries, relative attention
- *        working sets, compress-or-grow at every capacity boundary, on top of
+ *        Technical Details: query summaries at a short and a long time
+ *        scale, their attention working sets compared to track demand,
+ *        compress-or-grow at every capacity boundary, on top of
  *        PagedAttention's page abstraction.
  *  [EKV] paperlayer.ai, "Elastic KV Cache for LLM Serving" -- section 2:
  *        fixed-size KV blocks handed out from an integer free list.
@@ -46,8 +47,9 @@
  *  - Workspace: `ws` is caller-allocated device memory of at least the size
  *    the matching *_workspace_size function returns, 256-byte aligned.  Its
  *    first 256 bytes hold the status word.  One workspace may serve several
- *    calls that run in order on one stream; calls that overlap on the device
- *    must not share one.  Zero it once before first use (kv_workspace_reset).
+ *    calls that run in order on one stream (kv_decode excepted: see
+ *    kv_decode_workspace_size); calls that overlap on the device must not
+ *    share one.  Zero it once before first use (kv_workspace_reset).
  */
 #ifndef PAGED_KV_B300_KV_H
 #define PAGED_KV_B300_KV_H
@@ -74,11 +76,19 @@ extern "C" {
 /* Text for a status code (static storage). */
 const char *kv_status_string(int code);
 
+/* The CUDA runtime call behind the most recent KV_ECUDA returned on the
+ * calling host thread, with the runtime's error name and text; "" if none.
+ * Thread-local storage owned by the library, valid until the next call that
+ * fails on this thread. */
+const char *kv_last_error(void);
+
 /* Bytes of the workspace header (the status word); the minimum workspace. */
 size_t kv_status_workspace_size(void);
 
-/* Zero the workspace header (status word) on `stream`. */
-int kv_workspace_reset(void *ws, void *stream);
+/* Zero the first ws_bytes bytes of a workspace (at least the status word)
+ * on `stream`.  A new workspace must be zeroed once before its first call;
+ * after a KV_ETIMEOUT zero it again before reusing it. */
+int kv_workspace_reset(void *ws, size_t ws_bytes, void *stream);
 
 /* Synchronise `stream`, return the first device-side error recorded in `ws`
  * since the last call (KV_OK if none) and clear it. */
@@ -94,7 +104,13 @@ int kv_get_status(void *ws, void *stream);
 int kv_decode_num_workers(int Hq, int Hkv, int d, int page_size, int dtype);
 
 /* Workspace bytes kv_decode needs for a batch of B sequences whose tables are
- * max_pages wide.  pages_per_split as passed to kv_decode (0 = automatic). */
+ * max_pages wide.  pages_per_split as passed to kv_decode (0 = automatic).
+ * Besides scratch, a decode workspace keeps one merge ticket per (sequence,
+ * KV head) that must read zero when a call starts: every kv_decode that
+ * completes leaves them zero, so a decode workspace stays valid across
+ * calls as long as no other call writes into it (give kv_decode a workspace
+ * of its own; the budgeting calls use theirs as scratch).  A counter found
+ * non-zero is reported as KV_EWORKSPACE. */
 size_t kv_decode_workspace_size(int B, int Hq, int Hkv, int d, int max_pages, int page_size,
                                 int pages_per_split);
 
@@ -107,9 +123,11 @@ size_t kv_decode_workspace_size(int B, int Hq, int Hkv, int d, int max_pages, in
  * Work split: the non-empty pages of the batch, laid end to end, are cut into
  * chunks of `pages_per_split` pages (0 = automatic: ceil(W / workers), at
  * least 8, W = total pages); each (sequence, chunk) overlap is one split, and
- * each split is one task per KV head.  A task streams each (page, KV head)
- * tile once from HBM and reuses it for all G = Hq/Hkv query heads; splits of
- * one sequence are recombined by a log-sum-exp merge.
+ * each split is one task per KV head (the queue kv_build_workqueue
+ * materialises).  A task streams each (page, KV head) tile once from HBM and
+ * reuses it for all G = Hq/Hkv query heads; splits of one sequence are
+ * recombined by a log-sum-exp merge done by whichever split finishes last.
+ * One kernel launch (two for B > 1024: a page-offset pass first). 
  * Device errors: KV_EBADPAGE (an entry in [0, ceil(L_b/16)) outside
  * [0, num_pages); page 0 is read in its place), KV_EINVAL (L_b < 0 or more
  * pages than max_pages), KV_EWORKSPACE, KV_ETIMEOUT. */

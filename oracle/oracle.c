@@ -14,9 +14,10 @@
  *         reused across the grouped query heads, a compact workqueue of
  *         non-empty (sequence, KV-head, split) tasks.
  *  [GP]   mlsanity.com, "GrowPage: On-Demand KV Budgeting for Efficient LLM
- *         Reasoning Serving" -- Abstract: dual-timescale query summaries,
- *         relative attention working sets, compress-or-grow at each capacity
- *         boundary, on top of PagedAttention pages.
+ *         Reasoning Serving" -- Abstract: query summaries kept at a short
+ *         and a long time scale, their attention working sets compared to
+ *         track demand, compress-or-grow at each capacity boundary, on top
+ *         of PagedAttention pages.
  *  [GP1]  aitrending.vip GrowPage summary -- Technical Details (same method).
  *  [EKV]  paperlayer.ai, "Elastic KV Cache for LLM Serving" -- section 2:
  *         fixed-size KV blocks handed out from an integer free list.
@@ -576,7 +577,7 @@ static void top_k(const int *cands, int n, const float *key, int k, uint8_t *sel
  *   w = ceil(ws_frac * |C|) (fp32, clipped to [1, |C|]);
  *   W_f = top_w(C, S_fast), W_s = top_w(C, S_slow), drift D = |W_f \ W_s|;
  *   wants_grow = D > delta * w (fp32) -- the recent working set has moved
- *   beyond the long-term one ("broader demand"); with C empty nothing can be
+ *   beyond the long-term one (demand is widening); with C empty nothing can be
  *   evicted and the sequence always wants to grow.
  *   Grows are granted in ascending b while granted < free_count; a granted
  *   sequence keeps every page, grow[b] = 1 and budget[b] += 1.  Otherwise

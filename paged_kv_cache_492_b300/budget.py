@@ -1,7 +1,7 @@
 """GrowPage-style budgeted decode step, as a sequence of C-ABI calls.
 
 GrowPage (mlsanity.com, "GrowPage: On-Demand KV Budgeting ...", Abstract):
-dual-timescale query summaries; at every capacity boundary either compress
+query summaries at two time scales; at every capacity boundary either compress
 the KV states inside the current allocation or take one more physical page
 when the recent attention working set has moved beyond the long-term one.
 This module only orders the library's kernels on one stream; it does no
@@ -66,11 +66,12 @@ class BudgetedDecoder:
         self.drift = torch.zeros(B, dtype=torch.int32, device=dev)
         self.out = torch.empty((B, Hq, d), dtype=torch.float32, device=dev)
         self.lse = torch.empty((B, Hq), dtype=torch.float32, device=dev)
-        ws = max(kv.kv_decode_workspace_size(B, Hq, Hkv, d, maxp),
-                 kv.kv_select_workspace_size(B, maxp),
+        ws = max(kv.kv_select_workspace_size(B, maxp),
                  kv.kv_compact_workspace_size(B, maxp),
                  kv.kv_append_workspace_size(B))
         self.ws = kv.alloc_workspace(ws, dev)
+        # kv_decode keeps merge tickets in its workspace between calls
+        self.decode_ws = kv.alloc_workspace(kv.kv_decode_workspace_size(B, Hq, Hkv, d, maxp), dev)
         self.scale = 1.0 / (d ** 0.5)
 
     # -- pieces ---------------------------------------------------------
@@ -117,4 +118,4 @@ class BudgetedDecoder:
         kv.kv_append(k_new, v_new, self.k_pool, self.v_pool, self.table, self.lens,
                      self.free_list, self.free_top, self.ws, stream=self.stream)
         kv.kv_decode(q, self.k_pool, self.v_pool, self.table, self.lens, self.scale, self.out,
-                     self.lse, self.ws, stream=self.stream)
+                     self.lse, self.decode_ws, stream=self.stream)

@@ -1,6 +1,7 @@
 // C ABI entry points: status handling, decode (device and host buffers), and
 // the stand-alone workqueue builder.  Argument checks happen here, on the
 // host, before anything is enqueued.
+#include <stdio.h>
 #include <string.h>
 
 #include <algorithm>
@@ -9,7 +10,24 @@
 
 using namespace kvb;
 
+namespace kvb {
+namespace {
+thread_local char t_last_error[256] = "";
+}
+int cuda_failed(cudaError_t err, const char* what) {
+  snprintf(t_last_error, sizeof t_last_error, "%s: %s (%s, %d)", what, cudaGetErrorString(err),
+           cudaGetErrorName(err), (int)err);
+  // A failed call leaves its (non-sticky) error pending in the runtime; it is
+  // reported here, so clear it rather than let the caller's next CUDA call
+  // pick it up.
+  (void)cudaGetLastError();
+  return KV_ECUDA;
+}
+}  // namespace kvb
+
 extern "C" {
+
+const char* kv_last_error(void) { return t_last_error; }
 
 const char* kv_status_string(int code) {
   switch (code) {
@@ -27,23 +45,21 @@ const char* kv_status_string(int code) {
 
 size_t kv_status_workspace_size(void) { return kHeaderBytes; }
 
-int kv_workspace_reset(void* ws, void* stream) {
-  if (!ws) return KV_EINVAL;
-  return cudaMemsetAsync(ws, 0, kHeaderBytes, static_cast<cudaStream_t>(stream)) == cudaSuccess
-             ? KV_OK
-             : KV_ECUDA;
+int kv_workspace_reset(void* ws, size_t ws_bytes, void* stream) {
+  if (!ws || ws_bytes < kHeaderBytes) return KV_EINVAL;
+  KV_CUDA_CHECK(cudaMemsetAsync(ws, 0, ws_bytes, static_cast<cudaStream_t>(stream)));
+  return KV_OK;
 }
 
 int kv_get_status(void* ws, void* stream) {
   if (!ws) return KV_EINVAL;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   int host = 0;
-  if (cudaMemcpyAsync(&host, ws, sizeof(int), cudaMemcpyDeviceToHost, s) != cudaSuccess)
-    return KV_ECUDA;
-  if (cudaStreamSynchronize(s) != cudaSuccess) return KV_ECUDA;
+  KV_CUDA_CHECK(cudaMemcpyAsync(&host, ws, sizeof(int), cudaMemcpyDeviceToHost, s));
+  KV_CUDA_CHECK(cudaStreamSynchronize(s));
   if (host != 0) {
-    if (cudaMemsetAsync(ws, 0, sizeof(int), s) != cudaSuccess) return KV_ECUDA;
-    if (cudaStreamSynchronize(s) != cudaSuccess) return KV_ECUDA;
+    KV_CUDA_CHECK(cudaMemsetAsync(ws, 0, sizeof(int), s));
+    KV_CUDA_CHECK(cudaStreamSynchronize(s));
   }
   return host;
 }
@@ -115,20 +131,17 @@ int kv_decode_hostio(const void* h_q, const void* k_pool, const void* v_pool, in
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   uint8_t* w = static_cast<uint8_t*>(ws);
   const size_t qb = (size_t)B * Hq * d * 2, tb = (size_t)B * max_pages * 4, sb = (size_t)B * 4;
-  if (cudaMemcpyAsync(w + L.q, h_q, qb, cudaMemcpyHostToDevice, s) != cudaSuccess ||
-      cudaMemcpyAsync(w + L.table, h_block_table, tb, cudaMemcpyHostToDevice, s) != cudaSuccess ||
-      cudaMemcpyAsync(w + L.seq_lens, h_seq_lens, sb, cudaMemcpyHostToDevice, s) != cudaSuccess)
-    return KV_ECUDA;
+  KV_CUDA_CHECK(cudaMemcpyAsync(w + L.q, h_q, qb, cudaMemcpyHostToDevice, s));
+  KV_CUDA_CHECK(cudaMemcpyAsync(w + L.table, h_block_table, tb, cudaMemcpyHostToDevice, s));
+  KV_CUDA_CHECK(cudaMemcpyAsync(w + L.seq_lens, h_seq_lens, sb, cudaMemcpyHostToDevice, s));
   int rc = decode_launch(w + L.q, k_pool, v_pool, num_pages,
                          reinterpret_cast<const int32_t*>(w + L.table), max_pages,
                          reinterpret_cast<const int32_t*>(w + L.seq_lens), B, page_size, Hq, Hkv, d,
                          dtype, scale, pages_per_split, reinterpret_cast<float*>(w + L.out),
                          reinterpret_cast<float*>(w + L.lse), ws, base, s);
   if (rc) return rc;
-  if (cudaMemcpyAsync(h_out, w + L.out, (size_t)B * Hq * d * 4, cudaMemcpyDeviceToHost, s) !=
-          cudaSuccess ||
-      cudaMemcpyAsync(h_lse, w + L.lse, (size_t)B * Hq * 4, cudaMemcpyDeviceToHost, s) != cudaSuccess)
-    return KV_ECUDA;
+  KV_CUDA_CHECK(cudaMemcpyAsync(h_out, w + L.out, (size_t)B * Hq * d * 4, cudaMemcpyDeviceToHost, s));
+  KV_CUDA_CHECK(cudaMemcpyAsync(h_lse, w + L.lse, (size_t)B * Hq * 4, cudaMemcpyDeviceToHost, s));
   return KV_OK;
 }
 
@@ -164,8 +177,8 @@ int kv_build_workqueue(const int32_t* seq_lens, int B, int Hkv, int page_size, i
                                             align_up((size_t)(B > 0 ? B : 1) * 8, 256));
   a.meta = meta;
   a.status = static_cast<int*>(ws);
-  return launch_build_workqueue(a, static_cast<cudaStream_t>(stream)) == cudaSuccess ? KV_OK
-                                                                                     : KV_ECUDA;
+  KV_CUDA_CHECK(launch_build_workqueue(a, static_cast<cudaStream_t>(stream)));
+  return KV_OK;
 }
 
 int kv_profile_next_decode(void* event_before, void* event_after) {

@@ -1,5 +1,5 @@
 // Page budgeting (GrowPage, mlsanity.com -- Abstract; aitrending.vip summary
-// -- Technical Details): dual-timescale query summaries, page key summaries,
+// -- Technical Details): query summaries at two time scales, page key summaries,
 // page scores, top-k retention with compress-or-grow at capacity boundaries,
 // compaction of the block table (and K/V for token-granular masks), and the
 // per-token append that draws pages from the integer free list (Elastic KV
@@ -705,6 +705,8 @@ __global__ void append_copy_kernel(const AppendArgs a) {
 
 bool dtype_ok(int dtype) { return dtype == KV_F16 || dtype == KV_BF16; }
 
+constexpr int kCompactMaxSmem = 200 * 1024;  // shared memory of compact_apply_kernel, at most
+
 size_t ws_take(size_t* off, size_t bytes) {
   size_t o = *off;
   *off = align_up(*off + bytes, 256);
@@ -725,13 +727,10 @@ int kv_update_query_summaries(const void* q, int B, int Hq, int Hkv, int d, int 
   if (!q || !ema) return KV_EINVAL;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const int threads = d < 128 ? d : 128;
-  if (dtype == KV_BF16)
-    ema_kernel<BF16><<<B * Hkv, threads, 0, s>>>(static_cast<const uint16_t*>(q), Hq, Hkv, d, a_fast,
-                                                 a_slow, first, ema);
-  else
-    ema_kernel<F16><<<B * Hkv, threads, 0, s>>>(static_cast<const uint16_t*>(q), Hq, Hkv, d, a_fast,
-                                                a_slow, first, ema);
-  return cudaGetLastError() == cudaSuccess ? KV_OK : KV_ECUDA;
+  KV_CUDA_CHECK(launch(dtype == KV_BF16 ? ema_kernel<BF16> : ema_kernel<F16>, dim3(B * Hkv),
+                       dim3(threads), 0, s, false, static_cast<const uint16_t*>(q), Hq, Hkv, d,
+                       a_fast, a_slow, first, ema));
+  return KV_OK;
 }
 
 int kv_mark_active(const int32_t* seq_lens, const int32_t* budget, int B, int page_size, int mode,
@@ -739,9 +738,10 @@ int kv_mark_active(const int32_t* seq_lens, const int32_t* budget, int B, int pa
   if (B < 0 || page_size <= 0 || (mode != 0 && mode != 1)) return KV_EINVAL;
   if (B == 0) return KV_OK;
   if (!seq_lens || !budget || !active) return KV_EINVAL;
-  mark_kernel<<<ceil_div(B, 256), 256, 0, static_cast<cudaStream_t>(stream)>>>(seq_lens, budget, B,
-                                                                              page_size, mode, active);
-  return cudaGetLastError() == cudaSuccess ? KV_OK : KV_ECUDA;
+  KV_CUDA_CHECK(launch(mark_kernel, dim3(ceil_div(B, 256)), dim3(256), 0,
+                       static_cast<cudaStream_t>(stream), false, seq_lens, budget, B, page_size,
+                       mode, active));
+  return KV_OK;
 }
 
 static int launch_summaries(const void* k_pool, int num_pages, const int32_t* page_ids, int n,
@@ -757,15 +757,11 @@ static int launch_summaries(const void* k_pool, int num_pages, const int32_t* pa
   int* status = static_cast<int*>(ws);
   const long long blocks = (long long)n * Hkv;
   if (blocks > 0x7fffffffll) return KV_EINVAL;
-  if (dtype == KV_BF16)
-    summary_kernel<BF16><<<(unsigned)blocks, threads, 0, s>>>(
-        static_cast<const uint16_t*>(k_pool), num_pages, page_ids, n, table, max_pages, seq_lens,
-        active, Hkv, page_size, d, summ, status);
-  else
-    summary_kernel<F16><<<(unsigned)blocks, threads, 0, s>>>(
-        static_cast<const uint16_t*>(k_pool), num_pages, page_ids, n, table, max_pages, seq_lens,
-        active, Hkv, page_size, d, summ, status);
-  return cudaGetLastError() == cudaSuccess ? KV_OK : KV_ECUDA;
+  KV_CUDA_CHECK(launch(dtype == KV_BF16 ? summary_kernel<BF16> : summary_kernel<F16>,
+                       dim3((unsigned)blocks), dim3(threads), 0, s, false,
+                       static_cast<const uint16_t*>(k_pool), num_pages, page_ids, n, table,
+                       max_pages, seq_lens, active, Hkv, page_size, d, summ, status));
+  return KV_OK;
 }
 
 int kv_page_summaries(const void* k_pool, int num_pages, const int32_t* page_ids, int n, int Hkv,
@@ -801,15 +797,11 @@ int kv_score_pages(const float* query_summaries, const float* page_key_summaries
   if (blocks > 0x7fffffffll) return KV_EINVAL;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   int* status = static_cast<int*>(ws);
-  if (d == 128)
-    score_kernel<4><<<(unsigned)blocks, wpb * 32, 0, s>>>(query_summaries, page_key_summaries,
-                                                          num_pages, block_table, max_pages, seq_lens,
-                                                          active, B, Hkv, page_size, scores, status);
-  else
-    score_kernel<2><<<(unsigned)blocks, wpb * 32, 0, s>>>(query_summaries, page_key_summaries,
-                                                          num_pages, block_table, max_pages, seq_lens,
-                                                          active, B, Hkv, page_size, scores, status);
-  return cudaGetLastError() == cudaSuccess ? KV_OK : KV_ECUDA;
+  KV_CUDA_CHECK(launch(d == 128 ? score_kernel<4> : score_kernel<2>, dim3((unsigned)blocks),
+                       dim3(wpb * 32), 0, s, false, query_summaries, page_key_summaries, num_pages,
+                       block_table, max_pages, seq_lens, active, B, Hkv, page_size, scores,
+                       status));
+  return KV_OK;
 }
 
 size_t kv_select_workspace_size(int B, int max_pages) {
@@ -851,15 +843,11 @@ int kv_select_pages(const float* scores, const int32_t* seq_lens, const uint8_t*
   a.wants = reinterpret_cast<int32_t*>(static_cast<uint8_t*>(ws) + kHeaderBytes);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const size_t smem = (size_t)max_pages * (3 * sizeof(float) + 1) + 16;
-  if (cudaFuncSetAttribute(select_rank_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           (int)((size_t)kMaxSelectPages * 13 + 16)) != cudaSuccess)
-    return KV_ECUDA;
-  select_rank_kernel<<<B, kSelThreads, smem, s>>>(a);
-  if (cudaGetLastError() != cudaSuccess) return KV_ECUDA;
-  if (mode == KV_SELECT_BOUNDARY) {
-    select_grant_kernel<<<1, 1024, 0, s>>>(a, free_top);
-    if (cudaGetLastError() != cudaSuccess) return KV_ECUDA;
-  }
+  KV_CUDA_CHECK(cudaFuncSetAttribute(select_rank_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     (int)((size_t)kMaxSelectPages * 13 + 16)));
+  KV_CUDA_CHECK(launch(select_rank_kernel, dim3(B), dim3(kSelThreads), smem, s, false, a));
+  if (mode == KV_SELECT_BOUNDARY)
+    KV_CUDA_CHECK(launch(select_grant_kernel, dim3(1), dim3(1024), 0, s, false, a, free_top));
   return KV_OK;
 }
 
@@ -897,7 +885,7 @@ int kv_compact(int32_t* block_table, int max_pages, int32_t* seq_lens, const uin
   if (token_granular && (!k_pool || !v_pool || ((uintptr_t)k_pool & 15) || ((uintptr_t)v_pool & 15)))
     return KV_EINVAL;
   const size_t smem = (size_t)3 * max_pages * 4;
-  if (smem > 200 * 1024) return KV_EINVAL;
+  if (smem > (size_t)kCompactMaxSmem) return KV_EINVAL;
   size_t o_len, o_pop, o_push, o_ctl, o_fresh, total;
   long long max_fresh;
   compact_layout(B, max_pages, &o_len, &o_pop, &o_push, &o_ctl, &o_fresh, &max_fresh, &total);
@@ -926,14 +914,12 @@ int kv_compact(int32_t* block_table, int max_pages, int32_t* seq_lens, const uin
   a.max_fresh = max_fresh;
   a.status = reinterpret_cast<int*>(w);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  compact_plan_kernel<<<1, 1024, 0, s>>>(a);
-  if (cudaGetLastError() != cudaSuccess) return KV_ECUDA;
-  if (smem > 48 * 1024 &&
-      cudaFuncSetAttribute(compact_apply_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           (int)smem) != cudaSuccess)
-    return KV_ECUDA;
-  compact_apply_kernel<<<B, kApplyThreads, smem, s>>>(a);
-  return cudaGetLastError() == cudaSuccess ? KV_OK : KV_ECUDA;
+  KV_CUDA_CHECK(launch(compact_plan_kernel, dim3(1), dim3(1024), 0, s, false, a));
+  if (smem > 48 * 1024)  // one fixed limit for every call (the attribute is per function)
+    KV_CUDA_CHECK(cudaFuncSetAttribute(compact_apply_kernel,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, kCompactMaxSmem));
+  KV_CUDA_CHECK(launch(compact_apply_kernel, dim3(B), dim3(kApplyThreads), smem, s, false, a));
+  return KV_OK;
 }
 
 size_t kv_append_workspace_size(int B) {
@@ -979,10 +965,9 @@ int kv_append(const void* k_new, const void* v_new, void* k_pool, void* v_pool, 
   a.ctl = reinterpret_cast<int32_t*>(w + o_ctl);
   a.status = reinterpret_cast<int*>(w);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  append_plan_kernel<<<1, 1024, 0, s>>>(a);
-  if (cudaGetLastError() != cudaSuccess) return KV_ECUDA;
-  append_copy_kernel<<<B, 128, 0, s>>>(a);
-  return cudaGetLastError() == cudaSuccess ? KV_OK : KV_ECUDA;
+  KV_CUDA_CHECK(launch(append_plan_kernel, dim3(1), dim3(1024), 0, s, false, a));
+  KV_CUDA_CHECK(launch(append_copy_kernel, dim3(B), dim3(128), 0, s, false, a));
+  return KV_OK;
 }
 
 }  // extern "C"

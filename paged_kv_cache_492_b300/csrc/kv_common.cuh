@@ -127,4 +127,58 @@ __host__ __device__ constexpr long long ceil_div_ll(long long a, long long b) {
   return (a + b - 1) / b;
 }
 
+// ---- the split rule --------------------------------------------------------
+// The non-empty pages of a batch, laid end to end (sequence b owns pages
+// [O_b, O_b + np_b) of the flattened range), are cut into chunks of `chunk`
+// pages; every non-empty (sequence, chunk) intersection is one split of that
+// sequence.  The workqueue builder and the decode kernel both use these.
+
+// Automatic chunk: the W pages spread over n_workers, never below min_chunk.
+__host__ __device__ inline long long auto_chunk(long long W, long long n_workers, int min_chunk) {
+  long long c = n_workers > 0 ? ceil_div_ll(W, n_workers) : W;
+  if (c < min_chunk) c = min_chunk;
+  return c < 1 ? 1 : c;
+}
+// Splits of a sequence with np > 0 pages starting at flattened page O.
+__host__ __device__ inline long long split_count(long long O, long long np, long long chunk) {
+  return np > 0 ? (O + np - 1) / chunk - O / chunk + 1 : 0;
+}
+// Pages [lo, hi) of the sequence (its own numbering) that fall in chunk c.
+__host__ __device__ inline void split_range(long long O, long long np, long long chunk, long long c,
+                                            long long* lo, long long* hi) {
+  const long long a = c * chunk > O ? c * chunk : O;
+  const long long e = (c + 1) * chunk < O + np ? (c + 1) * chunk : O + np;
+  *lo = a - O;
+  *hi = e - O;
+}
+
+// Exclusive block-wide scan of one value per thread (blockDim a multiple of
+// 32, at most 1024); returns the total.  `sm` holds 32 values.
+__device__ __forceinline__ long long block_exclusive_scan(long long v, long long* out_excl, long long* sm) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nwarps = blockDim.x >> 5;
+  long long x = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    long long y = __shfl_up_sync(0xffffffffu, x, o);
+    if (lane >= o) x += y;
+  }
+  if (lane == 31) sm[warp] = x;
+  __syncthreads();
+  if (warp == 0) {
+    long long w = lane < nwarps ? sm[lane] : 0;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      long long y = __shfl_up_sync(0xffffffffu, w, o);
+      if (lane >= o) w += y;
+    }
+    if (lane < nwarps) sm[lane] = w;  // inclusive warp totals
+  }
+  __syncthreads();
+  long long base = warp > 0 ? sm[warp - 1] : 0;
+  *out_excl = base + x - v;
+  long long total = sm[nwarps - 1];
+  __syncthreads();
+  return total;
+}
+
 }  // namespace kvb

@@ -10,6 +10,38 @@
 
 namespace kvb {
 
+// Record a failed CUDA runtime call for kv_last_error (per host thread) and
+// return KV_ECUDA.
+int cuda_failed(cudaError_t err, const char* what);
+
+#define KV_CUDA_CHECK(expr)                                              \
+  do {                                                                   \
+    const cudaError_t kv_err_ = (expr);                                  \
+    if (kv_err_ != cudaSuccess) return ::kvb::cuda_failed(kv_err_, #expr); \
+  } while (0)
+
+// Launch through cudaLaunchKernelEx so the returned code is this launch's
+// own (a bare <<<>>> launch is checked with cudaGetLastError, which also
+// reports errors left behind by unrelated calls).  `pdl` allows programmatic
+// dependent launch: the kernel may start while its predecessor on the
+// stream finishes, and must call griddepcontrol.wait before touching that
+// predecessor's outputs.
+template <class... KArgs, class... Args>
+inline cudaError_t launch(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                          cudaStream_t stream, bool pdl, Args... args) {
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cfg.attrs = pdl ? attr : nullptr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
+}
+
 // Batches up to this many sequences keep the builder's arrays in shared memory.
 constexpr int kSmemSeqs = 2048;
 
@@ -29,24 +61,30 @@ struct WorkqueueArgs {
   int32_t* scratch_np;       // [B] scratch (used when B > kSmemSeqs)
   int32_t* meta;             // [5]
   int* status;
-  // decode call only (NULL otherwise)
-  int32_t* row_done;  // [B * Hkv] split-merge completion counters, zeroed here
-  float* out;         // [B][Hq][d]: rows of empty sequences set to 0
-  float* lse;         // [B][Hq]:    rows of empty sequences set to -inf
-  int Hq, d;
 };
 
 size_t workqueue_smem_bytes(int B);
 cudaError_t launch_build_workqueue(const WorkqueueArgs& a, cudaStream_t stream);
+
+// Decode batches up to this many sequences compute their page offsets inside
+// every decode CTA; larger ones take them from page_offsets_kernel.
+constexpr int kFusedMaxB = 1024;
+
+struct OffsetsArgs {
+  const int32_t* seq_lens;
+  int B, page_size, max_pages;
+  int32_t* page_off;  // [B + 1]
+  int* status;
+};
+cudaError_t launch_page_offsets(const OffsetsArgs& a, cudaStream_t stream);
 
 // Smallest automatic split (pages): keeps merge traffic small on tiny batches.
 constexpr int kMinChunk = 8;
 
 // Decode workspace layout (offsets from the start of the workspace).
 struct DecodeLayout {
-  size_t tasks, chunk_begin, seq_group_begin, seq_nsplit, seq_page_off, scratch_np, row_done,
-      meta, part_o, part_lse, total;
-  long long max_tasks, max_chunks;
+  size_t row_done, group_done, page_off, part_o, part_lse, total;
+  long long max_chunks, max_slots;
 };
 DecodeLayout decode_layout(int B, int Hq, int Hkv, int d, int max_pages, int page_size,
                            int pages_per_split, long long n_workers);

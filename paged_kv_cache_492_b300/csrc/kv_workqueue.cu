@@ -12,10 +12,11 @@
 //
 // One CTA builds the whole queue.  Per-sequence arrays live in shared memory
 // for batches up to kSmemSeqs sequences (global scratch beyond), so the build
-// costs one read of seq_lens plus a few block-wide scans.  For a decode call it
-// also zeroes the per-(sequence, KV head) completion counters the decode
-// kernel's split merge uses, and writes out = 0 / lse = -inf for sequences
-// with no tokens (the decode kernel never visits them).
+// costs one read of seq_lens plus a few block-wide scans.  The decode kernel
+// does not read this materialised queue: each decode CTA derives the tasks
+// of its own chunks from the same page offsets and the same split helpers
+// (kv_common.cuh), so the builder is the inspectable form of that queue.
+// This file also holds the page-offset kernel large decode batches use.
 #include "kv_internal.h"
 
 namespace kvb {
@@ -23,34 +24,6 @@ namespace kvb {
 namespace {
 
 constexpr int kWqThreads = 1024;
-
-// Exclusive block-wide scan of one value per thread; returns the total.
-__device__ long long block_exclusive_scan(long long v, long long* out_excl, long long* sm) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nwarps = blockDim.x >> 5;
-  long long x = v;
-#pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    long long y = __shfl_up_sync(0xffffffffu, x, o);
-    if (lane >= o) x += y;
-  }
-  if (lane == 31) sm[warp] = x;
-  __syncthreads();
-  if (warp == 0) {
-    long long w = lane < nwarps ? sm[lane] : 0;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      long long y = __shfl_up_sync(0xffffffffu, w, o);
-      if (lane >= o) w += y;
-    }
-    if (lane < nwarps) sm[lane] = w;  // inclusive warp totals
-  }
-  __syncthreads();
-  long long base = warp > 0 ? sm[warp - 1] : 0;
-  *out_excl = base + x - v;
-  long long total = sm[nwarps - 1];
-  __syncthreads();
-  return total;
-}
 
 // Largest b with gbeg[b] <= gi: the sequence that owns group gi (sequences
 // without splits share their successor's begin and are skipped over).
@@ -95,9 +68,7 @@ __global__ void __launch_bounds__(kWqThreads, 1) build_workqueue_kernel(Workqueu
   if (bad) set_status(a.status, KV_EINVAL);
   long long page_off;
   const long long W = block_exclusive_scan(my_pages, &page_off, sm);
-  long long chunk = a.chunk_req > 0 ? a.chunk_req
-                                    : max((long long)a.min_chunk, ceil_div_ll(W, a.n_workers));
-  if (chunk < 1) chunk = 1;
+  const long long chunk = a.chunk_req > 0 ? a.chunk_req : auto_chunk(W, a.n_workers, a.min_chunk);
   const long long nchunks = W > 0 ? ceil_div_ll(W, chunk) : 0;
 
   // pass 2: splits per sequence
@@ -106,7 +77,7 @@ __global__ void __launch_bounds__(kWqThreads, 1) build_workqueue_kernel(Workqueu
     long long O = page_off;
     for (int b = b0; b < b1; ++b) {
       const long long np = np_arr[b];
-      const long long ns = np > 0 ? (O + np - 1) / chunk - O / chunk + 1 : 0;
+      const long long ns = split_count(O, np, chunk);
       poff[b] = O;
       nspl[b] = (int32_t)ns;
       my_groups += ns;
@@ -135,17 +106,6 @@ __global__ void __launch_bounds__(kWqThreads, 1) build_workqueue_kernel(Workqueu
       g += ns;
     }
   }
-  // decode only: completion counters of the split merge, empty-sequence outputs
-  if (a.row_done)
-    for (long long i = tid; i < (long long)a.B * a.Hkv; i += nth) a.row_done[i] = 0;
-  if (a.out) {
-    const int per_seq = a.Hq * a.d;
-    for (int b = 0; b < a.B; ++b) {
-      if (np_arr[b] != 0 && !overflow) continue;
-      for (int i = tid; i < per_seq; i += nth) a.out[(size_t)b * per_seq + i] = 0.f;
-      for (int i = tid; i < a.Hq; i += nth) a.lse[(size_t)b * a.Hq + i] = -INFINITY;
-    }
-  }
   __syncthreads();  // sequence arrays visible to the whole block
   if (overflow) {
     if (tid == 0) {
@@ -165,8 +125,8 @@ __global__ void __launch_bounds__(kWqThreads, 1) build_workqueue_kernel(Workqueu
     const long long np = np_arr[b];
     const long long O = poff[b];
     const long long c = O / chunk + s;
-    const long long lo = max(O, c * chunk) - O;
-    const long long hi = min(O + np, (c + 1) * chunk) - O;
+    long long lo, hi;
+    split_range(O, np, chunk, c, &lo, &hi);
     int4* rec = reinterpret_cast<int4*>(a.tasks + ti * 8);
     rec[0] = make_int4(b, h, s, nspl[b]);
     rec[1] = make_int4((int)lo, (int)hi, (int)c, a.seq_lens[b]);
@@ -194,15 +154,55 @@ __global__ void __launch_bounds__(kWqThreads, 1) build_workqueue_kernel(Workqueu
   }
 }
 
+// Page offsets of the batch for decode calls too large to compute them in
+// every decode CTA: page_off[b] = sum of ceil(L_b' / page_size) over b' < b,
+// page_off[B] = total.  Invalid lengths count as 0 pages and set KV_EINVAL;
+// a total beyond int32 sets KV_EINVAL and yields an empty batch.
+__global__ void __launch_bounds__(kWqThreads, 1) page_offsets_kernel(const OffsetsArgs a) {
+  __shared__ long long sm[32];
+  pdl_wait();  // seq_lens may come from the previous kernel on the stream
+  pdl_launch_dependents();
+  const int tid = threadIdx.x, nth = blockDim.x;
+  const int per = ceil_div(a.B, nth);
+  const int b0 = min(a.B, tid * per), b1 = min(a.B, b0 + per);
+  long long mine = 0;
+  bool bad = false;
+  for (int b = b0; b < b1; ++b) {
+    const int L = a.seq_lens[b];
+    long long np = L > 0 ? ceil_div_ll(L, a.page_size) : 0;
+    if (L < 0 || np > a.max_pages) {
+      bad = true;
+      np = 0;
+    }
+    mine += np;
+  }
+  if (bad) set_status(a.status, KV_EINVAL);
+  long long off;
+  const long long W = block_exclusive_scan(mine, &off, sm);
+  const bool overflow = W > 0x7fffffffll;
+  if (overflow && tid == 0) set_status(a.status, KV_EINVAL);
+  for (int b = b0; b < b1; ++b) {
+    a.page_off[b] = overflow ? 0 : (int32_t)off;
+    const int L = a.seq_lens[b];
+    const long long np = L > 0 ? ceil_div_ll(L, a.page_size) : 0;
+    if (L >= 0 && np <= a.max_pages) off += np;
+  }
+  if (tid == 0) a.page_off[a.B] = overflow ? 0 : (int32_t)W;
+}
+
 }  // namespace
+
+cudaError_t launch_page_offsets(const OffsetsArgs& a, cudaStream_t stream) {
+  return launch(page_offsets_kernel, dim3(1), dim3(kWqThreads), 0, stream, true, a);
+}
 
 size_t workqueue_smem_bytes(int B) {
   return B <= kSmemSeqs ? ((size_t)ceil_div(3 * B, 2) + 1 + B) * 8 : 0;
 }
 
 cudaError_t launch_build_workqueue(const WorkqueueArgs& a, cudaStream_t stream) {
-  build_workqueue_kernel<<<1, kWqThreads, workqueue_smem_bytes(a.B), stream>>>(a);
-  return cudaGetLastError();
+  return launch(build_workqueue_kernel, dim3(1), dim3(kWqThreads), workqueue_smem_bytes(a.B), stream,
+                false, a);
 }
 
 }  // namespace kvb

@@ -31,6 +31,8 @@ _lib = None
 class KVError(RuntimeError):
     def __init__(self, code: int, what: str = ""):
         msg = status_string(code) if _lib is not None else str(code)
+        if code == KV_ECUDA and _lib is not None:
+            msg += f" [{last_error()}]"
         super().__init__(f"{what}: {msg} ({code})" if what else f"{msg} ({code})")
         self.code = code
 
@@ -60,8 +62,9 @@ P, I, SZ, F = C.c_void_p, C.c_int, C.c_size_t, C.c_float
 
 _SIGS = {
     "kv_status_string": ([I], C.c_char_p),
+    "kv_last_error": ([], C.c_char_p),
     "kv_status_workspace_size": ([], SZ),
-    "kv_workspace_reset": ([P, P], I),
+    "kv_workspace_reset": ([P, SZ, P], I),
     "kv_get_status": ([P, P], I),
     "kv_decode_num_workers": ([I, I, I, I, I], I),
     "kv_decode_workspace_size": ([I, I, I, I, I, I, I], SZ),
@@ -130,6 +133,11 @@ def status_string(code: int) -> str:
     return lib().kv_status_string(int(code)).decode()
 
 
+def last_error() -> str:
+    """The failing CUDA runtime call behind the last KV_ECUDA on this thread."""
+    return lib().kv_last_error().decode()
+
+
 # ---------------------------------------------------------------- workspace
 def alloc_workspace(nbytes: int, device="cuda") -> torch.Tensor:
     """Zeroed device buffer usable as a workspace (torch allocations are
@@ -144,7 +152,7 @@ def kv_status_workspace_size() -> int:
 
 
 def kv_workspace_reset(ws, stream=None):
-    _check(lib().kv_workspace_reset(_p(ws), _s(stream)), "kv_workspace_reset")
+    _check(lib().kv_workspace_reset(_p(ws), ws.numel(), _s(stream)), "kv_workspace_reset")
 
 
 def kv_get_status(ws, stream=None) -> int:
@@ -180,6 +188,25 @@ def kv_decode(q, k_pool, v_pool, block_table, seq_lens, scale, out, lse, ws,
                          dtype_code(q) if dtype is None else dtype, float(scale),
                          int(pages_per_split), _p(out), _p(lse), _p(ws), ws.numel(), _s(stream))
     _check(rc, "kv_decode")
+
+
+def prepare_decode(q, k_pool, v_pool, block_table, seq_lens, scale, out, lse, ws,
+                   pages_per_split=0, stream=None):
+    """kv_decode with its arguments marshalled once: returns a callable that
+    issues the same C call again (returning the status code) -- for loops
+    that replay one step and should not pay the marshalling each time."""
+    B, Hq, d = q.shape
+    P_, Hkv, ps, _ = k_pool.shape
+    fn = lib().kv_decode
+    args = (_p(q), _p(k_pool), _p(v_pool), P_, _p(block_table), block_table.shape[1],
+            _p(seq_lens), B, ps, Hq, Hkv, d, dtype_code(q), float(scale), int(pages_per_split),
+            _p(out), _p(lse), _p(ws), ws.numel(), _s(stream))
+    cargs = [t(a) if a is not None else None for t, a in zip(fn.argtypes, args)]
+
+    def call() -> int:
+        return fn(*cargs)
+
+    return call
 
 
 def kv_decode_hostio_workspace_size(B, Hq, Hkv, d, max_pages, page_size=16, pages_per_split=0):

@@ -213,9 +213,12 @@ def bucketed_long(L0: int, seed: int = 3, steps: int = 64) -> DecodeInputs:
                        extra_pages=extra + 8, max_pages=max_pages, rng=rng)
 
 
-def step_tokens(seed: int, step: int, B: int, Hq: int, Hkv: int, d: int, dtype: int):
-    """The new query and the new token's K/V for one decode step."""
-    rng = np.random.default_rng([seed, 1000 + step])
+def step_tokens(seed: int, step: int, B: int, Hq: int, Hkv: int, d: int, dtype: int,
+                trace: Optional[int] = None):
+    """The new query and the new token's K/V for one decode step (`trace`
+    separates independent traces drawn from one seed)."""
+    key = [seed, 1000 + step] if trace is None else [seed, trace, 1000 + step]
+    rng = np.random.default_rng(key)
     q = normal_bits(rng, (B, Hq, d), dtype)
     k_new = normal_bits(rng, (B, Hkv, d), dtype)
     v_new = normal_bits(rng, (B, Hkv, d), dtype)

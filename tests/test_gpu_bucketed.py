@@ -1,0 +1,69 @@
+"""GPU parity of the batch-1 long-context bucketed trace: contexts of 32768,
+65536 and 131072 fp16 tokens (Hq=32, Hkv=8, d=128, page 16), 64 decode steps
+each; every step appends the new token's K/V (a page comes off the free list
+at each page boundary) and decodes over all tokens, with the split size
+chosen from the length.  Each step is checked against the oracle run on the
+same input state: the append bit for bit, the decode within tolerance."""
+import os
+
+import numpy as np
+import pytest
+import torch
+
+from oracle import oracle as O
+from paged_kv_cache_492_b300 import kv
+from paged_kv_cache_492_b300 import workloads as W
+from tests.gpu_util import DeviceDecode, assert_decode_close, bits_to_dev, i32
+
+pytestmark = pytest.mark.gpu
+NCPU = len(os.sched_getaffinity(0))
+
+
+def _pool_bits(t):
+    return t.view(torch.int16).cpu().numpy().view(np.uint16)
+
+
+@pytest.mark.parametrize("L0", [32768, 65536, 131072])
+def test_bucketed_trace(L0):
+    steps = int(os.environ.get("KV_BUCKET_STEPS", "64"))
+    seed = 3
+    x = W.bucketed_long(L0, seed=seed, steps=steps)
+    dd = DeviceDecode(x)
+    fl, ft = i32(x.free_list), i32([x.free_top])
+    ws = kv.alloc_workspace(kv.kv_decode_workspace_size(x.B, x.Hq, x.Hkv, x.d, x.max_pages))
+    ws_append = kv.alloc_workspace(kv.kv_append_workspace_size(x.B))
+    # host state the oracle advances
+    hk, hv = x.k_pool.copy(), x.v_pool.copy()
+    ht, hl = x.block_table.copy(), x.seq_lens.copy()
+    hfl, htop = x.free_list.copy(), np.array([x.free_top], np.int32)
+    page_counts = set()
+    for t in range(steps):
+        q, kn, vn = W.step_tokens(seed, t, x.B, x.Hq, x.Hkv, x.d, x.dtype, trace=L0)
+        L = int(hl[0])
+        kv.kv_append(bits_to_dev(kn, x.dtype), bits_to_dev(vn, x.dtype), dd.k, dd.v, dd.table,
+                     dd.lens, fl, ft, ws_append)
+        assert kv.kv_get_status(ws_append) == 0, t
+        rc = O.append_inplace(kn, vn, hk, hv, ht, hl, hfl, htop, x.Hkv, x.d, 16)
+        assert rc == 0
+        dd.q.copy_(bits_to_dev(q, x.dtype))
+        dd.out.fill_(float("nan"))
+        kv.kv_decode(dd.q, dd.k, dd.v, dd.table, dd.lens, x.scale, dd.out, dd.lse, ws)
+        assert kv.kv_get_status(ws) == 0, t
+        # append: table, length, free list, and the written slot bit for bit
+        assert np.array_equal(dd.table.cpu().numpy(), ht), t
+        assert np.array_equal(dd.lens.cpu().numpy(), hl), t
+        assert int(ft.item()) == int(htop[0]), t
+        page = int(ht[0, L // 16])
+        assert np.array_equal(_pool_bits(dd.k[page, :, L % 16]), hk[page, :, L % 16]), t
+        assert np.array_equal(_pool_bits(dd.v[page, :, L % 16]), hv[page, :, L % 16]), t
+        # decode over L + 1 tokens
+        y = W.DecodeInputs(name=x.name, B=1, Hq=x.Hq, Hkv=x.Hkv, d=x.d, page_size=16,
+                           dtype=x.dtype, scale=x.scale, q=q, k_pool=hk, v_pool=hv,
+                           block_table=ht, seq_lens=hl)
+        ref_out, ref_lse = O.decode(y, nthreads=NCPU)
+        assert_decode_close(y, dd.out.cpu().numpy().astype(np.float64),
+                            dd.lse.cpu().numpy().astype(np.float64), ref_out, ref_lse)
+        page_counts.add(int(-(-(L + 1) // 16)))
+    # the whole pools agree at the end (nothing else was written)
+    assert np.array_equal(_pool_bits(dd.k), hk) and np.array_equal(_pool_bits(dd.v), hv)
+    assert len(page_counts) == -(-steps // 16)  # a new page every 16 appends

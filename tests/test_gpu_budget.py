@@ -296,6 +296,7 @@ def test_budgeted_serving_trajectory():
 
     def check_state(where):
         assert kv.kv_get_status(dec.ws) == 0, where
+        assert kv.kv_get_status(dec.decode_ws) == 0, where
         assert np.array_equal(dec.table.cpu().numpy(), orc.table), where
         assert np.array_equal(dec.lens.cpu().numpy(), orc.lens), where
         assert np.array_equal(dec.budget.cpu().numpy(), orc.budget), where

@@ -58,6 +58,55 @@ def test_deterministic():
     assert np.array_equal(o1, o2) and np.array_equal(l1, l2)
 
 
+def test_workspace_reused_across_calls():
+    """One decode workspace serves many calls (its merge tickets return to
+    zero after each); lengths, split sizes and batch contents change."""
+    x = W.small_decode(27, 6, 32, 8, 128, [2000, 3, 0, 700, 1500, 64])
+    dd = DeviceDecode(x)
+    ws = kv.alloc_workspace(kv.kv_decode_workspace_size(x.B, x.Hq, x.Hkv, x.d, x.max_pages, 16, 1))
+    rng = np.random.default_rng(5)
+    for it in range(6):
+        lens = x.seq_lens.copy()
+        if it % 2:
+            lens = np.array([int(rng.integers(0, L + 1)) for L in x.seq_lens], np.int32)
+        y = W.DecodeInputs(**{**x.__dict__, "seq_lens": lens})
+        dd.lens.copy_(i32(lens))
+        out, lse, rc = dd.run(pages_per_split=(0, 1, 3)[it % 3], ws=ws)
+        assert rc == 0
+        ref_out, ref_lse = O.decode(y, nthreads=NCPU)
+        assert_decode_close(y, out, lse, ref_out, ref_lse)
+
+
+def test_dirty_workspace_reported():
+    """A decode workspace whose merge tickets were not zeroed is reported."""
+    x = W.small_decode(28, 2, 8, 2, 64, [900, 500])
+    dd = DeviceDecode(x)
+    ws = kv.alloc_workspace(kv.kv_decode_workspace_size(x.B, x.Hq, x.Hkv, x.d, x.max_pages, 16, 4))
+    ws[256:].fill_(1)
+    _, _, rc = dd.run(pages_per_split=4, ws=ws)
+    assert rc == kv.KV_EWORKSPACE
+    kv.kv_workspace_reset(ws)
+    out, lse, rc = dd.run(pages_per_split=4, ws=ws)
+    assert rc == 0
+    ref_out, ref_lse = O.decode(x, nthreads=NCPU)
+    assert_decode_close(x, out, lse, ref_out, ref_lse)
+
+
+def test_large_batch_offsets_pass():
+    """Batches above 1024 sequences take their page offsets from a separate
+    pass; ragged short lengths, empty rows and splits across sequences."""
+    rng = np.random.default_rng(29)
+    lens = rng.integers(0, 100, size=1500).astype(np.int32)
+    lens[::11] = 0
+    x = W.small_decode(29, 1500, 8, 2, 64, lens.tolist(), pool_factor=1.2)
+    dd = DeviceDecode(x)
+    for pps in (0, 3):
+        out, lse, rc = dd.run(pages_per_split=pps)
+        assert rc == 0
+        ref_out, ref_lse = O.decode(x, nthreads=NCPU)
+        assert_decode_close(x, out, lse, ref_out, ref_lse)
+
+
 def test_bad_page_reported():
     x = W.small_decode(23, 2, 8, 2, 64, [40, 40])
     x.block_table = x.block_table.copy()
