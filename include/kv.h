@@ -160,6 +160,31 @@ int kv_decode_hostio(const void *h_q, const void *k_pool, const void *v_pool, in
                      int pages_per_split, float *h_out, float *h_lse, void *ws, size_t ws_bytes,
                      void *stream);
 
+/* kv_decode for callers that cannot allocate device memory.  The paper has
+ * no counterpart: this is a library convenience.  Some callers only ever
+ * hold their own input and output buffers -- a host framework that plans and
+ * owns every device allocation, or a plugin interface that forbids
+ * allocating on the hot path (cudaMalloc synchronises the device) -- and so
+ * cannot hand kv_decode a workspace.  This entry point takes the same inputs
+ * and outputs as kv_decode, plus `status`, one int32 in device memory that
+ * the call sets to 0 and then to the first device-side error (the codes
+ * kv_get_status would return); it allocates nothing and calls no cudaMalloc,
+ * cudaFree or allocating library routine.
+ * Its scratch is one 16 MiB array in the library's device memory, present on
+ * every device that loads the library until the process exits.  The first
+ * call on a device looks up the array's device address (once per device);
+ * make that first call before any stream capture.  A batch whose scratch
+ * (the size kv_decode_workspace_size reports) exceeds 16 MiB is rejected
+ * with KV_EWORKSPACE and nothing is enqueued; with the automatic split this
+ * holds every supported shape up to tens of thousands of sequences.  Every
+ * call zeroes the part of the array it relies on, but all calls share the
+ * array: calls whose work overlaps on the GPU (other streams, other host
+ * threads) race and must be serialised by the caller. */
+int kv_decode_noalloc(const void *q, const void *k_pool, const void *v_pool, int num_pages,
+                      const int32_t *block_table, int max_pages, const int32_t *seq_lens, int B,
+                      int page_size, int Hq, int Hkv, int d, int dtype, float scale,
+                      int pages_per_split, float *out, float *lse, int32_t *status, void *stream);
+
 /* The decode workqueue on its own (for inspection and tests).  With
  * chunk = pages_per_split (> 0) or the automatic size for n_workers workers
  * (pages_per_split = 0): writes, in (b, split, h) order, one 8 x int32 record

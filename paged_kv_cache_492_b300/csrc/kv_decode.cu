@@ -852,3 +852,129 @@ int decode_launch(const void* q, const void* k_pool, const void* v_pool, int num
 }
 
 }  // namespace kvb
+
+// ---------------------------------------------------------------------------
+// Decode for callers that cannot allocate device memory.
+//
+// Some callers are handed only their input and output buffers: a host
+// framework that plans and owns every device allocation itself, or a
+// plugin interface whose contract forbids allocating on the hot path (where
+// cudaMalloc's implicit synchronisation would stall the whole device).  They
+// cannot provide kv_decode's workspace, so this variant keeps its scratch
+// (merge tickets, partial results, page offsets) in one file-scope device
+// array instead.  Every device that loads the library holds the array until
+// the process exits; all calls share it.
+// ---------------------------------------------------------------------------
+namespace kvb {
+namespace {
+
+constexpr size_t kNoAllocScratchBytes = size_t(16) << 20;  // 16 MiB
+constexpr int kNoAllocMaxDevices = 64;
+
+static __device__ __align__(256) uint8_t g_noalloc_scratch[kNoAllocScratchBytes];
+
+std::mutex g_noalloc_mu;
+void* g_noalloc_addr[kNoAllocMaxDevices] = {};
+
+// Device address of the scratch array on the current device, looked up once
+// per device (the host-side name of the array is not a device address).
+int noalloc_scratch(void** out) {
+  int dev = 0;
+  KV_CUDA_CHECK(cudaGetDevice(&dev));
+  if (dev < 0 || dev >= kNoAllocMaxDevices) return KV_EINVAL;
+  std::lock_guard<std::mutex> lk(g_noalloc_mu);
+  if (!g_noalloc_addr[dev]) {
+    void* ptr = nullptr;
+    KV_CUDA_CHECK(cudaGetSymbolAddress(&ptr, g_noalloc_scratch));
+    g_noalloc_addr[dev] = ptr;
+  }
+  *out = g_noalloc_addr[dev];
+  return KV_OK;
+}
+
+int decode_noalloc(const void* q, const void* k_pool, const void* v_pool, int num_pages,
+                   const int32_t* block_table, int max_pages, const int32_t* seq_lens, int B,
+                   int page_size, int Hq, int Hkv, int d, int dtype, float scale,
+                   int pages_per_split, float* out, float* lse, int32_t* status,
+                   cudaStream_t stream) {
+  if (!shape_ok(page_size, Hq, Hkv, d, dtype)) return KV_EINVAL;
+  if (B < 0 || num_pages < 0 || max_pages < 0 || pages_per_split < 0) return KV_EINVAL;
+  if (!status) return KV_EINVAL;
+  if (B == 0) return KV_OK;
+  if (num_pages < 1) return KV_EINVAL;
+  if (!q || !k_pool || !v_pool || !block_table || !seq_lens || !out || !lse) return KV_EINVAL;
+  if (((uintptr_t)q | (uintptr_t)k_pool | (uintptr_t)v_pool | (uintptr_t)out) & 15) return KV_EINVAL;
+  if ((uintptr_t)status & 3) return KV_EINVAL;
+  KernelConfig k;
+  int rc = kernel_config(Hq, Hkv, d, dtype, &k);
+  if (rc) return rc;
+  const long long n_workers = (long long)k.num_sms * k.blocks_per_sm;
+  const DecodeLayout L = decode_layout(B, Hq, Hkv, d, max_pages, page_size, pages_per_split, n_workers);
+  if (L.total > kNoAllocScratchBytes) return KV_EWORKSPACE;  // beyond the fixed scratch
+  void* scratch = nullptr;
+  rc = noalloc_scratch(&scratch);
+  if (rc) return rc;
+  uint8_t* w = static_cast<uint8_t*>(scratch);
+  // The array keeps the previous call's contents: zero the tickets (and
+  // offsets) this call relies on, and the caller's status word.
+  KV_CUDA_CHECK(cudaMemsetAsync(w, 0, L.part_o, stream));
+  KV_CUDA_CHECK(cudaMemsetAsync(status, 0, sizeof(int32_t), stream));
+
+  DecodeParams dp{};
+  dp.page_off = nullptr;
+  if (B > kFusedMaxB) {
+    OffsetsArgs oa{};
+    oa.seq_lens = seq_lens;
+    oa.B = B;
+    oa.page_size = page_size;
+    oa.max_pages = max_pages;
+    oa.page_off = reinterpret_cast<int32_t*>(w + L.page_off);
+    oa.status = status;
+    KV_CUDA_CHECK(launch_page_offsets(oa, stream));
+    dp.page_off = oa.page_off;
+  }
+  dp.q = static_cast<const uint8_t*>(q);
+  dp.k_pool = static_cast<const uint8_t*>(k_pool);
+  dp.v_pool = static_cast<const uint8_t*>(v_pool);
+  dp.table = block_table;
+  dp.seq_lens = seq_lens;
+  dp.out = out;
+  dp.lse = lse;
+  dp.part_o = reinterpret_cast<float*>(w + L.part_o);
+  dp.part_lse = reinterpret_cast<float*>(w + L.part_lse);
+  dp.row_done = reinterpret_cast<int32_t*>(w + L.row_done);
+  dp.group_done = reinterpret_cast<int32_t*>(w + L.group_done);
+  dp.status = status;
+  dp.chunk_req = pages_per_split;
+  dp.max_slots = L.max_slots;
+  dp.B = B;
+  dp.num_pages = num_pages;
+  dp.max_pages = max_pages;
+  dp.Hq = Hq;
+  dp.Hkv = Hkv;
+  dp.stages = k.stages;
+  dp.min_chunk = kMinChunk;
+  dp.scale_log2 = scale * 1.4426950408889634f;
+  dp.kv_bytes = k.kv_bytes;
+  dp.q_bytes = k.q_bytes;
+  dp.stage_bytes = k.stage_bytes;
+  dp.off_pbuf = k.off_pbuf;
+  dp.off_offsets = k.off_offsets;
+  dp.off_stages = k.off_stages;
+  KV_CUDA_CHECK(launch(k.fn, dim3((unsigned)n_workers), dim3((unsigned)k.threads), k.smem, stream,
+                       true, dp));
+  return KV_OK;
+}
+
+}  // namespace
+}  // namespace kvb
+
+extern "C" int kv_decode_noalloc(const void* q, const void* k_pool, const void* v_pool,
+                                 int num_pages, const int32_t* block_table, int max_pages,
+                                 const int32_t* seq_lens, int B, int page_size, int Hq, int Hkv,
+                                 int d, int dtype, float scale, int pages_per_split, float* out,
+                                 float* lse, int32_t* status, void* stream) {
+  return kvb::decode_noalloc(q, k_pool, v_pool, num_pages, block_table, max_pages, seq_lens, B,
+                             page_size, Hq, Hkv, d, dtype, scale, pages_per_split, out, lse, status,
+                             static_cast<cudaStream_t>(stream));
+}

@@ -69,6 +69,7 @@ _SIGS = {
     "kv_decode_num_workers": ([I, I, I, I, I], I),
     "kv_decode_workspace_size": ([I, I, I, I, I, I, I], SZ),
     "kv_decode": ([P, P, P, I, P, I, P, I, I, I, I, I, I, F, I, P, P, P, SZ, P], I),
+    "kv_decode_noalloc": ([P, P, P, I, P, I, P, I, I, I, I, I, I, F, I, P, P, P, P], I),
     "kv_decode_hostio_workspace_size": ([I, I, I, I, I, I, I], SZ),
     "kv_decode_hostio": ([P, P, P, I, P, I, P, I, I, I, I, I, I, F, I, P, P, P, SZ, P], I),
     "kv_workqueue_workspace_size": ([I], SZ),
@@ -207,6 +208,22 @@ def prepare_decode(q, k_pool, v_pool, block_table, seq_lens, scale, out, lse, ws
         return fn(*cargs)
 
     return call
+
+
+def kv_decode_noalloc(q, k_pool, v_pool, block_table, seq_lens, scale, out, lse, status,
+                      pages_per_split=0, stream=None):
+    """kv_decode without a workspace, for callers that cannot allocate device
+    memory: scratch lives in the library's fixed 16 MiB device array.
+    `status` is a 1-element int32 device tensor that receives the first
+    device-side error code (0 if none).  Calls that overlap on the GPU race
+    on the shared scratch."""
+    B, Hq, d = q.shape
+    P_, Hkv, ps, _ = k_pool.shape
+    rc = lib().kv_decode_noalloc(_p(q), _p(k_pool), _p(v_pool), P_, _p(block_table),
+                                 block_table.shape[1], _p(seq_lens), B, ps, Hq, Hkv, d,
+                                 dtype_code(q), float(scale), int(pages_per_split), _p(out),
+                                 _p(lse), _p(status), _s(stream))
+    _check(rc, "kv_decode_noalloc")
 
 
 def kv_decode_hostio_workspace_size(B, Hq, Hkv, d, max_pages, page_size=16, pages_per_split=0):
