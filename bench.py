@@ -126,6 +126,7 @@ def oracle_sample(x: W.DecodeInputs, heads: int = 2):
     """A bounded sample of the workload for the CPU oracle: every sequence,
     the first `heads` KV heads (with their query heads)."""
     G = x.Hq // x.Hkv
+    heads = min(heads, x.Hkv)
     y = W.DecodeInputs(name=x.name + "_sample", B=x.B, Hq=heads * G, Hkv=heads, d=x.d,
                        page_size=x.page_size, dtype=x.dtype, scale=x.scale,
                        q=np.ascontiguousarray(x.q[:, : heads * G]),
@@ -264,15 +265,12 @@ def run_ours(args, x, name, rank, world):
     t_step = sum(step_ms) / n / 1e3
     t_kern = sum(kern_ms) / n / 1e3
     t_e2e = statistics.median(e2e_t)
-    if world > 1:
-        tt = torch.tensor([t_step, t_e2e, t_kern], device=dev, dtype=torch.float64)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        t_step, t_e2e, t_kern = tt.tolist()
+    t_step, t_e2e, t_kern = max_over_ranks([t_step, t_e2e, t_kern], world, dev)
     if rank != 0:
         return
     nbytes = x.algorithmic_bytes()
     peak, peak_kind = measured_peaks()
-    value = world * nbytes / t_step / 1e9
+    value = whole_job_gbs(nbytes, t_step, world)
     achieved = nbytes / t_kern / 1e9
     traffic = None
     prof = os.path.join(ROOT, "profiles", f"decode_{name}_traffic.txt")
@@ -310,6 +308,25 @@ def run_ours(args, x, name, rank, world):
     if not args.no_cpu_baseline:
         line["cpu_baseline"] = time_oracle(x, 1, 0)
     print(json.dumps(line), flush=True)
+
+
+def max_over_ranks(values, world, device):
+    """Element-wise maximum of per-rank timings over all ranks (the slowest
+    replica sets the job's time); identity for one rank."""
+    if world <= 1:
+        return list(values)
+    import torch
+    import torch.distributed as dist
+
+    t = torch.tensor(values, device=device, dtype=torch.float64)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return t.tolist()
+
+
+def whole_job_gbs(bytes_per_replica, t_step_max, world):
+    """Whole-job throughput: every replica moves bytes_per_replica per step,
+    the job's step takes the slowest replica's time."""
+    return world * bytes_per_replica / t_step_max / 1e9
 
 
 def launches_per_step(B):

@@ -305,55 +305,101 @@ __global__ void __launch_bounds__(kDecodeThreadsMax, 1) decode_kernel(const Deco
   // Merge n partials of this head (partial i in slot slot_of(i)):
   //   L = log2 sum_i 2^{lse_i},  o = sum_i 2^{lse_i - L} o_i
   // into the final out/lse of sequence b (natural-log lse) or into the
-  // partial slot dst_slot (normalised o, base-2 lse).
+  // partial slot dst_slot (normalised o, base-2 lse).  Up to 32 parts: lane
+  // i reads part i's lse once and holds its weights, which the accumulation
+  // takes by shuffle while it keeps four parts' loads in flight.
   auto merge = [&](int n, auto slot_of, int b, long long dst_slot) {
-    float mx[G], sum[G], L2[G];
-#pragma unroll
-    for (int g = 0; g < G; ++g) { mx[g] = -INFINITY; sum[g] = 0.f; }
-    for (int i = lane; i < n; i += 32) {
-      const float* pl = p.part_lse + part_index(slot_of(i)) * G;
-#pragma unroll
-      for (int g = 0; g < G; ++g) mx[g] = fmaxf(mx[g], __ldcg(pl + g));
-    }
-#pragma unroll
-    for (int g = 0; g < G; ++g)
-#pragma unroll
-      for (int off = 16; off; off >>= 1) mx[g] = fmaxf(mx[g], __shfl_xor_sync(FULL, mx[g], off));
-    for (int i = lane; i < n; i += 32) {
-      const float* pl = p.part_lse + part_index(slot_of(i)) * G;
-#pragma unroll
-      for (int g = 0; g < G; ++g) sum[g] += ex2(__ldcg(pl + g) - mx[g]);
-    }
-#pragma unroll
-    for (int g = 0; g < G; ++g) {
-#pragma unroll
-      for (int off = 16; off; off >>= 1) sum[g] += __shfl_xor_sync(FULL, sum[g], off);
-      L2[g] = mx[g] + log2f(sum[g]);
-    }
     float acc[G][CPL];
 #pragma unroll
     for (int g = 0; g < G; ++g)
 #pragma unroll
       for (int c = 0; c < CPL; ++c) acc[g][c] = 0.f;
-#pragma unroll 2
-    for (int i = 0; i < n; ++i) {
-      const size_t t = part_index(slot_of(i));
-      const float* pl = p.part_lse + t * G;
-      const float* po = p.part_o + t * G * D + lane * CPL;
+    float L2[G];
+    auto accumulate = [&](int i, const float* w) {
+      const float* po = p.part_o + part_index(slot_of(i)) * G * D + lane * CPL;
 #pragma unroll
       for (int g = 0; g < G; ++g) {
-        const float w = ex2(__ldcg(pl + g) - L2[g]);
         if constexpr (CPL == 4) {
           const float4 v = __ldcg(reinterpret_cast<const float4*>(po + (size_t)g * D));
-          acc[g][0] = fmaf(w, v.x, acc[g][0]);
-          acc[g][1] = fmaf(w, v.y, acc[g][1]);
-          acc[g][2] = fmaf(w, v.z, acc[g][2]);
-          acc[g][3] = fmaf(w, v.w, acc[g][3]);
+          acc[g][0] = fmaf(w[g], v.x, acc[g][0]);
+          acc[g][1] = fmaf(w[g], v.y, acc[g][1]);
+          acc[g][2] = fmaf(w[g], v.z, acc[g][2]);
+          acc[g][3] = fmaf(w[g], v.w, acc[g][3]);
         } else {
           const float2 v = __ldcg(reinterpret_cast<const float2*>(po + (size_t)g * D));
-          acc[g][0] = fmaf(w, v.x, acc[g][0]);
-          acc[g][1] = fmaf(w, v.y, acc[g][1]);
+          acc[g][0] = fmaf(w[g], v.x, acc[g][0]);
+          acc[g][1] = fmaf(w[g], v.y, acc[g][1]);
         }
+      }
+    };
+    if (n <= 32) {
+      float lv[G], wl[G];
+#pragma unroll
+      for (int g = 0; g < G; ++g) lv[g] = -INFINITY;
+      if (lane < n) {
+        const float* pl = p.part_lse + part_index(slot_of(lane)) * G;
+#pragma unroll
+        for (int g = 0; g < G; ++g) lv[g] = __ldcg(pl + g);
+      }
+#pragma unroll
+      for (int g = 0; g < G; ++g) {
+        float mx = lv[g];
+#pragma unroll
+        for (int off = 16; off; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(FULL, mx, off));
+        float e = lane < n ? ex2(lv[g] - mx) : 0.f;
+        float sum = e;
+#pragma unroll
+        for (int off = 16; off; off >>= 1) sum += __shfl_xor_sync(FULL, sum, off);
+        L2[g] = mx + log2f(sum);
+        wl[g] = lane < n ? ex2(lv[g] - L2[g]) : 0.f;
+      }
+      int i = 0;
+      for (; i + 4 <= n; i += 4) {
+        float w[4][G];
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+#pragma unroll
+          for (int g = 0; g < G; ++g) w[j][g] = __shfl_sync(FULL, wl[g], i + j);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) accumulate(i + j, w[j]);
+      }
+      for (; i < n; ++i) {
+        float w[G];
+#pragma unroll
+        for (int g = 0; g < G; ++g) w[g] = __shfl_sync(FULL, wl[g], i);
+        accumulate(i, w);
+      }
+    } else {
+      float mx[G], sum[G];
+#pragma unroll
+      for (int g = 0; g < G; ++g) { mx[g] = -INFINITY; sum[g] = 0.f; }
+      for (int i = lane; i < n; i += 32) {
+        const float* pl = p.part_lse + part_index(slot_of(i)) * G;
+#pragma unroll
+        for (int g = 0; g < G; ++g) mx[g] = fmaxf(mx[g], __ldcg(pl + g));
+      }
+#pragma unroll
+      for (int g = 0; g < G; ++g)
+#pragma unroll
+        for (int off = 16; off; off >>= 1) mx[g] = fmaxf(mx[g], __shfl_xor_sync(FULL, mx[g], off));
+      for (int i = lane; i < n; i += 32) {
+        const float* pl = p.part_lse + part_index(slot_of(i)) * G;
+#pragma unroll
+        for (int g = 0; g < G; ++g) sum[g] += ex2(__ldcg(pl + g) - mx[g]);
+      }
+#pragma unroll
+      for (int g = 0; g < G; ++g) {
+#pragma unroll
+        for (int off = 16; off; off >>= 1) sum[g] += __shfl_xor_sync(FULL, sum[g], off);
+        L2[g] = mx[g] + log2f(sum[g]);
+      }
+#pragma unroll 2
+      for (int i = 0; i < n; ++i) {
+        const float* pl = p.part_lse + part_index(slot_of(i)) * G;
+        float w[G];
+#pragma unroll
+        for (int g = 0; g < G; ++g) w[g] = ex2(__ldcg(pl + g) - L2[g]);
+        accumulate(i, w);
       }
     }
     __syncwarp();  // every lane has read the sources before any overwrite
