@@ -132,6 +132,15 @@ __global__ void __launch_bounds__(kDecodeThreadsMax, 1) decode_kernel(const Deco
   pdl_launch_dependents();
 
   // ---- prologue: page offsets, chunk size, outputs of empty sequences
+  // Every producer reads block-table entries right after the offsets: have
+  // the table on its way to L2 meanwhile (spread over all CTAs).
+  {
+    const size_t lines = ((size_t)B * p.max_pages * 4 + 127) / 128;
+    const char* tb = reinterpret_cast<const char*>(p.table);
+    for (size_t i = (size_t)blockIdx.x * nth + tid; i < lines && i < (1u << 20);
+         i += (size_t)gridDim.x * nth)
+      prefetch_l2(tb + i * 128);
+  }
   const int32_t* O;
   if (p.page_off) {
     O = p.page_off;
@@ -288,19 +297,20 @@ __global__ void __launch_bounds__(kDecodeThreadsMax, 1) decode_kernel(const Deco
   auto part_index = [&](long long slot) { return (size_t)slot * p.Hkv + h; };
 
   // Ticket on a completion counter of n arrivals: true for the last one.
+  // The warp's partial writes are ordered before the ticket by the warp
+  // barrier and published by the atomic's release; the winner's acquire
+  // orders its reads of the other splits' partials after it.
   auto ticket = [&](int32_t* ctr, int n) -> bool {
-    __threadfence();
     __syncwarp();
     int prev = 0;
-    if (lane == 0) prev = atomicAdd(ctr, 1);
+    if (lane == 0) prev = atom_add_acq_rel_gpu(ctr, 1);
     prev = __shfl_sync(FULL, prev, 0);
+    __syncwarp();
     if (prev >= n) {  // the counter did not start at zero
       if (lane == 0) set_status(p.status, KV_EWORKSPACE);
       return false;
     }
-    if (prev != n - 1) return false;
-    __threadfence();
-    return true;
+    return prev == n - 1;
   };
   // Merge n partials of this head (partial i in slot slot_of(i)):
   //   L = log2 sum_i 2^{lse_i},  o = sum_i 2^{lse_i - L} o_i
