@@ -268,7 +268,9 @@ int kv_select_pages(const float *scores, const int32_t *seq_lens, const uint8_t 
                     uint8_t *keep_mask, uint8_t *grow, int32_t *drift, void *ws, size_t ws_bytes,
                     void *stream);
 
-size_t kv_compact_workspace_size(int B, int max_pages, int page_size, int token_granular);
+/* num_pages: the pool's page count when kv_compact will be given refcnt
+ * (shared pages), else 0. */
+size_t kv_compact_workspace_size(int B, int max_pages, int num_pages, int token_granular);
 
 /* Stable compaction [GP] with the free list of [EKV]: the kept tokens of
  * each sequence (keep_mask [B][max_pages] per page, or [B][max_pages*16]
@@ -279,23 +281,37 @@ size_t kv_compact_workspace_size(int B, int max_pages, int page_size, int token_
  * the tokens' K and V (all heads) are copied there.  Old pages not reused
  * are then pushed in (b, j) order.  block_table rows are rewritten (-1
  * padded), seq_lens become the kept counts, *free_top is updated.
- * free_list has num_pages entries (device).  Device errors: KV_ENOSPACE
- * (nothing is changed), KV_EBADPAGE. */
+ * free_list has num_pages entries (device).
+ * Shared pages (prefix caching, which GrowPage keeps [GP]): refcnt [num_pages]
+ * int32 (device, or NULL when every page belongs to one sequence) holds each
+ * pool page's number of block-table references.  A fresh page gets 1; every
+ * old page not reused loses one reference, in (b, j) order, and is pushed
+ * when none is left (by the reference that takes it to zero).  Kept pages are
+ * never written, so a page other sequences still use is left as it is.
+ * Device errors: KV_ENOSPACE (nothing is changed), KV_EBADPAGE. */
 int kv_compact(int32_t *block_table, int max_pages, int32_t *seq_lens, const uint8_t *keep_mask,
                int token_granular, void *k_pool, void *v_pool, int num_pages, int32_t *free_list,
-               int32_t *free_top, int B, int Hkv, int d, int page_size, int dtype, void *ws,
-               size_t ws_bytes, void *stream);
+               int32_t *free_top, int32_t *refcnt, int B, int Hkv, int d, int page_size, int dtype,
+               void *ws, size_t ws_bytes, void *stream);
 
 size_t kv_append_workspace_size(int B);
 
 /* Append one token per sequence: K/V (k_new, v_new [B][Hkv][d], device) go
  * to slot L_b % 16 of page block_table[b][L_b / 16]; when L_b % 16 == 0 that
  * page is first popped from the free list (pops in ascending b).  Then
- * L_b += 1.  Device errors (nothing is changed): KV_ENOSPACE, KV_EFULL. */
+ * L_b += 1.  With refcnt (shared pages, as for kv_compact; NULL = none), a
+ * sequence whose partly filled last page is shared copies it first
+ * (copy-on-write): in ascending b, while the page has more than one
+ * reference left, the sequence pops a fresh page (same pop order), the
+ * page's filled slots (K and V, all heads) are copied there, its table entry
+ * moves to the fresh page and the shared page loses one reference; the last
+ * sharer writes in place.  Popped pages get count 1.  All copies are made
+ * before any token is written.  Device errors (nothing is changed):
+ * KV_ENOSPACE, KV_EFULL, KV_EBADPAGE. */
 int kv_append(const void *k_new, const void *v_new, void *k_pool, void *v_pool, int num_pages,
               int32_t *block_table, int max_pages, int32_t *seq_lens, int32_t *free_list,
-              int32_t *free_top, int B, int Hkv, int d, int page_size, int dtype, void *ws,
-              size_t ws_bytes, void *stream);
+              int32_t *free_top, int32_t *refcnt, int B, int Hkv, int d, int page_size, int dtype,
+              void *ws, size_t ws_bytes, void *stream);
 
 #ifdef __cplusplus
 }

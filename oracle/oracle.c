@@ -678,10 +678,16 @@ int or_select_pages(const float *scores, const int32_t *seq_lens, const uint8_t 
  * -3 is returned.  The K/V of every token placed in a fresh page is copied
  * there (all KV heads).  Old pages that are not reused are then pushed in
  * (b, j) order.  The row is rewritten (-1 padded) and L_b = kept count.
- * free_list has room for num_pages entries.                                  */
+ * free_list has room for num_pages entries.
+ * Shared pages (prefix caching, GrowPage Abstract): when refcnt is not NULL
+ * it holds each pool page's number of block-table references.  A fresh page
+ * gets count 1; each old page that is not reused loses one reference, in
+ * (b, j) order, and is pushed when its count reaches 0.  Kept pages are never
+ * written, so a page another sequence still uses is never modified.          */
 int or_compact(int32_t *table, int max_pages, int32_t *seq_lens, const uint8_t *keep,
                int token_granular, uint16_t *k_pool, uint16_t *v_pool, int num_pages,
-               int32_t *free_list, int32_t *free_top, int B, int Hkv, int d, int ps) {
+               int32_t *free_list, int32_t *free_top, int32_t *refcnt, int B, int Hkv, int d,
+               int ps) {
   int64_t mask_w = token_granular ? (int64_t)max_pages * ps : max_pages;
   int64_t total_fresh = 0;
   /* pass 1: count fresh pages */
@@ -733,6 +739,7 @@ int or_compact(int32_t *table, int max_pages, int32_t *seq_lens, const uint8_t *
           int32_t fresh = free_list[top - 1 - pops];
           ++pops;
           newrow[m] = fresh;
+          if (refcnt) refcnt[fresh] = 1;
           for (int64_t s = 0; s < cnt; ++s) {
             int64_t t = kept[b][m * ps + s];
             int32_t src = table[(size_t)b * max_pages + t / ps];
@@ -752,7 +759,15 @@ int or_compact(int32_t *table, int max_pages, int32_t *seq_lens, const uint8_t *
       seq_lens[b] = (int32_t)nkept[b];
     }
     top -= pops;
-    for (int64_t i = 0; i < nfreed; ++i) free_list[top++] = freed[i];
+    /* With shared pages, a freed reference only drops the page's count; the
+     * page returns to the free list when its last reference goes. */
+    for (int64_t i = 0; i < nfreed; ++i) {
+      if (refcnt) {
+        refcnt[freed[i]] -= 1;
+        if (refcnt[freed[i]] != 0) continue;
+      }
+      free_list[top++] = freed[i];
+    }
     *free_top = (int32_t)top;
     free(newrow);
     free(reused);
@@ -767,16 +782,20 @@ out:
 }
 
 /* ------------------------------------------------------------------------ */
-/* Append: write the new token's K/V at slot L_b % ps of page               */
+/* Append: write the new token's K/V at slot L_b % ps of page             */
 /* block_table[b][L_b / ps]; when L_b % ps == 0 the page is first popped     */
 /* from the free list (pops in ascending b).  Then L_b += 1.  Nothing        */
 /* changes on an error: a full row (-6), else a bad page id in use or about  */
 /* to be popped (-2), else too few free pages (-3).                          */
 /* k_new, v_new: [B][Hkv][d].                                                 */
-/* ------------------------------------------------------------------------ */
+/* Shared pages: with refcnt (not NULL), a sequence whose last page is       */
+/* partly filled and shared (count > 1) first copies it (copy-on-write): it  */
+/* pops a fresh page in the same ascending-b order, copies the page's first  */
+/* L_b % ps slots (K and V, all heads) there, points its table entry at it,  */
+/* drops one reference from the shared page; popped pages get count 1.      */
 int or_append(const uint16_t *k_new, const uint16_t *v_new, uint16_t *k_pool, uint16_t *v_pool,
               int num_pages, int32_t *table, int max_pages, int32_t *seq_lens, int32_t *free_list,
-              int32_t *free_top, int B, int Hkv, int d, int ps) {
+              int32_t *free_top, int32_t *refcnt, int B, int Hkv, int d, int ps) {
   /* checks first, in this order of precedence: a full row, a bad page id (one
    * in use, or one that would be popped), too few free pages */
   int64_t need = 0;
@@ -791,6 +810,7 @@ int or_append(const uint16_t *k_new, const uint16_t *v_new, uint16_t *k_pool, ui
     } else {
       int32_t p = table[(size_t)b * max_pages + L / ps];
       if (p < 0 || p >= num_pages) bad = 1;
+      else if (refcnt && refcnt[p] > 1) ++need;
     }
   }
   if (need <= *free_top)
@@ -802,10 +822,24 @@ int or_append(const uint16_t *k_new, const uint16_t *v_new, uint16_t *k_pool, ui
   if (bad) return OR_EBADPAGE;
   if (need > *free_top) return OR_ENOSPACE;
   int64_t top = *free_top;
+  size_t tile = (size_t)ps * d; /* elements of one (page, head) tile */
   for (int b = 0; b < B; ++b) {
     int64_t L = seq_lens[b];
     int32_t *slot = &table[(size_t)b * max_pages + L / ps];
-    if (L % ps == 0) *slot = free_list[--top];
+    if (L % ps == 0) {
+      *slot = free_list[--top];
+      if (refcnt) refcnt[*slot] = 1;
+    } else if (refcnt && refcnt[*slot] > 1) {
+      int32_t old = *slot, fresh = free_list[--top];
+      for (int h = 0; h < Hkv; ++h) {
+        size_t so = ((size_t)old * Hkv + h) * tile, dst = ((size_t)fresh * Hkv + h) * tile;
+        memcpy(k_pool + dst, k_pool + so, sizeof(uint16_t) * (size_t)(L % ps) * d);
+        memcpy(v_pool + dst, v_pool + so, sizeof(uint16_t) * (size_t)(L % ps) * d);
+      }
+      refcnt[old] -= 1;
+      refcnt[fresh] = 1;
+      *slot = fresh;
+    }
     int32_t p = *slot;
     for (int h = 0; h < Hkv; ++h) {
       size_t dst = (((size_t)p * Hkv + h) * ps + (size_t)(L % ps)) * d;

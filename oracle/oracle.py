@@ -86,9 +86,9 @@ def _declare(L):
     L.or_score_pages_f64.restype = I
     L.or_select_pages.argtypes = [P, P, P, P, I, I, I, I, I, F, F, I, I, P, P, P]
     L.or_select_pages.restype = I
-    L.or_compact.argtypes = [P, I, P, P, I, P, P, I, P, P, I, I, I, I]
+    L.or_compact.argtypes = [P, I, P, P, I, P, P, I, P, P, P, I, I, I, I]
     L.or_compact.restype = I
-    L.or_append.argtypes = [P, P, P, P, I, P, I, P, P, P, I, I, I, I]
+    L.or_append.argtypes = [P, P, P, P, I, P, I, P, P, P, P, I, I, I, I]
     L.or_append.restype = I
     L.or_mark_active.argtypes = [P, P, I, I, I, P]
     L.or_mark_active.restype = I
@@ -272,8 +272,9 @@ def select_pages(scores, seq_lens, active, budget, ps, n_first, n_last, delta, m
 
 
 def compact(table, seq_lens, keep, token_granular, k_pool, v_pool, free_list, free_top,
-            Hkv, d, ps):
-    """In-place compaction on copies -> (table, seq_lens, k_pool, v_pool, free_list, free_top, rc)."""
+            Hkv, d, ps, refcnt=None):
+    """In-place compaction on copies -> (table, seq_lens, k_pool, v_pool, free_list, free_top, rc);
+    with refcnt (shared pages) the updated counts are written back into that array."""
     table = _c(table, np.int32).copy()
     seq_lens = _c(seq_lens, np.int32).copy()
     keep = _c(keep, np.uint8)
@@ -282,14 +283,18 @@ def compact(table, seq_lens, keep, token_granular, k_pool, v_pool, free_list, fr
     free_list = _c(free_list, np.int32).copy()
     top = np.array([free_top], dtype=np.int32)
     B, maxp = table.shape
+    if refcnt is not None:
+        assert refcnt.dtype == np.int32 and refcnt.flags.c_contiguous
     rc = lib().or_compact(_p(table), maxp, _p(seq_lens), _p(keep), int(token_granular),
                           _p(k_pool), _p(v_pool), k_pool.shape[0], _p(free_list), _p(top),
-                          B, Hkv, d, ps)
+                          _p(refcnt), B, Hkv, d, ps)
     return table, seq_lens, k_pool, v_pool, free_list, int(top[0]), rc
 
 
-def append(k_new, v_new, k_pool, v_pool, table, seq_lens, free_list, free_top, Hkv, d, ps):
-    """-> (k_pool, v_pool, table, seq_lens, free_list, free_top, rc), all copies."""
+def append(k_new, v_new, k_pool, v_pool, table, seq_lens, free_list, free_top, Hkv, d, ps,
+           refcnt=None):
+    """-> (k_pool, v_pool, table, seq_lens, free_list, free_top, rc), all copies; with refcnt
+    (shared pages) the updated counts are written back into that array."""
     k_pool = _c(k_pool, np.uint16).copy()
     v_pool = _c(v_pool, np.uint16).copy()
     table = _c(table, np.int32).copy()
@@ -297,9 +302,11 @@ def append(k_new, v_new, k_pool, v_pool, table, seq_lens, free_list, free_top, H
     free_list = _c(free_list, np.int32).copy()
     top = np.array([free_top], dtype=np.int32)
     B, maxp = table.shape
+    if refcnt is not None:
+        assert refcnt.dtype == np.int32 and refcnt.flags.c_contiguous
     rc = lib().or_append(_p(_c(k_new, np.uint16)), _p(_c(v_new, np.uint16)), _p(k_pool),
                          _p(v_pool), k_pool.shape[0], _p(table), maxp, _p(seq_lens),
-                         _p(free_list), _p(top), B, Hkv, d, ps)
+                         _p(free_list), _p(top), _p(refcnt), B, Hkv, d, ps)
     return k_pool, v_pool, table, seq_lens, free_list, int(top[0]), rc
 
 
@@ -351,7 +358,7 @@ def source() -> str:
 
 
 def compact_inplace(table, seq_lens, keep, token_granular, k_pool, v_pool, free_list, free_top_arr,
-                    Hkv, d, ps):
+                    Hkv, d, ps, refcnt=None):
     """or_compact on the caller's arrays (all C-contiguous, right dtypes);
     free_top_arr is a 1-element int32 array.  Returns the status."""
     for a, dt in ((table, np.int32), (seq_lens, np.int32), (keep, np.uint8), (k_pool, np.uint16),
@@ -360,11 +367,11 @@ def compact_inplace(table, seq_lens, keep, token_granular, k_pool, v_pool, free_
     B, maxp = table.shape
     return lib().or_compact(_p(table), maxp, _p(seq_lens), _p(keep), int(token_granular),
                             _p(k_pool), _p(v_pool), k_pool.shape[0], _p(free_list),
-                            _p(free_top_arr), B, Hkv, d, ps)
+                            _p(free_top_arr), _p(refcnt), B, Hkv, d, ps)
 
 
 def append_inplace(k_new, v_new, k_pool, v_pool, table, seq_lens, free_list, free_top_arr,
-                   Hkv, d, ps):
+                   Hkv, d, ps, refcnt=None):
     """or_append on the caller's arrays.  Returns the status."""
     for a, dt in ((table, np.int32), (seq_lens, np.int32), (k_pool, np.uint16),
                   (v_pool, np.uint16), (free_list, np.int32), (free_top_arr, np.int32)):
@@ -372,4 +379,4 @@ def append_inplace(k_new, v_new, k_pool, v_pool, table, seq_lens, free_list, fre
     B, maxp = table.shape
     return lib().or_append(_p(_c(k_new, np.uint16)), _p(_c(v_new, np.uint16)), _p(k_pool),
                            _p(v_pool), k_pool.shape[0], _p(table), maxp, _p(seq_lens),
-                           _p(free_list), _p(free_top_arr), B, Hkv, d, ps)
+                           _p(free_list), _p(free_top_arr), _p(refcnt), B, Hkv, d, ps)

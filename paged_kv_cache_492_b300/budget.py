@@ -42,15 +42,17 @@ class BudgetedDecoder:
 
     k_pool, v_pool [P, Hkv, 16, d] (f16/bf16), block_table [B, maxP] int32,
     seq_lens [B] int32, free_list [P] int32 + free_top [1] int32 (stack),
-    budget [B] int32.  All tensors live on one device and are updated in
-    place by the kernels."""
+    budget [B] int32, refcnt [P] int32 (block-table references per pool page,
+    for batches whose sequences share prefix pages; None = no sharing).  All
+    tensors live on one device and are updated in place by the kernels."""
 
     def __init__(self, k_pool, v_pool, block_table, seq_lens, free_list, free_top, budget,
-                 Hq: int, cfg: BudgetConfig, stream=None):
+                 Hq: int, cfg: BudgetConfig, stream=None, refcnt=None):
         self.k_pool, self.v_pool = k_pool, v_pool
         self.table, self.lens = block_table, seq_lens
         self.free_list, self.free_top = free_list, free_top
         self.budget = budget
+        self.refcnt = refcnt
         self.cfg = cfg
         self.stream = stream
         dev = k_pool.device
@@ -67,7 +69,7 @@ class BudgetedDecoder:
         self.out = torch.empty((B, Hq, d), dtype=torch.float32, device=dev)
         self.lse = torch.empty((B, Hq), dtype=torch.float32, device=dev)
         ws = max(kv.kv_select_workspace_size(B, maxp),
-                 kv.kv_compact_workspace_size(B, maxp),
+                 kv.kv_compact_workspace_size(B, maxp, P if refcnt is not None else 0),
                  kv.kv_append_workspace_size(B))
         self.ws = kv.alloc_workspace(ws, dev)
         # kv_decode keeps merge tickets in its workspace between calls
@@ -94,7 +96,8 @@ class BudgetedDecoder:
                            c.delta, c.ws_frac, kv.KV_SELECT_TOPK, self.free_top, self.keep,
                            self.grow, self.drift, self.ws, stream=self.stream)
         kv.kv_compact(self.table, self.lens, self.keep, False, self.k_pool, self.v_pool,
-                      self.free_list, self.free_top, self.ws, stream=self.stream)
+                      self.free_list, self.free_top, self.ws, stream=self.stream,
+                      refcnt=self.refcnt)
 
     def boundary(self):
         """Compress-or-grow for the sequences at a capacity boundary."""
@@ -108,7 +111,8 @@ class BudgetedDecoder:
                            c.delta, c.ws_frac, kv.KV_SELECT_BOUNDARY, self.free_top, self.keep,
                            self.grow, self.drift, self.ws, stream=self.stream)
         kv.kv_compact(self.table, self.lens, self.keep, False, self.k_pool, self.v_pool,
-                      self.free_list, self.free_top, self.ws, stream=self.stream)
+                      self.free_list, self.free_top, self.ws, stream=self.stream,
+                      refcnt=self.refcnt)
 
     def step(self, q, k_new, v_new, t: int):
         """One decode step for token t (q [B, Hq, d], k_new/v_new [B, Hkv, d])."""
@@ -116,6 +120,7 @@ class BudgetedDecoder:
             self.update_summaries(q, False)
         self.boundary()
         kv.kv_append(k_new, v_new, self.k_pool, self.v_pool, self.table, self.lens,
-                     self.free_list, self.free_top, self.ws, stream=self.stream)
+                     self.free_list, self.free_top, self.ws, stream=self.stream,
+                     refcnt=self.refcnt)
         kv.kv_decode(q, self.k_pool, self.v_pool, self.table, self.lens, self.scale, self.out,
                      self.lse, self.decode_ws, stream=self.stream)

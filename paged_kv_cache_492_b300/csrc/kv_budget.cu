@@ -308,6 +308,11 @@ struct CompactArgs {
   long long max_fresh;
   int32_t* ctl;        // [0] abort flag, [1] top after pops
   int* status;
+  // shared pages (refcnt != NULL)
+  int32_t* refcnt;     // [num_pages] block-table references per pool page
+  uint8_t* freed_flag; // [B][max_pages] 1: old page j of b not reused; 2: and pushed
+  int32_t* page_cnt;   // [num_pages] references freed in this call
+  int32_t* page_key;   // [num_pages] largest (b * max_pages + j) freeing the page
 };
 
 // keep bit of token t (valid token of b)
@@ -341,6 +346,13 @@ __global__ void __launch_bounds__(1024) compact_plan_kernel(const CompactArgs a)
   __shared__ long long sm[32];
   __shared__ int s_info[4];
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
+  if (a.refcnt) {
+    for (int pg = threadIdx.x; pg < a.num_pages; pg += blockDim.x) {
+      a.page_cnt[pg] = 0;
+      a.page_key[pg] = -1;
+    }
+    __syncthreads();
+  }
   // per-sequence counts into the workspace (new_len, pop_base <- fresh, push_base <- freed)
   for (int b = warp; b < a.B; b += nw) {
     const int L = a.seq_lens[b];
@@ -370,6 +382,18 @@ __global__ void __launch_bounds__(1024) compact_plan_kernel(const CompactArgs a)
       const bool reuse = j < np && c > 0 && pre && (kb % a.ps == 0) && (c == a.ps || kb + c == K);
       reused += __popc(__ballot_sync(FULL, reuse));
       kept_before += __shfl_sync(FULL, x, 31);
+      if (a.refcnt && j < np) {
+        a.freed_flag[(size_t)b * a.max_pages + j] = reuse ? 0 : 1;
+        if (!reuse) {
+          const int pg = a.table[(size_t)b * a.max_pages + j];
+          if (pg >= 0 && pg < a.num_pages) {
+            atomicAdd(&a.page_cnt[pg], 1);
+            atomicMax(&a.page_key[pg], b * a.max_pages + j);
+          } else {
+            set_status(a.status, KV_EBADPAGE);
+          }
+        }
+      }
     }
     if (lane == 0) {
       const int n_new = (int)ceil_div_ll(K, a.ps);
@@ -379,6 +403,30 @@ __global__ void __launch_bounds__(1024) compact_plan_kernel(const CompactArgs a)
     }
   }
   __syncthreads();
+  if (a.refcnt) {
+    // A freed page goes back on the free list with the reference that takes
+    // its count to zero: the last one in (b, j) order, if the call frees all
+    // of them.  That reference also lowers the count by the call's total.
+    for (int b = warp; b < a.B; b += nw) {
+      const int np = (int)ceil_div_ll(a.seq_lens[b], a.ps);
+      int pushed = 0;
+      for (int j0 = 0; j0 < np; j0 += 32) {
+        const int j = j0 + lane;
+        bool push = false;
+        if (j < np && a.freed_flag[(size_t)b * a.max_pages + j]) {
+          const int pg = a.table[(size_t)b * a.max_pages + j];
+          if (pg >= 0 && pg < a.num_pages && a.page_key[pg] == b * a.max_pages + j) {
+            push = a.page_cnt[pg] == a.refcnt[pg];
+            a.refcnt[pg] -= a.page_cnt[pg];
+            if (push) a.freed_flag[(size_t)b * a.max_pages + j] = 2;
+          }
+        }
+        pushed += __popc(__ballot_sync(FULL, push));
+      }
+      if (lane == 0) a.push_base[b] = pushed;
+    }
+    __syncthreads();
+  }
   // exclusive scans over b (single block, sequential chunks)
   if (threadIdx.x == 0) {
     s_info[0] = 0;
@@ -420,7 +468,11 @@ __global__ void __launch_bounds__(1024) compact_plan_kernel(const CompactArgs a)
     }
     return;
   }
-  for (int i = threadIdx.x; i < pops; i += blockDim.x) a.fresh_ids[i] = a.free_list[top - 1 - i];
+  for (int i = threadIdx.x; i < pops; i += blockDim.x) {
+    const int pg = a.free_list[top - 1 - i];
+    a.fresh_ids[i] = pg;
+    if (a.refcnt && pg >= 0 && pg < a.num_pages) a.refcnt[pg] = 1;
+  }
   __syncthreads();
   if (threadIdx.x == 0) {
     a.ctl[0] = 0;
@@ -489,6 +541,8 @@ __global__ void __launch_bounds__(kApplyThreads) compact_apply_kernel(const Comp
     if (j < np) {
       const int m = kb_arr[j] / a.ps;
       freed = !(m < a.max_pages && dest_src[m] == j && (kb_arr[j] % a.ps) == 0);
+      // with shared pages only the reference that frees the page pushes it
+      if (a.refcnt) freed = a.freed_flag[(size_t)b * a.max_pages + j] == 2;
     }
     const unsigned bal = __ballot_sync(FULL, freed);
     const int x = __popc(bal & ((1u << lane) - 1u));
@@ -609,6 +663,10 @@ struct AppendArgs {
   int2* dest;    // [B] (page, slot) workspace
   int32_t* ctl;  // [0] abort
   int* status;
+  // shared pages (refcnt != NULL)
+  int32_t* refcnt;   // [num_pages] block-table references per pool page
+  int32_t* cand;     // [B] shared, partly filled last page of b, or -1
+  int32_t* cow_src;  // [B] page b copies before writing (copy-on-write), or -1
 };
 
 __global__ void __launch_bounds__(1024) append_plan_kernel(const AppendArgs a) {
@@ -622,6 +680,7 @@ __global__ void __launch_bounds__(1024) append_plan_kernel(const AppendArgs a) {
   int my_need = 0;
   for (int b = threadIdx.x; b < a.B; b += blockDim.x) {
     const int L = a.seq_lens[b];
+    int cand = -1;
     if (L < 0) {
       s_err[1] = 1;
     } else if (L % a.ps == 0) {
@@ -630,6 +689,25 @@ __global__ void __launch_bounds__(1024) append_plan_kernel(const AppendArgs a) {
     } else {
       const int p = a.table[(size_t)b * a.max_pages + L / a.ps];
       if (p < 0 || p >= a.num_pages) s_err[1] = 1;
+      else if (a.refcnt && a.refcnt[p] > 1) cand = p;
+    }
+    if (a.refcnt) a.cand[b] = cand;
+  }
+  if (a.refcnt) {
+    // Copy-on-write in ascending b: sequence b copies its shared last page p
+    // unless the sharers before it have already copied so that it is the
+    // only reference left (then it writes in place).
+    __syncthreads();
+    for (int b = threadIdx.x; b < a.B; b += blockDim.x) {
+      const int p = a.cand[b];
+      int cow = -1;
+      if (p >= 0) {
+        int rank = 0;
+        for (int b2 = 0; b2 < b; ++b2) rank += a.cand[b2] == p;
+        if (a.refcnt[p] - rank > 1) cow = p;
+      }
+      a.cow_src[b] = cow;
+      my_need += cow >= 0;
     }
   }
   int need = my_need;
@@ -658,7 +736,8 @@ __global__ void __launch_bounds__(1024) append_plan_kernel(const AppendArgs a) {
   for (int base = 0; base < a.B; base += blockDim.x) {
     const int b = base + threadIdx.x;
     const int L = b < a.B ? a.seq_lens[b] : 1;
-    const bool nd = b < a.B && L % a.ps == 0;
+    const bool cow = a.refcnt && b < a.B && a.cow_src[b] >= 0;
+    const bool nd = b < a.B && (L % a.ps == 0 || cow);
     const unsigned bal = __ballot_sync(FULL, nd);
     const int x = __popc(bal & ((1u << lane) - 1u));
     __syncthreads();
@@ -669,7 +748,14 @@ __global__ void __launch_bounds__(1024) append_plan_kernel(const AppendArgs a) {
     const int carry = s_carry;
     if (b < a.B) {
       int32_t* slot = &a.table[(size_t)b * a.max_pages + L / a.ps];
-      if (nd) *slot = a.free_list[top - 1 - (carry + before + x)];
+      if (nd) {
+        const int fresh = a.free_list[top - 1 - (carry + before + x)];
+        if (a.refcnt) {
+          a.refcnt[fresh] = 1;
+          if (cow) atomicSub(&a.refcnt[*slot], 1);
+        }
+        *slot = fresh;
+      }
       a.dest[b] = make_int2(*slot, L % a.ps);
       a.seq_lens[b] = L + 1;
     }
@@ -684,6 +770,27 @@ __global__ void __launch_bounds__(1024) append_plan_kernel(const AppendArgs a) {
   if (threadIdx.x == 0) {
     a.ctl[0] = 0;
     *a.free_top = top - total;
+  }
+}
+
+// Copy-on-write: the filled slots of the shared page b leaves, into its
+// fresh page (all heads, K and V).  Runs before any token is written, so a
+// sharer that writes into the old page in place cannot race with the copy.
+__global__ void append_cow_kernel(const AppendArgs a) {
+  if (a.ctl[0]) return;
+  const int b = blockIdx.x;
+  const int src = a.cow_src[b];
+  if (src < 0) return;
+  const int2 dst = a.dest[b];
+  const size_t row_bytes = (size_t)a.d * 2;
+  const int vec = (int)(row_bytes / 16);
+  const int n = dst.y * vec;  // filled slots x 16-byte pieces per row
+  for (int i = threadIdx.x; i < a.Hkv * n; i += blockDim.x) {
+    const int h = i / n, r = i - h * n;
+    const size_t so = ((size_t)src * a.Hkv + h) * a.ps * row_bytes + (size_t)r * 16;
+    const size_t dof = ((size_t)dst.x * a.Hkv + h) * a.ps * row_bytes + (size_t)r * 16;
+    *reinterpret_cast<uint4*>(a.k_pool + dof) = *reinterpret_cast<const uint4*>(a.k_pool + so);
+    *reinterpret_cast<uint4*>(a.v_pool + dof) = *reinterpret_cast<const uint4*>(a.v_pool + so);
   }
 }
 
@@ -851,33 +958,37 @@ int kv_select_pages(const float* scores, const int32_t* seq_lens, const uint8_t*
   return KV_OK;
 }
 
-static void compact_layout(int B, int max_pages, size_t* off_new_len, size_t* off_pop,
-                           size_t* off_push, size_t* off_ctl, size_t* off_fresh, long long* max_fresh,
-                           size_t* total) {
+struct CompactLayout {
+  size_t new_len, pop, push, ctl, fresh, freed_flag, page_cnt, page_key, total;
+  long long max_fresh;
+};
+static CompactLayout compact_layout(int B, int max_pages, int num_pages) {
+  CompactLayout L{};
   size_t off = kHeaderBytes;
   const size_t nb = (size_t)(B > 0 ? B : 1);
-  *off_new_len = ws_take(&off, nb * 4);
-  *off_pop = ws_take(&off, nb * 4);
-  *off_push = ws_take(&off, nb * 4);
-  *off_ctl = ws_take(&off, 16);
-  *max_fresh = (long long)nb * (max_pages > 0 ? max_pages : 1);
-  *off_fresh = ws_take(&off, (size_t)*max_fresh * 4);
-  *total = off;
+  L.new_len = ws_take(&off, nb * 4);
+  L.pop = ws_take(&off, nb * 4);
+  L.push = ws_take(&off, nb * 4);
+  L.ctl = ws_take(&off, 16);
+  L.max_fresh = (long long)nb * (max_pages > 0 ? max_pages : 1);
+  L.fresh = ws_take(&off, (size_t)L.max_fresh * 4);
+  // shared pages only (num_pages > 0)
+  L.freed_flag = ws_take(&off, num_pages > 0 ? (size_t)L.max_fresh : 0);
+  L.page_cnt = ws_take(&off, (size_t)(num_pages > 0 ? num_pages : 0) * 4);
+  L.page_key = ws_take(&off, (size_t)(num_pages > 0 ? num_pages : 0) * 4);
+  L.total = off;
+  return L;
 }
 
-size_t kv_compact_workspace_size(int B, int max_pages, int page_size, int token_granular) {
-  (void)page_size;
+size_t kv_compact_workspace_size(int B, int max_pages, int num_pages, int token_granular) {
   (void)token_granular;
-  size_t a, b, c, d, e, t;
-  long long mf;
-  compact_layout(B, max_pages, &a, &b, &c, &d, &e, &mf, &t);
-  return t;
+  return compact_layout(B, max_pages, num_pages).total;
 }
 
 int kv_compact(int32_t* block_table, int max_pages, int32_t* seq_lens, const uint8_t* keep_mask,
                int token_granular, void* k_pool, void* v_pool, int num_pages, int32_t* free_list,
-               int32_t* free_top, int B, int Hkv, int d, int page_size, int dtype, void* ws,
-               size_t ws_bytes, void* stream) {
+               int32_t* free_top, int32_t* refcnt, int B, int Hkv, int d, int page_size,
+               int dtype, void* ws, size_t ws_bytes, void* stream) {
   if (B < 0 || max_pages < 0 || Hkv <= 0 || page_size <= 0 || (d % 8) || d <= 0 || !dtype_ok(dtype))
     return KV_EINVAL;
   if (B == 0) return KV_OK;
@@ -886,10 +997,9 @@ int kv_compact(int32_t* block_table, int max_pages, int32_t* seq_lens, const uin
     return KV_EINVAL;
   const size_t smem = (size_t)3 * max_pages * 4;
   if (smem > (size_t)kCompactMaxSmem) return KV_EINVAL;
-  size_t o_len, o_pop, o_push, o_ctl, o_fresh, total;
-  long long max_fresh;
-  compact_layout(B, max_pages, &o_len, &o_pop, &o_push, &o_ctl, &o_fresh, &max_fresh, &total);
-  if (ws_bytes < total) return KV_EWORKSPACE;
+  if (refcnt && num_pages < 1) return KV_EINVAL;
+  const CompactLayout CL = compact_layout(B, max_pages, refcnt ? num_pages : 0);
+  if (ws_bytes < CL.total) return KV_EWORKSPACE;
   uint8_t* w = static_cast<uint8_t*>(ws);
   CompactArgs a{};
   a.table = block_table;
@@ -906,13 +1016,17 @@ int kv_compact(int32_t* block_table, int max_pages, int32_t* seq_lens, const uin
   a.Hkv = Hkv;
   a.d = d;
   a.ps = page_size;
-  a.new_len = reinterpret_cast<int32_t*>(w + o_len);
-  a.pop_base = reinterpret_cast<int32_t*>(w + o_pop);
-  a.push_base = reinterpret_cast<int32_t*>(w + o_push);
-  a.ctl = reinterpret_cast<int32_t*>(w + o_ctl);
-  a.fresh_ids = reinterpret_cast<int32_t*>(w + o_fresh);
-  a.max_fresh = max_fresh;
+  a.new_len = reinterpret_cast<int32_t*>(w + CL.new_len);
+  a.pop_base = reinterpret_cast<int32_t*>(w + CL.pop);
+  a.push_base = reinterpret_cast<int32_t*>(w + CL.push);
+  a.ctl = reinterpret_cast<int32_t*>(w + CL.ctl);
+  a.fresh_ids = reinterpret_cast<int32_t*>(w + CL.fresh);
+  a.max_fresh = CL.max_fresh;
   a.status = reinterpret_cast<int*>(w);
+  a.refcnt = refcnt;
+  a.freed_flag = w + CL.freed_flag;
+  a.page_cnt = reinterpret_cast<int32_t*>(w + CL.page_cnt);
+  a.page_key = reinterpret_cast<int32_t*>(w + CL.page_key);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   KV_CUDA_CHECK(launch(compact_plan_kernel, dim3(1), dim3(1024), 0, s, false, a));
   if (smem > 48 * 1024)  // one fixed limit for every call (the attribute is per function)
@@ -924,15 +1038,18 @@ int kv_compact(int32_t* block_table, int max_pages, int32_t* seq_lens, const uin
 
 size_t kv_append_workspace_size(int B) {
   size_t off = kHeaderBytes;
-  ws_take(&off, (size_t)(B > 0 ? B : 1) * 8);
-  ws_take(&off, 16);
+  const size_t nb = (size_t)(B > 0 ? B : 1);
+  ws_take(&off, nb * 8);   // dest
+  ws_take(&off, 16);       // ctl
+  ws_take(&off, nb * 4);   // cand
+  ws_take(&off, nb * 4);   // cow_src
   return off;
 }
 
 int kv_append(const void* k_new, const void* v_new, void* k_pool, void* v_pool, int num_pages,
               int32_t* block_table, int max_pages, int32_t* seq_lens, int32_t* free_list,
-              int32_t* free_top, int B, int Hkv, int d, int page_size, int dtype, void* ws,
-              size_t ws_bytes, void* stream) {
+              int32_t* free_top, int32_t* refcnt, int B, int Hkv, int d, int page_size, int dtype,
+              void* ws, size_t ws_bytes, void* stream) {
   if (B < 0 || max_pages < 0 || Hkv <= 0 || page_size <= 0 || d <= 0 || (d % 8) || !dtype_ok(dtype))
     return KV_EINVAL;
   if (B == 0) return KV_OK;
@@ -946,6 +1063,8 @@ int kv_append(const void* k_new, const void* v_new, void* k_pool, void* v_pool, 
   size_t off = kHeaderBytes;
   const size_t o_dest = ws_take(&off, (size_t)B * 8);
   const size_t o_ctl = ws_take(&off, 16);
+  const size_t o_cand = ws_take(&off, (size_t)B * 4);
+  const size_t o_cow = ws_take(&off, (size_t)B * 4);
   AppendArgs a{};
   a.k_new = static_cast<const uint8_t*>(k_new);
   a.v_new = static_cast<const uint8_t*>(v_new);
@@ -964,8 +1083,12 @@ int kv_append(const void* k_new, const void* v_new, void* k_pool, void* v_pool, 
   a.dest = reinterpret_cast<int2*>(w + o_dest);
   a.ctl = reinterpret_cast<int32_t*>(w + o_ctl);
   a.status = reinterpret_cast<int*>(w);
+  a.refcnt = refcnt;
+  a.cand = reinterpret_cast<int32_t*>(w + o_cand);
+  a.cow_src = reinterpret_cast<int32_t*>(w + o_cow);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   KV_CUDA_CHECK(launch(append_plan_kernel, dim3(1), dim3(1024), 0, s, false, a));
+  if (refcnt) KV_CUDA_CHECK(launch(append_cow_kernel, dim3(B), dim3(128), 0, s, false, a));
   KV_CUDA_CHECK(launch(append_copy_kernel, dim3(B), dim3(128), 0, s, false, a));
   return KV_OK;
 }

@@ -83,9 +83,9 @@ _SIGS = {
     "kv_select_workspace_size": ([I, I], SZ),
     "kv_select_pages": ([P, P, P, P, I, I, I, I, I, F, F, I, P, P, P, P, P, SZ, P], I),
     "kv_compact_workspace_size": ([I, I, I, I], SZ),
-    "kv_compact": ([P, I, P, P, I, P, P, I, P, P, I, I, I, I, I, P, SZ, P], I),
+    "kv_compact": ([P, I, P, P, I, P, P, I, P, P, P, I, I, I, I, I, P, SZ, P], I),
     "kv_append_workspace_size": ([I], SZ),
-    "kv_append": ([P, P, P, P, I, P, I, P, P, P, I, I, I, I, I, P, SZ, P], I),
+    "kv_append": ([P, P, P, P, I, P, I, P, P, P, P, I, I, I, I, I, P, SZ, P], I),
 }
 
 
@@ -318,18 +318,19 @@ def kv_select_pages(scores, seq_lens, active, budget, n_first, n_last, delta, ws
     _check(rc, "kv_select_pages")
 
 
-def kv_compact_workspace_size(B, max_pages, page_size=16, token_granular=False) -> int:
-    return lib().kv_compact_workspace_size(B, max_pages, page_size, int(bool(token_granular)))
+def kv_compact_workspace_size(B, max_pages, num_pages=0, token_granular=False) -> int:
+    """num_pages: the pool's pages if the compaction will get refcnt, else 0."""
+    return lib().kv_compact_workspace_size(B, max_pages, num_pages, int(bool(token_granular)))
 
 
 def kv_compact(block_table, seq_lens, keep_mask, token_granular, k_pool, v_pool, free_list,
-               free_top, ws, stream=None):
+               free_top, ws, stream=None, refcnt=None):
     B, maxp = block_table.shape
     P_, Hkv, ps, d = k_pool.shape
     rc = lib().kv_compact(_p(block_table), maxp, _p(seq_lens), _p(keep_mask),
                           int(bool(token_granular)), _p(k_pool), _p(v_pool), P_, _p(free_list),
-                          _p(free_top), B, Hkv, d, ps, dtype_code(k_pool), _p(ws), ws.numel(),
-                          _s(stream))
+                          _p(free_top), _p(refcnt), B, Hkv, d, ps, dtype_code(k_pool), _p(ws),
+                          ws.numel(), _s(stream))
     _check(rc, "kv_compact")
 
 
@@ -338,10 +339,12 @@ def kv_append_workspace_size(B) -> int:
 
 
 def kv_append(k_new, v_new, k_pool, v_pool, block_table, seq_lens, free_list, free_top, ws,
-              stream=None):
+              stream=None, refcnt=None):
     B, Hkv, d = k_new.shape
     P_, _, ps, _ = k_pool.shape
     rc = lib().kv_append(_p(k_new), _p(v_new), _p(k_pool), _p(v_pool), P_, _p(block_table),
-                         block_table.shape[1], _p(seq_lens), _p(free_list), _p(free_top), B, Hkv,
-                         d, ps, dtype_code(k_pool), _p(ws), ws.numel(), _s(stream))
+                         block_table.shape[1], _p(seq_lens), _p(free_list), _p(free_top),
+                         _p(refcnt), B, Hkv, d, ps, dtype_code(k_pool), _p(ws), ws.numel(),
+                         _s(stream))
     _check(rc, "kv_append")
+

@@ -252,3 +252,58 @@ def small_decode(seed: int, B: int, Hq: int, Hkv: int, d: int, seq_lens: List[in
     max_pages = max(1, max(nps) + pad_pages)
     return make_decode(f"small_s{seed}", seed, B, Hq, Hkv, d, page_size, dtype, seq_lens,
                        pool_factor=pool_factor, max_pages=max_pages, rng=rng)
+
+
+def shared_prefix(seed: int, B: int, group: int, prefix_tokens: int, tail_lens: List[int],
+                  Hq: int = 8, Hkv: int = 2, d: int = 64, dtype: int = F16,
+                  pool_factor: float = 2.0, pad_pages: int = 2) -> Dict:
+    """Sequences in groups of `group` share a cached prompt prefix of
+    `prefix_tokens` tokens (the prefix caching GrowPage keeps, mlsanity.com
+    GrowPage page, Abstract).  The prefix's full pages are one set of pool
+    pages referenced by every member's block table.  A member with
+    tail_lens[b] == 0 has not diverged yet (a fork): it also shares the
+    prefix's partly filled last page, if any, and L_b = prefix_tokens.  A
+    member with a tail owns every page after the full prefix pages (the rest
+    of the prefix and its tail_lens[b] own tokens).  Returns the decode
+    inputs and refcnt [P] int32, the number of block-table references to
+    each pool page (0 = free)."""
+    rng = np.random.default_rng(seed)
+    ps = 16
+    nfull = prefix_tokens // ps
+    partial = prefix_tokens % ps != 0
+    lens = np.array([prefix_tokens + int(t) for t in tail_lens], dtype=np.int32)
+    own = [0 if int(t) == 0 else ceil_div(int(lens[b]), ps) - nfull for b, t in enumerate(tail_lens)]
+    ngroups = ceil_div(B, group)
+    total = ngroups * (nfull + int(partial)) + sum(own)
+    P = max(1, int(math.ceil(pool_factor * total)))
+    perm = rng.permutation(P).astype(np.int32)
+    pos = 0
+    shared = []
+    for _ in range(ngroups):
+        shared.append(perm[pos: pos + nfull + int(partial)].copy())
+        pos += nfull + int(partial)
+    max_pages = max(ceil_div(int(L), ps) for L in lens) + pad_pages
+    table = np.full((B, max_pages), -1, dtype=np.int32)
+    for b in range(B):
+        g = shared[b // group]
+        if tail_lens[b] == 0:
+            table[b, : len(g)] = g
+        else:
+            table[b, :nfull] = g[:nfull]
+            table[b, nfull: nfull + own[b]] = perm[pos: pos + own[b]]
+            pos += own[b]
+    refcnt = np.zeros(P, dtype=np.int32)
+    for b in range(B):
+        for j in range(ceil_div(int(lens[b]), ps)):
+            refcnt[table[b, j]] += 1
+    # the free list: every page no table references (in permutation order)
+    free = perm[refcnt[perm] == 0].copy()
+    free_list = np.full(P, -1, dtype=np.int32)
+    free_list[: len(free)] = free
+    q = normal_bits(rng, (B, Hq, d), dtype)
+    k_pool = normal_bits(rng, (P, Hkv, ps, d), dtype)
+    v_pool = normal_bits(rng, (P, Hkv, ps, d), dtype)
+    dec = DecodeInputs(name=f"shared_prefix_s{seed}", B=B, Hq=Hq, Hkv=Hkv, d=d, page_size=ps,
+                       dtype=dtype, scale=1.0 / math.sqrt(d), q=q, k_pool=k_pool, v_pool=v_pool,
+                       block_table=table, seq_lens=lens, free_list=free_list, free_top=len(free))
+    return dict(decode=dec, refcnt=refcnt)

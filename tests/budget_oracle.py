@@ -9,7 +9,7 @@ from paged_kv_cache_492_b300 import workloads as W
 
 
 class OracleBudget:
-    def __init__(self, x: W.DecodeInputs, budget, cfg):
+    def __init__(self, x: W.DecodeInputs, budget, cfg, refcnt=None):
         self.x = x
         self.cfg = cfg
         self.k = np.ascontiguousarray(x.k_pool).copy()
@@ -19,6 +19,7 @@ class OracleBudget:
         self.free_list = np.ascontiguousarray(x.free_list, dtype=np.int32).copy()
         self.top = np.array([x.free_top], dtype=np.int32)
         self.budget = np.asarray(budget, dtype=np.int32).copy()
+        self.refcnt = None if refcnt is None else np.asarray(refcnt, dtype=np.int32).copy()
         B, maxp = self.table.shape
         P = self.k.shape[0]
         self.ema = np.zeros((B, 2, x.Hkv, x.d), np.float32)
@@ -38,7 +39,8 @@ class OracleBudget:
         self.keep, self.grow, self.drift = keep, grow, drift
         self.budget = bud
         rc = O.compact_inplace(self.table, self.lens, np.ascontiguousarray(keep), False, self.k,
-                               self.v, self.free_list, self.top, self.x.Hkv, self.x.d, 16)
+                               self.v, self.free_list, self.top, self.x.Hkv, self.x.d, 16,
+                               refcnt=self.refcnt)
         assert rc == 0, rc
 
     def fit(self, q0):
@@ -65,7 +67,7 @@ class OracleBudget:
                           self.scores)
         self._select(O.SELECT_BOUNDARY)
         rc = O.append_inplace(k_new, v_new, self.k, self.v, self.table, self.lens,
-                              self.free_list, self.top, x.Hkv, x.d, 16)
+                              self.free_list, self.top, x.Hkv, x.d, 16, refcnt=self.refcnt)
         assert rc == 0, rc
 
     def decode_inputs(self, q):

@@ -705,6 +705,132 @@ def pin_compaction():
     assert res[-1] == O.ENOSPACE and np.array_equal(res[0], x.block_table)
 
 
+def _compact_naive_shared(x, keep, token_gran, refcnt, top):
+    """Refcounted re-pack written from the definition with Python lists:
+    plan as for private pages; fresh pages get one reference; every old page
+    not reused loses one reference in (b, j) order and goes back on the free
+    list when none is left."""
+    ps = x.page_size
+    table = x.block_table.copy()
+    lens = x.seq_lens.copy()
+    kp, vp = x.k_pool.copy(), x.v_pool.copy()
+    rc = refcnt.copy()
+    free = list(x.free_list[:top])
+    out_rows, freed = [], []
+    for b in range(x.B):
+        L = int(lens[b])
+        toks = [t for t in range(L) if keep[b, t if token_gran else t // ps]]
+        old = table[b].copy()
+        row = [-1] * table.shape[1]
+        used = set()
+        for m in range(0, len(toks), ps):
+            grp = toks[m: m + ps]
+            j = grp[0] // ps
+            if grp == list(range(j * ps, j * ps + len(grp))):
+                row[m // ps] = int(old[j])
+                used.add(j)
+            else:
+                page = free.pop()
+                rc[page] = 1
+                row[m // ps] = page
+                for s_, t in enumerate(grp):
+                    kp[page, :, s_] = kp[old[t // ps], :, t % ps]
+                    vp[page, :, s_] = vp[old[t // ps], :, t % ps]
+        freed += [int(old[j]) for j in range(-(-L // ps)) if j not in used]
+        out_rows.append(row)
+        lens[b] = len(toks)
+    for pg in freed:
+        rc[pg] -= 1
+        if rc[pg] == 0:
+            free.append(pg)
+    table[:] = np.array(out_rows, np.int32)
+    return table, lens, kp, vp, free, rc
+
+
+def _refs(table, lens, P, ps=16):
+    n = np.zeros(P, np.int64)
+    for b in range(table.shape[0]):
+        for j in range(-(-int(lens[b]) // ps)):
+            n[table[b, j]] += 1
+    return n
+
+
+def pin_shared_pages():
+    """Shared (prefix) pages through compaction and append: the oracle against
+    a refcounted re-pack written independently, plus the invariants -- a
+    page's count equals its block-table references, the free list is exactly
+    the unreferenced pages, a page still referenced is never written, and an
+    append into a shared partly filled page copies it first."""
+    rng = np.random.default_rng(21)
+    ps = 16
+    for trial in range(8):
+        tails = [int(v) for v in rng.integers(0, 60, size=6)]
+        tails[trial % 6] = 0
+        c = W.shared_prefix(40 + trial, 6, 3, int(rng.integers(17, 60)), tails,
+                            pool_factor=3.0)
+        x, refcnt = c["decode"], c["refcnt"]
+        token_gran = trial % 2 == 1
+        width = x.max_pages * (ps if token_gran else 1)
+        keep = (rng.random((x.B, width)) < 0.6).astype(np.uint8)
+        if trial == 4:
+            keep[:] = 0
+        rc = refcnt.copy()
+        t, sl, kp, vp, fl, top, st = O.compact(x.block_table, x.seq_lens, keep, token_gran,
+                                               x.k_pool, x.v_pool, x.free_list, x.free_top,
+                                               x.Hkv, x.d, ps, refcnt=rc)
+        assert st == 0
+        nt, nl, nkp, nvp, nfree, nrc = _compact_naive_shared(x, keep, token_gran, refcnt,
+                                                             x.free_top)
+        assert np.array_equal(t, nt) and np.array_equal(sl, nl) and np.array_equal(rc, nrc)
+        assert np.array_equal(kp, nkp) and np.array_equal(vp, nvp)
+        assert top == len(nfree) and fl[:top].tolist() == nfree
+        P = x.num_pages
+        assert np.array_equal(rc, _refs(t, sl, P))
+        assert sorted(fl[:top].tolist()) == sorted(np.nonzero(rc == 0)[0].tolist())
+        for pg in np.nonzero(rc > 0)[0]:
+            if refcnt[pg] > 0:  # referenced before and after: untouched
+                assert np.array_equal(kp[pg], x.k_pool[pg]) and np.array_equal(vp[pg], x.v_pool[pg])
+    # append: forks (no own tokens) share the prefix's partly filled page
+    c = W.shared_prefix(60, 6, 3, 37, [0, 0, 9, 0, 40, 0], pool_factor=3.0)
+    x, refcnt = c["decode"], c["refcnt"]
+    kn = W.normal_bits(rng, (x.B, x.Hkv, x.d), W.F16)
+    vn = W.normal_bits(rng, (x.B, x.Hkv, x.d), W.F16)
+    rc = refcnt.copy()
+    kp, vp, t, sl, fl, top, st = O.append(kn, vn, x.k_pool, x.v_pool, x.block_table, x.seq_lens,
+                                          x.free_list, x.free_top, x.Hkv, x.d, ps, refcnt=rc)
+    assert st == 0 and sl.tolist() == (x.seq_lens + 1).tolist()
+    pops, cows, running = 0, 0, refcnt.astype(np.int64).copy()
+    for b in range(x.B):
+        L = int(x.seq_lens[b])
+        j = L // ps
+        old = int(x.block_table[b, j]) if L % ps else -1
+        if L % ps and running[old] > 1:  # copy-on-write, pops in ascending b
+            assert t[b, j] == x.free_list[x.free_top - 1 - pops] != old
+            pops += 1
+            cows += 1
+            running[old] -= 1
+            assert np.array_equal(kp[t[b, j], :, : L % ps], x.k_pool[old, :, : L % ps])
+            assert np.array_equal(vp[t[b, j], :, : L % ps], x.v_pool[old, :, : L % ps])
+        elif L % ps == 0:
+            pops += 1
+        else:  # sole owner (last sharer after the others copied): in place
+            assert t[b, j] == old
+        assert np.array_equal(kp[t[b, j], :, L % ps], kn[b])
+        assert np.array_equal(vp[t[b, j], :, L % ps], vn[b])
+    assert cows == 2 and top == x.free_top - pops  # two fork pairs: the first of each copies
+    assert np.array_equal(rc, _refs(t, sl, x.num_pages))
+    # every page referenced before the call and still referenced by a
+    # sequence that did not write into it is unchanged
+    for b in range(x.B):
+        for jj in range(-(-int(x.seq_lens[b]) // ps) - 1):
+            pg = t[b, jj]
+            assert np.array_equal(kp[pg], x.k_pool[pg]) and np.array_equal(vp[pg], x.v_pool[pg])
+    # without counts nothing is shared: the page is written in place
+    kp2, _, t2, *_ = O.append(kn, vn, x.k_pool, x.v_pool, x.block_table, x.seq_lens, x.free_list,
+                              x.free_top, x.Hkv, x.d, ps)
+    assert t2[0, 2] == x.block_table[0, 2]
+
+
 def pin_append():
     ps, Hkv, d = 16, 2, 8
     x = W.small_decode(31, B=4, Hq=4, Hkv=Hkv, d=d, seq_lens=[16, 5, 32, 0], pool_factor=2.0,

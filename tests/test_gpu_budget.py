@@ -170,7 +170,7 @@ def test_compact_bit_exact(seed, token_granular):
     dd = DeviceDecode(x)
     fl = i32(x.free_list)
     ft = i32([top])
-    ws = kv.alloc_workspace(kv.kv_compact_workspace_size(x.B, x.max_pages, 16, token_granular))
+    ws = kv.alloc_workspace(kv.kv_compact_workspace_size(x.B, x.max_pages, 0, token_granular))
     kv.kv_compact(dd.table, dd.lens, u8(keep), token_granular, dd.k, dd.v, fl, ft, ws)
     assert kv.kv_get_status(ws) == 0
     t, sl, kp, vp, fl_ref, top_ref, _ = ref
@@ -188,7 +188,7 @@ def test_compact_no_space_changes_nothing():
     t0 = dd.table.clone()
     fl = i32(x.free_list)
     ft = i32([0])
-    ws = kv.alloc_workspace(kv.kv_compact_workspace_size(x.B, x.max_pages, 16, True))
+    ws = kv.alloc_workspace(kv.kv_compact_workspace_size(x.B, x.max_pages, 0, True))
     ref = O.compact(x.block_table, x.seq_lens, keep, True, x.k_pool, x.v_pool, x.free_list, 0,
                     x.Hkv, x.d, 16)
     kv.kv_compact(dd.table, dd.lens, u8(keep), True, dd.k, dd.v, fl, ft, ws)
@@ -325,3 +325,109 @@ def test_budgeted_serving_trajectory():
                                 dec.lse.cpu().numpy().astype(np.float64), ref_out, ref_lse)
     print(f"budgeted serving: {steps} steps, {grows} grows, {compacts} compactions")
     assert grows > 0 and compacts > 0
+
+
+# ---------------------------------------------------------------- shared pages
+def _shared_case(seed, tails, prefix=37):
+    c = W.shared_prefix(seed, len(tails), 3, prefix, tails, pool_factor=3.0)
+    return c["decode"], c["refcnt"]
+
+
+@pytest.mark.parametrize("seed,token_granular", [(51, False), (52, True), (53, False), (54, True)])
+def test_compact_shared_bit_exact(seed, token_granular):
+    """Refcounted compaction: counts, free list (a page returns when its last
+    reference goes), tables and pools bit for bit against the oracle."""
+    rng = np.random.default_rng(seed)
+    tails = [int(v) for v in rng.integers(0, 80, size=9)]
+    tails[seed % 9] = 0
+    x, refcnt = _shared_case(seed, tails, prefix=int(rng.integers(17, 70)))
+    width = x.max_pages * (16 if token_granular else 1)
+    keep = (rng.random((x.B, width)) < 0.5).astype(np.uint8)
+    rc_ref = refcnt.copy()
+    t, sl, kp, vp, fl, top, st = O.compact(x.block_table, x.seq_lens, keep, token_granular,
+                                           x.k_pool, x.v_pool, x.free_list, x.free_top, x.Hkv,
+                                           x.d, 16, refcnt=rc_ref)
+    assert st == 0
+    dd = DeviceDecode(x)
+    fl_d, ft_d, rc_d = i32(x.free_list), i32([x.free_top]), i32(refcnt)
+    ws = kv.alloc_workspace(kv.kv_compact_workspace_size(x.B, x.max_pages, x.num_pages,
+                                                         token_granular))
+    kv.kv_compact(dd.table, dd.lens, u8(keep), token_granular, dd.k, dd.v, fl_d, ft_d, ws,
+                  refcnt=rc_d)
+    assert kv.kv_get_status(ws) == 0
+    assert np.array_equal(dd.table.cpu().numpy(), t)
+    assert np.array_equal(dd.lens.cpu().numpy(), sl)
+    assert np.array_equal(rc_d.cpu().numpy(), rc_ref)
+    assert int(ft_d.item()) == top
+    assert np.array_equal(fl_d.cpu().numpy()[:top], fl[:top])
+    assert np.array_equal(dd.k.view(torch.int16).cpu().numpy().view(np.uint16), kp)
+    assert np.array_equal(dd.v.view(torch.int16).cpu().numpy().view(np.uint16), vp)
+
+
+def test_append_shared_bit_exact():
+    """Copy-on-write append of forks sharing a partly filled prefix page."""
+    rng = np.random.default_rng(61)
+    x, refcnt = _shared_case(61, [0, 0, 9, 0, 40, 0, 0, 0, 0], prefix=37)
+    kn = W.normal_bits(rng, (x.B, x.Hkv, x.d), W.F16)
+    vn = W.normal_bits(rng, (x.B, x.Hkv, x.d), W.F16)
+    rc_ref = refcnt.copy()
+    kp, vp, t, sl, fl, top, st = O.append(kn, vn, x.k_pool, x.v_pool, x.block_table, x.seq_lens,
+                                          x.free_list, x.free_top, x.Hkv, x.d, 16, refcnt=rc_ref)
+    assert st == 0
+    dd = DeviceDecode(x)
+    fl_d, ft_d, rc_d = i32(x.free_list), i32([x.free_top]), i32(refcnt)
+    ws = kv.alloc_workspace(kv.kv_append_workspace_size(x.B))
+    kv.kv_append(bits_to_dev(kn, W.F16), bits_to_dev(vn, W.F16), dd.k, dd.v, dd.table, dd.lens,
+                 fl_d, ft_d, ws, refcnt=rc_d)
+    assert kv.kv_get_status(ws) == 0
+    assert np.array_equal(dd.table.cpu().numpy(), t) and np.array_equal(dd.lens.cpu().numpy(), sl)
+    assert np.array_equal(rc_d.cpu().numpy(), rc_ref) and int(ft_d.item()) == top
+    assert np.array_equal(dd.k.view(torch.int16).cpu().numpy().view(np.uint16), kp)
+    assert np.array_equal(dd.v.view(torch.int16).cpu().numpy().view(np.uint16), vp)
+    assert (refcnt > 1).sum() > 0 and not np.array_equal(t, x.block_table)  # forks copied
+
+
+def test_budgeted_shared_prefix_trajectory():
+    """Budgeted decode over sequences that share prompt prefixes: 48 steps of
+    compress-or-grow, copy-on-write appends and decode, every table, count,
+    free list and EMA bit-exact against the oracle; decode within tolerance."""
+    rng = np.random.default_rng(71)
+    B, steps = 12, 48
+    tails = [int(v) for v in rng.integers(200, 1200, size=B)]
+    tails[0] = tails[4] = 0           # forks sharing the partial prefix page
+    c = W.shared_prefix(71, B, 4, 700, tails, Hq=32, Hkv=8, d=128, dtype=W.BF16, pool_factor=1.6)
+    x, refcnt = c["decode"], c["refcnt"]
+    budget = rng.integers(20, 60, size=B).astype(np.int32)
+    cfg = BG.BudgetConfig(a_fast=0.9, a_slow=0.999, n_first=2, n_last=2, delta=0.5)
+    orc = OracleBudget(x, budget, cfg, refcnt=refcnt)
+    orc.summarize_all()
+    dd = DeviceDecode(x)
+    dec = BG.BudgetedDecoder(dd.k, dd.v, dd.table, dd.lens, i32(x.free_list), i32([x.free_top]),
+                             i32(budget), x.Hq, cfg, refcnt=i32(refcnt))
+    dec.summarize_pages(i32(np.arange(x.num_pages)))
+    q0, _, _ = W.step_tokens(71, 0, x.B, x.Hq, x.Hkv, x.d, x.dtype)
+    dec.fit(bits_to_dev(q0, x.dtype))
+    orc.fit(q0)
+
+    def check(where):
+        assert kv.kv_get_status(dec.ws) == 0, where
+        assert kv.kv_get_status(dec.decode_ws) == 0, where
+        assert np.array_equal(dec.table.cpu().numpy(), orc.table), where
+        assert np.array_equal(dec.lens.cpu().numpy(), orc.lens), where
+        assert np.array_equal(dec.refcnt.cpu().numpy(), orc.refcnt), where
+        top = int(dec.free_top.item())
+        assert top == int(orc.top[0]), where
+        assert np.array_equal(dec.free_list.cpu().numpy()[:top], orc.free_list[:top]), where
+
+    check("fit")
+    for t in range(steps):
+        q, kn, vn = W.step_tokens(71, t, x.B, x.Hq, x.Hkv, x.d, x.dtype)
+        dec.step(bits_to_dev(q, x.dtype), bits_to_dev(kn, x.dtype), bits_to_dev(vn, x.dtype), t)
+        orc.step(q, kn, vn, t)
+        check(f"step {t}")
+        if t % 12 == 11:
+            y = orc.decode_inputs(q)
+            ref_out, ref_lse = O.decode(y, nthreads=NCPU)
+            assert_decode_close(y, dec.out.cpu().numpy().astype(np.float64),
+                                dec.lse.cpu().numpy().astype(np.float64), ref_out, ref_lse)
+    assert (orc.refcnt > 1).any()  # some pages are still shared at the end

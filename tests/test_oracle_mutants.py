@@ -39,7 +39,10 @@ MUTANTS = [
     ("compact_reuse_apply", "int reuse = (t0 % ps) == 0;", "int reuse = 0;", 1),
     ("compact_reuse_slots", "reuse = kept[b][m * ps + s] == t0 + s;", "reuse = kept[b][m * ps + s] >= t0 + s;", 1),
     ("compact_push_order", "free_list[top++] = freed[i];", "free_list[top++] = freed[nfreed - 1 - i];", 0),
-    ("append_pop", "if (L % ps == 0) *slot = free_list[--top];", "if (L % ps == 0) *slot = free_list[top-- - 2];", 0),
+    ("append_pop", "      *slot = free_list[--top];", "      *slot = free_list[top-- - 2];", 0),
+    ("cow_copy_len", "sizeof(uint16_t) * (size_t)(L % ps) * d);", "sizeof(uint16_t) * (size_t)(L % ps - 1) * d);", 0),
+    ("cow_old_ref", "refcnt[old] -= 1;", "refcnt[old] -= 0;", 0),
+    ("shared_free", "if (refcnt[freed[i]] != 0) continue;", "if (refcnt[freed[i]] < 0) continue;", 0),
     ("mark_boundary", "L / ps >= budget[b]", "L / ps > budget[b]", 0),
 ]
 
