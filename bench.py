@@ -41,6 +41,7 @@ from paged_kv_cache_492_b300 import workloads as W  # noqa: E402
 
 WORKLOADS = {
     "bimodal": W.bimodal,
+    "bimodal_b4": W.bimodal_b4,
     "uniform": W.uniform_lengths,
     "zipf": W.zipf_lengths,
     "bucket32k": lambda: W.bucketed_long(32768),
@@ -302,6 +303,14 @@ def run_ours(args, x, name, rank, world):
                              "LSE merge fused); a page-offset pass is added above 1024 sequences",
         "clocks": clocks,
     }
+    # the calibrated split-size choice for this workload (own variants only)
+    cands = [0, 8, 16, 32, 64, 128]
+    ws_t = kv.alloc_workspace(max(
+        kv.kv_decode_workspace_size(x.B, x.Hq, x.Hkv, x.d, x.max_pages, 16, 8),
+        kv.kv_decode_workspace_size(x.B, x.Hq, x.Hkv, x.d, x.max_pages, 16, 0)), device=dev)
+    best, us = kv.kv_decode_tune(q, k, v, table, lens, x.scale, out, lse, ws_t, cands, reps=5)
+    line["policy"] = {"candidates_pages_per_split": cands, "median_us": us, "best": best,
+                      "note": "0 = automatic split rule; L2 not flushed between these calls"}
     if not args.no_budget:
         line["budget_step"] = measure_budget(dev, peak, peak_kind, args.budget_steps,
                                              args.budget_warmup)

@@ -137,6 +137,22 @@ int kv_decode(const void *q, const void *k_pool, const void *v_pool, int num_pag
               int pages_per_split, float *out, float *lse, void *ws, size_t ws_bytes,
               void *stream);
 
+/* Calibration among this library's own decode variants (the adaptive policy
+ * of [PKV] Summary picks an engine per workload by measurement; here the
+ * variants are split sizes): runs kv_decode on the given inputs once per
+ * candidate pages_per_split (0 = automatic) untimed, then `reps` (<= 64)
+ * times timed with CUDA events on `stream`, writes the median microseconds
+ * per candidate to us[n_candidates] (host) and the fastest candidate to
+ * *best (host).  Synchronises `stream`; out/lse hold the last call's result.
+ * `ws` must be sized for every candidate (kv_decode_workspace_size with the
+ * smallest positive candidate covers all of them and the automatic one is
+ * covered by its own size: pass the larger). */
+int kv_decode_tune(const void *q, const void *k_pool, const void *v_pool, int num_pages,
+                   const int32_t *block_table, int max_pages, const int32_t *seq_lens, int B,
+                   int page_size, int Hq, int Hkv, int d, int dtype, float scale,
+                   const int32_t *candidates, int n_candidates, int reps, float *out, float *lse,
+                   float *us, int32_t *best, void *ws, size_t ws_bytes, void *stream);
+
 /* Profiling aid: the next kv_decode (or kv_decode_hostio) issued from the
  * calling host thread records `event_before` (a cudaEvent_t) on its stream
  * just before the attention kernel and `event_after` just after it, so the
@@ -312,6 +328,37 @@ int kv_append(const void *k_new, const void *v_new, void *k_pool, void *v_pool, 
               int32_t *block_table, int max_pages, int32_t *seq_lens, int32_t *free_list,
               int32_t *free_top, int32_t *refcnt, int B, int Hkv, int d, int page_size, int dtype,
               void *ws, size_t ws_bytes, void *stream);
+
+/* ------------------------------------------------------------------------ */
+/* Elastic page pool [EKV, section 3]: one reserved virtual address range     */
+/* per pool whose physical backing grows and shrinks at its top, so pages     */
+/* never move, block tables stay valid and the kernels are unchanged.  This   */
+/* is the one part of the library that allocates device memory, on request.   */
+/* ------------------------------------------------------------------------ */
+
+/* Reserve max_bytes (rounded up to the allocation granularity) of virtual
+ * address space on `device`; nothing is backed yet.  *pool: opaque handle;
+ * *base: the range's device address (page p of a pool of page_bytes pages
+ * lives at base + p * page_bytes); *granularity (may be NULL): the size unit
+ * of every resize.  Errors: KV_EINVAL, KV_ECUDA (kv_last_error names the
+ * driver call). */
+int kv_vmm_pool_create(int device, size_t max_bytes, void **pool, void **base,
+                       size_t *granularity);
+
+/* Back the first `bytes` (rounded up to the granularity) of the range.
+ * Growing maps one new physical allocation directly above the mapped part;
+ * shrinking unmaps and frees whole earlier growths from the top, so the
+ * result may stay above `bytes` (*mapped, may be NULL, reports it).  The
+ * contents of pages that stay mapped are untouched.  Synchronous with respect
+ * to the device (the driver calls are); the caller must not shrink under
+ * pages that are still referenced or in use by running kernels. */
+int kv_vmm_pool_resize(void *pool, size_t bytes, size_t *mapped);
+
+/* Bytes currently backed (0 for a NULL pool). */
+size_t kv_vmm_pool_mapped(void *pool);
+
+/* Unmap and free everything and release the address range. */
+int kv_vmm_pool_destroy(void *pool);
 
 #ifdef __cplusplus
 }

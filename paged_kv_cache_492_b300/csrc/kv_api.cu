@@ -181,6 +181,51 @@ int kv_build_workqueue(const int32_t* seq_lens, int B, int Hkv, int page_size, i
   return KV_OK;
 }
 
+int kv_decode_tune(const void* q, const void* k_pool, const void* v_pool, int num_pages,
+                   const int32_t* block_table, int max_pages, const int32_t* seq_lens, int B,
+                   int page_size, int Hq, int Hkv, int d, int dtype, float scale,
+                   const int32_t* candidates, int n_candidates, int reps, float* out, float* lse,
+                   float* us, int32_t* best, void* ws, size_t ws_bytes, void* stream) {
+  if (!candidates || n_candidates < 1 || reps < 1 || !us || !best) return KV_EINVAL;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaEvent_t e0 = nullptr, e1 = nullptr;
+  KV_CUDA_CHECK(cudaEventCreate(&e0));
+  if (cudaEventCreate(&e1) != cudaSuccess) {
+    cudaEventDestroy(e0);
+    return cuda_failed(cudaErrorUnknown, "cudaEventCreate");
+  }
+  int rc = KV_OK;
+  int best_i = 0;
+  for (int c = 0; c < n_candidates && rc == KV_OK; ++c) {
+    float times[64];
+    const int n = reps < 64 ? reps : 64;
+    // one untimed call first (launch shape set-up, caches)
+    rc = decode_launch(q, k_pool, v_pool, num_pages, block_table, max_pages, seq_lens, B,
+                       page_size, Hq, Hkv, d, dtype, scale, candidates[c], out, lse, ws, ws_bytes,
+                       s);
+    for (int r = 0; r < n && rc == KV_OK; ++r) {
+      if (cudaEventRecord(e0, s) != cudaSuccess) { rc = cuda_failed(cudaErrorUnknown, "cudaEventRecord"); break; }
+      rc = decode_launch(q, k_pool, v_pool, num_pages, block_table, max_pages, seq_lens, B,
+                         page_size, Hq, Hkv, d, dtype, scale, candidates[c], out, lse, ws,
+                         ws_bytes, s);
+      if (rc) break;
+      if (cudaEventRecord(e1, s) != cudaSuccess || cudaEventSynchronize(e1) != cudaSuccess ||
+          cudaEventElapsedTime(&times[r], e0, e1) != cudaSuccess) {
+        rc = cuda_failed(cudaErrorUnknown, "timing events");
+        break;
+      }
+    }
+    if (rc) break;
+    std::sort(times, times + n);
+    us[c] = times[n / 2] * 1e3f;
+    if (us[c] < us[best_i]) best_i = c;
+  }
+  cudaEventDestroy(e0);
+  cudaEventDestroy(e1);
+  if (rc == KV_OK) *best = candidates[best_i];
+  return rc;
+}
+
 int kv_profile_next_decode(void* event_before, void* event_after) {
   set_profile_events(static_cast<cudaEvent_t>(event_before), static_cast<cudaEvent_t>(event_after));
   return KV_OK;

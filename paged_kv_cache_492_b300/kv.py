@@ -74,6 +74,8 @@ _SIGS = {
     "kv_decode_hostio": ([P, P, P, I, P, I, P, I, I, I, I, I, I, F, I, P, P, P, SZ, P], I),
     "kv_workqueue_workspace_size": ([I], SZ),
     "kv_profile_next_decode": ([P, P], I),
+    "kv_decode_tune": ([P, P, P, I, P, I, P, I, I, I, I, I, I, F, P, I, I, P, P, P, P, P, SZ, P],
+                       I),
     "kv_build_workqueue": ([P, I, I, I, I, I, I, P, I, P, I, P, P, P, P, P], I),
     "kv_update_query_summaries": ([P, I, I, I, I, I, F, F, I, P, P], I),
     "kv_mark_active": ([P, P, I, I, I, P, P], I),
@@ -85,6 +87,11 @@ _SIGS = {
     "kv_compact_workspace_size": ([I, I, I, I], SZ),
     "kv_compact": ([P, I, P, P, I, P, P, I, P, P, P, I, I, I, I, I, P, SZ, P], I),
     "kv_append_workspace_size": ([I], SZ),
+    "kv_vmm_pool_create": ([I, SZ, C.POINTER(C.c_void_p), C.POINTER(C.c_void_p),
+                            C.POINTER(C.c_size_t)], I),
+    "kv_vmm_pool_resize": ([P, SZ, C.POINTER(C.c_size_t)], I),
+    "kv_vmm_pool_mapped": ([P], SZ),
+    "kv_vmm_pool_destroy": ([P], I),
     "kv_append": ([P, P, P, P, I, P, I, P, P, P, P, I, I, I, I, I, P, SZ, P], I),
 }
 
@@ -243,6 +250,56 @@ def kv_decode_hostio(h_q, k_pool, v_pool, h_block_table, h_seq_lens, scale, h_ou
     _check(rc, "kv_decode_hostio")
 
 
+def kv_decode_tune(q, k_pool, v_pool, block_table, seq_lens, scale, out, lse, ws, candidates,
+                   reps=5, stream=None):
+    """Time kv_decode for each candidate pages_per_split (0 = automatic) on
+    these inputs -> (best candidate, [median us per candidate])."""
+    B, Hq, d = q.shape
+    P_, Hkv, ps, _ = k_pool.shape
+    cand = (C.c_int32 * len(candidates))(*[int(c) for c in candidates])
+    us = (C.c_float * len(candidates))()
+    best = C.c_int32()
+    rc = lib().kv_decode_tune(_p(q), _p(k_pool), _p(v_pool), P_, _p(block_table),
+                              block_table.shape[1], _p(seq_lens), B, ps, Hq, Hkv, d,
+                              dtype_code(q), float(scale), cand, len(candidates), int(reps),
+                              _p(out), _p(lse), us, C.byref(best), _p(ws), ws.numel(), _s(stream))
+    _check(rc, "kv_decode_tune")
+    return int(best.value), [float(u) for u in us]
+
+
+class DecodePolicy:
+    """Per-workload choice of the split size, calibrated on first sight
+    (PersistentKV's adaptive policy, aissential.tech, Summary, restated among
+    this library's own variants).  A workload's signature is its batch size,
+    log2 of its page count and its long-to-mean length ratio (rounded); the
+    first batch with a new signature is timed with kv_decode_tune and the
+    fastest split size is reused for every later batch with that signature."""
+
+    def __init__(self, candidates=(0, 8, 16, 32, 64, 128), reps=5):
+        self.candidates = tuple(int(c) for c in candidates)
+        self.reps = reps
+        self.table = {}
+
+    @staticmethod
+    def signature(seq_lens_host, page_size=16):
+        import math
+
+        pages = [-(-int(L) // page_size) for L in seq_lens_host]
+        W = sum(pages)
+        mean = W / max(1, len(pages))
+        ratio = (max(pages) / mean) if W else 0.0
+        return (len(pages), int(math.log2(W)) if W else -1, round(ratio))
+
+    def pages_per_split(self, seq_lens_host, q, k_pool, v_pool, block_table, seq_lens, scale, out,
+                        lse, ws, stream=None):
+        sig = self.signature(seq_lens_host, k_pool.shape[2])
+        if sig not in self.table:
+            best, us = kv_decode_tune(q, k_pool, v_pool, block_table, seq_lens, scale, out, lse, ws,
+                                      self.candidates, self.reps, stream)
+            self.table[sig] = (best, dict(zip(self.candidates, us)))
+        return self.table[sig][0]
+
+
 def kv_profile_next_decode(event_before, event_after):
     """Arm CUDA events (torch.cuda.Event) around the next decode's attention kernel."""
     ev0 = event_before.cuda_event if event_before is not None else None
@@ -347,4 +404,50 @@ def kv_append(k_new, v_new, k_pool, v_pool, block_table, seq_lens, free_list, fr
                          _p(refcnt), B, Hkv, d, ps, dtype_code(k_pool), _p(ws), ws.numel(),
                          _s(stream))
     _check(rc, "kv_append")
+
+# ---------------------------------------------------------------- elastic pool
+class VmmPool:
+    """An elastic page pool: a reserved device address range whose backing
+    grows and shrinks at the top (kv_vmm_pool_*).  `tensor(shape, dtype)`
+    views the range's start as a torch tensor (the caller keeps the pool
+    alive and only touches the mapped part)."""
+
+    def __init__(self, max_bytes: int, device: int = 0):
+        h, base, gran = C.c_void_p(), C.c_void_p(), C.c_size_t()
+        _check(lib().kv_vmm_pool_create(int(device), int(max_bytes), C.byref(h), C.byref(base),
+                                        C.byref(gran)), "kv_vmm_pool_create")
+        self.handle, self.base, self.granularity = h.value, base.value, gran.value
+        self.device = device
+
+    def resize(self, nbytes: int) -> int:
+        m = C.c_size_t()
+        _check(lib().kv_vmm_pool_resize(self.handle, int(nbytes), C.byref(m)), "kv_vmm_pool_resize")
+        return m.value
+
+    @property
+    def mapped(self) -> int:
+        return lib().kv_vmm_pool_mapped(self.handle)
+
+    def tensor(self, shape, dtype) -> torch.Tensor:
+        """A tensor over the start of the range (no copy, no ownership); it
+        must lie inside the mapped part, and the pool must outlive it."""
+        import math
+
+        esize = torch.empty((), dtype=dtype).element_size()
+        n = math.prod(shape)
+        if n * esize > self.mapped:
+            raise ValueError("view larger than the mapped part of the pool")
+        code = {1: "|u1", 2: "<i2", 4: "<i4"}[esize]
+
+        class _View:
+            __cuda_array_interface__ = {"shape": (n,), "typestr": code,
+                                        "data": (self.base, False), "version": 3}
+
+        raw = torch.as_tensor(_View(), device=f"cuda:{self.device}")
+        return raw.view(dtype).view(*shape)
+
+    def close(self):
+        if self.handle:
+            _check(lib().kv_vmm_pool_destroy(self.handle), "kv_vmm_pool_destroy")
+            self.handle = None
 

@@ -186,6 +186,19 @@ def bimodal(seed: int = 1) -> DecodeInputs:
                        k_channel_scale=(0.5, 2.0), rng=rng)
 
 
+def bimodal_b4(seed: int = 5) -> DecodeInputs:
+    """Batch-4 bimodal fp16 decode (the B4 bimodal case of the PersistentKV
+    summary, aissential.tech, Summary): 2 lengths from U[512, 2048] and 2
+    from U[16384, 32768], shuffled; otherwise as the batch-8 bimodal case."""
+    rng = np.random.default_rng(seed)
+    short = rng.integers(512, 2048, size=2, endpoint=True)
+    long_ = rng.integers(16384, 32768, size=2, endpoint=True)
+    lens = np.concatenate([short, long_])
+    rng.shuffle(lens)
+    return make_decode("bimodal_b4_fp16", seed, 4, 32, 8, 128, 16, F16, lens,
+                       k_channel_scale=(0.5, 2.0), rng=rng)
+
+
 def uniform_lengths(seed: int = 2) -> DecodeInputs:
     """Batch-8 bf16 decode with lengths U[1024, 32768]."""
     rng = np.random.default_rng(seed)

@@ -214,6 +214,7 @@ def test_hostio_matches_device_call():
 CONFIGS = {
     "tiny": lambda: W.tiny()["decode"],
     "bimodal": W.bimodal,
+    "bimodal_b4": W.bimodal_b4,
     "uniform": W.uniform_lengths,
     "zipf": W.zipf_lengths,
     "bucket32k": lambda: W.bucketed_long(32768),
@@ -231,3 +232,29 @@ def test_decode_full_config(name):
     ref_out, ref_lse = O.decode(x, nthreads=NCPU)
     worst = assert_decode_close(x, out, lse, ref_out, ref_lse)
     print(f"{name}: worst |out-oracle|/max|V| = {worst:.2e}")
+
+
+def test_decode_tune_and_policy():
+    """The calibrated choice among split sizes: every candidate is timed, the
+    winner's output matches the oracle, and the policy reuses a signature's
+    choice without timing again."""
+    x = W.bimodal_b4()
+    dd = DeviceDecode(x)
+    cands = [0, 8, 32, 128]
+    ws = kv.alloc_workspace(max(kv.kv_decode_workspace_size(x.B, x.Hq, x.Hkv, x.d, x.max_pages, 16, 8),
+                                kv.kv_decode_workspace_size(x.B, x.Hq, x.Hkv, x.d, x.max_pages, 16, 0)))
+    best, us = kv.kv_decode_tune(dd.q, dd.k, dd.v, dd.table, dd.lens, x.scale, dd.out, dd.lse, ws,
+                                 cands, reps=3)
+    assert best in cands and len(us) == len(cands) and all(u > 0 for u in us)
+    assert us[cands.index(best)] == min(us)
+    out, lse, rc = dd.run(pages_per_split=best, ws=ws)
+    assert rc == 0
+    ref_out, ref_lse = O.decode(x, nthreads=NCPU)
+    assert_decode_close(x, out, lse, ref_out, ref_lse)
+    pol = kv.DecodePolicy(candidates=cands, reps=2)
+    p1 = pol.pages_per_split(x.seq_lens, dd.q, dd.k, dd.v, dd.table, dd.lens, x.scale, dd.out,
+                             dd.lse, ws)
+    p2 = pol.pages_per_split(x.seq_lens, dd.q, dd.k, dd.v, dd.table, dd.lens, x.scale, dd.out,
+                             dd.lse, ws)
+    assert p1 == p2 and len(pol.table) == 1 and p1 in cands
+    print(f"B4 bimodal split sizes {dict(zip(cands, [round(u, 1) for u in us]))} us; best {best}")
