@@ -137,6 +137,27 @@ int kv_decode(const void *q, const void *k_pool, const void *v_pool, int num_pag
               int pages_per_split, float *out, float *lse, void *ws, size_t ws_bytes,
               void *stream);
 
+/* Several new query tokens per sequence (a prefill chunk, or the drafted
+ * tokens of a speculative step) over the same pool and block table: the T
+ * queries of sequence b are its last T cached tokens (their K/V already
+ * appended), and query i attends causally to tokens [0, L_b - T + 1 + i):
+ *   s_t = scale * <q[b][i][hq], k_t>,  lse = ln sum_t exp(s_t),
+ *   out[b][i][hq] = sum_t exp(s_t - lse) v_t;
+ * a query with no token to attend to gets out = 0 and lse = -inf.
+ * q [B][T][Hq][d] 16-bit, out [B][T][Hq][d] fp32, lse [B][T][Hq] fp32
+ * (device).  Other arguments and errors as kv_decode; the workspace is
+ * kv_attend_multi_workspace_size bytes and, as for kv_decode, keeps merge
+ * tickets between calls (give it its own).  This form runs the decode
+ * kernel on B*T causal views of the batch, so each page is streamed once per
+ * query token. */
+size_t kv_attend_multi_workspace_size(int B, int T, int Hq, int Hkv, int d, int max_pages,
+                                      int page_size, int pages_per_split);
+int kv_attend_multi(const void *q, const void *k_pool, const void *v_pool, int num_pages,
+                    const int32_t *block_table, int max_pages, const int32_t *seq_lens, int B,
+                    int T, int page_size, int Hq, int Hkv, int d, int dtype, float scale,
+                    int pages_per_split, float *out, float *lse, void *ws, size_t ws_bytes,
+                    void *stream);
+
 /* Calibration among this library's own decode variants (the adaptive policy
  * of [PKV] Summary picks an engine per workload by measurement; here the
  * variants are split sizes): runs kv_decode on the given inputs once per

@@ -98,6 +98,7 @@ typedef struct {
   const int32_t *table, *seq_lens;
   int max_pages, num_pages, B, ps, Hq, Hkv, d, dtype;
   double scale;
+  size_t q_seq_stride; /* elements between two sequences' q (0 = Hq * d) */
 } DecodeArgs;
 
 /* Attention of query head hq of sequence b over its tokens [t0, t1).
@@ -116,7 +117,8 @@ static int decode_range(const DecodeArgs *a, int b, int hq, int64_t t0, int64_t 
     *lse = -INFINITY;
     return OR_OK;
   }
-  const uint16_t *qv = a->q + ((size_t)b * a->Hq + hq) * d;
+  const size_t qs = a->q_seq_stride ? a->q_seq_stride : (size_t)a->Hq * d;
+  const uint16_t *qv = a->q + (size_t)b * qs + (size_t)hq * d;
   double *qd = (double *)malloc(sizeof(double) * d);
   double *s = (double *)malloc(sizeof(double) * (size_t)(t1 - t0));
   for (int c = 0; c < d; ++c) qd[c] = cv(qv[c], a->dtype);
@@ -193,7 +195,7 @@ int or_decode(const uint16_t *q, const uint16_t *k_pool, const uint16_t *v_pool,
               int B, int page_size, int Hq, int Hkv, int d, int dtype, double scale,
               double *out, double *lse, int nthreads) {
   DecodeArgs a = {q, k_pool, v_pool, block_table, seq_lens, max_pages, num_pages,
-                  B, page_size, Hq, Hkv, d, dtype, scale};
+                  B, page_size, Hq, Hkv, d, dtype, scale, 0};
   int rc = check_decode_args(&a);
   if (rc) return rc;
   DecodePool pool;
@@ -220,7 +222,7 @@ int or_decode_rows(const uint16_t *q, const uint16_t *k_pool, const uint16_t *v_
                    int B, int page_size, int Hq, int Hkv, int d, int dtype, double scale,
                    const int32_t *rows, int nrows, double *out, double *lse) {
   DecodeArgs a = {q, k_pool, v_pool, block_table, seq_lens, max_pages, num_pages,
-                  B, page_size, Hq, Hkv, d, dtype, scale};
+                  B, page_size, Hq, Hkv, d, dtype, scale, 0};
   int rc = check_decode_args(&a);
   if (rc) return rc;
   for (int r = 0; r < nrows; ++r) {
@@ -239,9 +241,79 @@ int or_decode_range(const uint16_t *q, const uint16_t *k_pool, const uint16_t *v
                     int B, int page_size, int Hq, int Hkv, int d, int dtype, double scale,
                     int b, int hq, int64_t t0, int64_t t1, double *out, double *lse) {
   DecodeArgs a = {q, k_pool, v_pool, block_table, seq_lens, max_pages, num_pages,
-                  B, page_size, Hq, Hkv, d, dtype, scale};
+                  B, page_size, Hq, Hkv, d, dtype, scale, 0};
   if (t0 < 0 || t1 > seq_lens[b]) return OR_EINVAL;
   return decode_range(&a, b, hq, t0, t1, out, lse);
+}
+
+/* Several query tokens per sequence -- the step before decode (a prefill
+ * chunk, or drafted tokens being verified) over the same pool and table.
+ * The T queries of sequence b are its last T tokens; query i attends to the
+ * tokens [0, L_b - T + 1 + i) (causal), with the attention of decode_range.
+ * q, out: [B][T][Hq][d]; lse: [B][T][Hq].                                   */
+typedef struct {
+  const DecodeArgs *a;
+  const uint16_t *q;
+  int T;
+  double *out, *lse;
+  int next, n, rc;
+  pthread_mutex_t mu;
+} MultiPool;
+
+static void *multi_worker(void *p) {
+  MultiPool *pool = (MultiPool *)p;
+  for (;;) {
+    pthread_mutex_lock(&pool->mu);
+    int r = pool->next++;
+    pthread_mutex_unlock(&pool->mu);
+    if (r >= pool->n) break;
+    /* one work item = one (query token i, sequence b, KV head h) */
+    DecodeArgs a = *pool->a;
+    const int T = pool->T, Hq = a.Hq, d = a.d, G = a.Hq / a.Hkv;
+    const int h = r % a.Hkv, b = (r / a.Hkv) % a.B, i = r / (a.Hkv * a.B);
+    a.q = pool->q + (size_t)i * Hq * d;  /* query token i of every sequence */
+    int64_t lim = (int64_t)a.seq_lens[b] - T + 1 + i;
+    if (lim < 0) lim = 0;
+    for (int g = 0; g < G; ++g) {
+      const int hq = h * G + g;
+      const size_t row = ((size_t)b * T + i) * Hq + hq;
+      int rc = decode_range(&a, b, hq, 0, lim, pool->out + row * d, pool->lse + row);
+      if (rc) {
+        pthread_mutex_lock(&pool->mu);
+        pool->rc = rc;
+        pthread_mutex_unlock(&pool->mu);
+      }
+    }
+  }
+  return NULL;
+}
+
+int or_attend_multi(const uint16_t *q, const uint16_t *k_pool, const uint16_t *v_pool,
+                    const int32_t *block_table, int max_pages, int num_pages,
+                    const int32_t *seq_lens, int B, int T, int page_size, int Hq, int Hkv, int d,
+                    int dtype, double scale, double *out, double *lse, int nthreads) {
+  if (T < 1) return OR_EINVAL;
+  DecodeArgs a = {q, k_pool, v_pool, block_table, seq_lens, max_pages, num_pages,
+                  B, page_size, Hq, Hkv, d, dtype, scale, (size_t)T * Hq * d};
+  int rc = check_decode_args(&a);
+  if (rc) return rc;
+  MultiPool pool;
+  pool.a = &a;
+  pool.q = q;
+  pool.T = T;
+  pool.out = out;
+  pool.lse = lse;
+  pool.next = 0;
+  pool.n = T * B * Hkv;
+  pool.rc = OR_OK;
+  pthread_mutex_init(&pool.mu, NULL);
+  if (nthreads < 1) nthreads = 1;
+  pthread_t *th = (pthread_t *)malloc(sizeof(pthread_t) * nthreads);
+  for (int k = 0; k < nthreads; ++k) pthread_create(&th[k], NULL, multi_worker, &pool);
+  for (int k = 0; k < nthreads; ++k) pthread_join(th[k], NULL);
+  free(th);
+  pthread_mutex_destroy(&pool.mu);
+  return pool.rc;
 }
 
 /* Log-sum-exp merge of split partials (the exact recombination of softmax

@@ -66,6 +66,8 @@ def _declare(L):
     L.or_decode_rows.restype = I
     L.or_decode_range.argtypes = dec + [I, I, I64, I64, P, P]
     L.or_decode_range.restype = I
+    L.or_attend_multi.argtypes = [P, P, P, P, I, I, P, I, I, I, I, I, I, I, D, P, P, I]
+    L.or_attend_multi.restype = I
     L.or_merge.argtypes = [P, P, I, I, P, P]
     L.or_merge.restype = None
     L.or_chunk_auto.argtypes = [I64, I64, I64]
@@ -161,6 +163,21 @@ def decode_range(x, b, hq, t0, t1):
     _check(lib().or_decode_range(*_dec_args(x), int(b), int(hq), int(t0), int(t1),
                                  _p(out), _p(lse)))
     return out, float(lse[0])
+
+
+def attend_multi(x, q_multi, nthreads: int = 1):
+    """T query tokens per sequence (the last T tokens, causal) -> (out [B, T, Hq, d] f64,
+    lse [B, T, Hq] f64).  q_multi [B, T, Hq, d] 16-bit bits; the rest of x as for decode."""
+    _dec_fix(x)
+    q_multi = _c(q_multi, np.uint16)
+    B, T, Hq, d = q_multi.shape
+    out = np.zeros((B, T, Hq, d), dtype=np.float64)
+    lse = np.zeros((B, T, Hq), dtype=np.float64)
+    _check(lib().or_attend_multi(_p(q_multi), _p(x.k_pool), _p(x.v_pool), _p(x.block_table),
+                                 x.max_pages, x.num_pages, _p(x.seq_lens), B, T, x.page_size, Hq,
+                                 x.Hkv, d, x.dtype, float(x.scale), _p(out), _p(lse),
+                                 int(nthreads)))
+    return out, lse
 
 
 def merge(lse_parts, out_parts):

@@ -90,11 +90,13 @@ DecodeLayout decode_layout(int B, int Hq, int Hkv, int d, int max_pages, int pag
                            int pages_per_split, long long n_workers);
 
 // Decode entry used by both the device-pointer and the host-IO calls.
+// seqs_per_row > 1: sequences b read block-table row b / seqs_per_row (the
+// virtual sequences of a multi-token query share their sequence's row).
 int decode_launch(const void* q, const void* k_pool, const void* v_pool, int num_pages,
                   const int32_t* block_table, int max_pages, const int32_t* seq_lens, int B,
                   int page_size, int Hq, int Hkv, int d, int dtype, float scale,
                   int pages_per_split, float* out, float* lse, void* ws, size_t ws_bytes,
-                  cudaStream_t stream);
+                  cudaStream_t stream, int seqs_per_row = 1);
 int decode_num_workers(int Hq, int Hkv, int d, int page_size, int dtype);
 
 // One-shot profiling events for the next decode on this host thread.

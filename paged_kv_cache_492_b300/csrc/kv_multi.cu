@@ -1,0 +1,80 @@
+// Attention of several new query tokens per sequence over the paged cache --
+// the step before decode (a prefill chunk, or the verification of drafted
+// tokens), over the same pool and block table.  The T query tokens of
+// sequence b are its last T cached tokens (their K/V already appended), and
+// query i attends causally to tokens [0, L_b - T + 1 + i).
+//
+// This first form runs the decode kernel unchanged on B*T virtual sequences:
+// virtual sequence b*T + i has length max(0, L_b - T + 1 + i), reads block-
+// table row b, query row q[b][i] and output row out[b][i].  Each page is
+// therefore streamed once per query token (T times in all).
+#include "kv_internal.h"
+
+namespace kvb {
+namespace {
+
+struct MultiLensArgs {
+  const int32_t* seq_lens;
+  int B, T;
+  int32_t* lens_v;  // [B * T]
+};
+
+__global__ void multi_lens_kernel(const MultiLensArgs a) {
+  pdl_wait();  // seq_lens may come from the previous kernel on the stream
+  pdl_launch_dependents();
+  for (long long v = (long long)blockIdx.x * blockDim.x + threadIdx.x; v < (long long)a.B * a.T;
+       v += (long long)gridDim.x * blockDim.x) {
+    const int b = (int)(v / a.T), i = (int)(v - (long long)b * a.T);
+    const int L = a.seq_lens[b];
+    // a negative length stays negative so the decode reports it
+    a.lens_v[v] = L < 0 ? L : max(0, L - a.T + 1 + i);
+  }
+}
+
+size_t lens_offset(size_t decode_bytes) { return align_up(decode_bytes, 256); }
+
+}  // namespace
+}  // namespace kvb
+
+using namespace kvb;
+
+extern "C" {
+
+size_t kv_attend_multi_workspace_size(int B, int T, int Hq, int Hkv, int d, int max_pages,
+                                      int page_size, int pages_per_split) {
+  if (B < 0 || T < 1) return 0;
+  const size_t base = kv_decode_workspace_size(B * T, Hq, Hkv, d, max_pages, page_size,
+                                               pages_per_split);
+  if (!base) return 0;
+  return lens_offset(base) + align_up((size_t)(B > 0 ? B : 1) * T * 4, 256);
+}
+
+int kv_attend_multi(const void* q, const void* k_pool, const void* v_pool, int num_pages,
+                    const int32_t* block_table, int max_pages, const int32_t* seq_lens, int B,
+                    int T, int page_size, int Hq, int Hkv, int d, int dtype, float scale,
+                    int pages_per_split, float* out, float* lse, void* ws, size_t ws_bytes,
+                    void* stream) {
+  if (B < 0 || T < 1 || (long long)B * T > 0x7fffffffll) return KV_EINVAL;
+  if (B == 0) return KV_OK;
+  if (!seq_lens || !ws) return KV_EINVAL;
+  const size_t base = kv_decode_workspace_size(B * T, Hq, Hkv, d, max_pages, page_size,
+                                               pages_per_split);
+  if (!base) return KV_EINVAL;
+  if (ws_bytes < kv_attend_multi_workspace_size(B, T, Hq, Hkv, d, max_pages, page_size,
+                                                pages_per_split))
+    return KV_EWORKSPACE;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  MultiLensArgs a{};
+  a.seq_lens = seq_lens;
+  a.B = B;
+  a.T = T;
+  a.lens_v = reinterpret_cast<int32_t*>(static_cast<uint8_t*>(ws) + lens_offset(base));
+  const long long n = (long long)B * T;
+  const unsigned blocks = (unsigned)((n + 255) / 256 < 1024 ? (n + 255) / 256 : 1024);
+  KV_CUDA_CHECK(launch(multi_lens_kernel, dim3(blocks), dim3(256), 0, s, true, a));
+  return decode_launch(q, k_pool, v_pool, num_pages, block_table, max_pages, a.lens_v, B * T,
+                       page_size, Hq, Hkv, d, dtype, scale, pages_per_split, out, lse, ws, base, s,
+                       T);
+}
+
+}  // extern "C"

@@ -74,6 +74,8 @@ _SIGS = {
     "kv_decode_hostio": ([P, P, P, I, P, I, P, I, I, I, I, I, I, F, I, P, P, P, SZ, P], I),
     "kv_workqueue_workspace_size": ([I], SZ),
     "kv_profile_next_decode": ([P, P], I),
+    "kv_attend_multi_workspace_size": ([I, I, I, I, I, I, I, I], SZ),
+    "kv_attend_multi": ([P, P, P, I, P, I, P, I, I, I, I, I, I, I, F, I, P, P, P, SZ, P], I),
     "kv_decode_tune": ([P, P, P, I, P, I, P, I, I, I, I, I, I, F, P, I, I, P, P, P, P, P, SZ, P],
                        I),
     "kv_build_workqueue": ([P, I, I, I, I, I, I, P, I, P, I, P, P, P, P, P], I),
@@ -250,6 +252,25 @@ def kv_decode_hostio(h_q, k_pool, v_pool, h_block_table, h_seq_lens, scale, h_ou
     _check(rc, "kv_decode_hostio")
 
 
+def kv_attend_multi_workspace_size(B, T, Hq, Hkv, d, max_pages, page_size=16,
+                                   pages_per_split=0) -> int:
+    return lib().kv_attend_multi_workspace_size(B, T, Hq, Hkv, d, max_pages, page_size,
+                                                pages_per_split)
+
+
+def kv_attend_multi(q, k_pool, v_pool, block_table, seq_lens, scale, out, lse, ws,
+                    pages_per_split=0, stream=None):
+    """q [B, T, Hq, d] (the last T tokens of each sequence, causal), out
+    [B, T, Hq, d] f32, lse [B, T, Hq] f32."""
+    B, T, Hq, d = q.shape
+    P_, Hkv, ps, _ = k_pool.shape
+    rc = lib().kv_attend_multi(_p(q), _p(k_pool), _p(v_pool), P_, _p(block_table),
+                               block_table.shape[1], _p(seq_lens), B, T, ps, Hq, Hkv, d,
+                               dtype_code(q), float(scale), int(pages_per_split), _p(out), _p(lse),
+                               _p(ws), ws.numel(), _s(stream))
+    _check(rc, "kv_attend_multi")
+
+
 def kv_decode_tune(q, k_pool, v_pool, block_table, seq_lens, scale, out, lse, ws, candidates,
                    reps=5, stream=None):
     """Time kv_decode for each candidate pages_per_split (0 = automatic) on
@@ -298,6 +319,23 @@ class DecodePolicy:
                                       self.candidates, self.reps, stream)
             self.table[sig] = (best, dict(zip(self.candidates, us)))
         return self.table[sig][0]
+
+
+def prepare_decode_hostio(h_q, k_pool, v_pool, h_block_table, h_seq_lens, scale, h_out, h_lse, ws,
+                          pages_per_split=0, stream=None):
+    """kv_decode_hostio with its arguments marshalled once (see prepare_decode)."""
+    B, Hq, d = h_q.shape
+    P_, Hkv, ps, _ = k_pool.shape
+    fn = lib().kv_decode_hostio
+    args = (_p(h_q), _p(k_pool), _p(v_pool), P_, _p(h_block_table), h_block_table.shape[1],
+            _p(h_seq_lens), B, ps, Hq, Hkv, d, dtype_code(k_pool), float(scale),
+            int(pages_per_split), _p(h_out), _p(h_lse), _p(ws), ws.numel(), _s(stream))
+    cargs = [t(a) if a is not None else None for t, a in zip(fn.argtypes, args)]
+
+    def call() -> int:
+        return fn(*cargs)
+
+    return call
 
 
 def kv_profile_next_decode(event_before, event_after):

@@ -254,6 +254,46 @@ def pin_split_merge_invariance():
     assert np.allclose(o, out[0, 0], atol=1e-14) and abs(l - lse[0, 0]) < 1e-14
 
 
+def pin_attend_multi():
+    """T query tokens per sequence (the last T, causal): T = 1 is decode;
+    query i is decode over the first L - T + 1 + i tokens; and torch fp64
+    SDPA with an explicit causal mask on a dense copy agrees."""
+    rng = np.random.default_rng(17)
+    for dtype, G, T in ((W.F16, 4, 3), (W.BF16, 2, 1), (W.F16, 1, 5)):
+        Hkv = 2
+        x = W.small_decode(60 + T, B=3, Hq=Hkv * G, Hkv=Hkv, d=32, seq_lens=[37, 3, 16],
+                           dtype=dtype, pad_pages=1)
+        qm = W.normal_bits(rng, (x.B, T, x.Hq, x.d), dtype)
+        out, lse = O.attend_multi(x, qm)
+        for i in range(T):
+            y = W.DecodeInputs(**{**x.__dict__, "q": np.ascontiguousarray(qm[:, i]),
+                                  "seq_lens": np.maximum(0, x.seq_lens - T + 1 + i).astype(np.int32)})
+            o1, l1 = O.decode(y)
+            assert np.allclose(out[:, i], o1, rtol=0, atol=1e-13)
+            assert np.array_equal(np.isneginf(lse[:, i]), np.isneginf(l1))
+            fin = np.isfinite(l1)
+            assert np.allclose(lse[:, i][fin], l1[fin], rtol=0, atol=1e-13)
+        for b in range(x.B):
+            L = int(x.seq_lens[b])
+            k, v = _gather(x, b)
+            qd = torch.from_numpy(_f64(qm[b], dtype)).permute(1, 0, 2)[None]  # [1,Hq,T,d]
+            kd = torch.from_numpy(_f64(k, dtype)).permute(1, 0, 2)[None]
+            vd = torch.from_numpy(_f64(v, dtype)).permute(1, 0, 2)[None]
+            pos = torch.arange(L)[None, :]
+            lim = (L - T + 1 + torch.arange(T))[:, None]
+            mask = pos < lim                                                 # [T, L]
+            ok = mask.any(dim=1)
+            if not ok.any():
+                continue
+            ref = torch.nn.functional.scaled_dot_product_attention(
+                qd[:, :, ok], kd, vd, attn_mask=mask[ok], scale=x.scale, enable_gqa=True)
+            got = torch.from_numpy(out[b][ok.numpy()]).permute(1, 0, 2)[None]
+            assert torch.allclose(got, ref, rtol=0, atol=1e-12)
+        if T == 1:
+            o0, l0 = O.decode(W.DecodeInputs(**{**x.__dict__, "q": np.ascontiguousarray(qm[:, 0])}))
+            assert np.allclose(out[:, 0], o0, rtol=0, atol=0)
+
+
 def pin_decode_edge_cases():
     x = W.small_decode(29, B=3, Hq=4, Hkv=2, d=32, seq_lens=[0, 16, 17], pad_pages=2)
     out, lse = O.decode(x)

@@ -1,0 +1,73 @@
+"""GPU parity of multi-token query attention (kv_attend_multi): T new query
+tokens per sequence, the last T of its cached tokens, each attending
+causally, over the same pool and block table as decode."""
+import os
+
+import numpy as np
+import pytest
+import torch
+
+from oracle import oracle as O
+from paged_kv_cache_492_b300 import kv
+from paged_kv_cache_492_b300 import workloads as W
+from tests.gpu_util import DeviceDecode, bits_to_dev, vmax_per_seq
+
+pytestmark = pytest.mark.gpu
+NCPU = len(os.sched_getaffinity(0))
+
+
+def _run(x, qm, T, pps=0):
+    dd = DeviceDecode(x)
+    q = bits_to_dev(qm, x.dtype)
+    out = torch.full((x.B, T, x.Hq, x.d), float("nan"), dtype=torch.float32, device="cuda")
+    lse = torch.full((x.B, T, x.Hq), float("nan"), dtype=torch.float32, device="cuda")
+    ws = kv.alloc_workspace(kv.kv_attend_multi_workspace_size(x.B, T, x.Hq, x.Hkv, x.d,
+                                                              x.max_pages, 16, pps))
+    kv.kv_attend_multi(q, dd.k, dd.v, dd.table, dd.lens, x.scale, out, lse, ws,
+                       pages_per_split=pps)
+    assert kv.kv_get_status(ws) == 0
+    return out.cpu().numpy().astype(np.float64), lse.cpu().numpy().astype(np.float64)
+
+
+def _check(x, T, out, lse, ref_out, ref_lse):
+    vmax = vmax_per_seq(x)
+    for b in range(x.B):
+        for i in range(T):
+            if int(x.seq_lens[b]) - T + 1 + i <= 0:
+                assert np.all(out[b, i] == 0) and np.all(np.isneginf(lse[b, i])), (b, i)
+                continue
+            assert np.abs(out[b, i] - ref_out[b, i]).max() <= 2e-3 * vmax[b], (b, i)
+            assert np.abs(lse[b, i] - ref_lse[b, i]).max() <= 1e-3, (b, i)
+
+
+@pytest.mark.parametrize("T,dtype,G,lens,pps", [
+    (4, W.F16, 4, [3000, 17, 0, 2, 900], 0),
+    (2, W.BF16, 4, [1, 16, 33, 5000], 3),
+    (8, W.F16, 2, [100, 7, 1200], 0),
+    (1, W.BF16, 8, [640, 12], 0),
+])
+def test_attend_multi_small(T, dtype, G, lens, pps):
+    rng = np.random.default_rng(T * 10 + G)
+    Hkv = 8 if G * 8 <= 64 else 4
+    x = W.small_decode(90 + T, len(lens), Hkv * G, Hkv, 128, lens, dtype=dtype, pad_pages=1)
+    qm = W.normal_bits(rng, (x.B, T, x.Hq, x.d), dtype)
+    out, lse = _run(x, qm, T, pps)
+    ref_out, ref_lse = O.attend_multi(x, qm, nthreads=NCPU)
+    _check(x, T, out, lse, ref_out, ref_lse)
+
+
+def test_attend_multi_bimodal_t4():
+    """Four query tokens per sequence on the batch-8 bimodal fp16 workload."""
+    x = W.bimodal()
+    rng = np.random.default_rng(4)
+    qm = W.normal_bits(rng, (x.B, 4, x.Hq, x.d), x.dtype)
+    out, lse = _run(x, qm, 4)
+    ref_out, ref_lse = O.attend_multi(x, qm, nthreads=NCPU)
+    _check(x, 4, out, lse, ref_out, ref_lse)
+
+
+def test_attend_multi_t1_is_decode():
+    x = W.small_decode(97, 3, 32, 8, 128, [700, 33, 2100])
+    out, lse = _run(x, x.q[:, None], 1)
+    o, l, rc = DeviceDecode(x).run()
+    assert rc == 0 and np.array_equal(out[:, 0], o) and np.array_equal(lse[:, 0], l)

@@ -19,6 +19,9 @@ MUTANTS = [
     ("merge_weight", "double w = exp(lse_parts[s] - *lse);", "double w = exp(lse_parts[s] - m);", 0),
     ("wq_first_chunk", "int64_t c_first = O / chunk", "int64_t c_first = (O + 1) / chunk", 0),
     ("wq_page_end", "r[5] = (int32_t)(hi - O);", "r[5] = (int32_t)(hi - O - 1);", 0),
+    ("multi_causal", "int64_t lim = (int64_t)a.seq_lens[b] - T + 1 + i;",
+     "int64_t lim = (int64_t)a.seq_lens[b] - T + i;", 0),
+    ("multi_q_row", "a.q = pool->q + (size_t)i * Hq * d;", "a.q = pool->q + (size_t)(T - 1 - i) * Hq * d;", 0),
     ("f16_bias", "v = ldexp((double)(1024 + m), e - 25);", "v = ldexp((double)(1024 + m), e - 24);", 0),
     ("bf16_subnormal", "v = ldexp((double)m, -133);", "v = ldexp((double)m, -134);", 0),
     ("ema_decay_swap", "*e = first ? gm : a[u] * *e + (1.0 - a[u]) * gm;",
