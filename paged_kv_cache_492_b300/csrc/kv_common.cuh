@@ -166,6 +166,17 @@ __host__ __device__ inline void split_range(long long O, long long np, long long
   *hi = e - O;
 }
 
+// Largest b in [0, B) with O[b] <= x (O nondecreasing, O[0] = 0 <= x): the
+// sequence that owns flattened page x.
+__device__ __forceinline__ int seq_at(const int32_t* O, int B, long long x) {
+  int lo = 0, hi = B - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (O[mid] <= x) lo = mid; else hi = mid - 1;
+  }
+  return lo;
+}
+
 // Exclusive block-wide scan of one value per thread (blockDim a multiple of
 // 32, at most 1024); returns the total.  `sm` holds 32 values.
 __device__ __forceinline__ long long block_exclusive_scan(long long v, long long* out_excl, long long* sm) {

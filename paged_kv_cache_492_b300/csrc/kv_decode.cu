@@ -91,16 +91,6 @@ __host__ __device__ constexpr uint32_t stage_header_offset(uint32_t kv_bytes, ui
   return 2 * kv_bytes + q_bytes;
 }
 
-// Largest b in [0, B) with O[b] <= x (O nondecreasing, O[0] = 0 <= x).
-__device__ __forceinline__ int seq_at(const int32_t* O, int B, long long x) {
-  int lo = 0, hi = B - 1;
-  while (lo < hi) {
-    const int mid = (lo + hi + 1) >> 1;
-    if (O[mid] <= x) lo = mid; else hi = mid - 1;
-  }
-  return lo;
-}
-
 template <int D, int G, class T>
 __global__ void __launch_bounds__(kDecodeThreadsMax, 1) decode_kernel(const DecodeParams p) {
   constexpr int CH = D / 8;                 // q.k channels per lane (8 lanes per row)

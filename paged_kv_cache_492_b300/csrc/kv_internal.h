@@ -99,6 +99,15 @@ int decode_launch(const void* q, const void* k_pool, const void* v_pool, int num
                   cudaStream_t stream, int seqs_per_row = 1);
 int decode_num_workers(int Hq, int Hkv, int d, int page_size, int dtype);
 
+// Tensor-core attention of T * G <= 16 query rows per KV head (d = 128,
+// page_size 16): one TMA-fed warp per workqueue task and a merge kernel.
+bool mma_attend_supported(int Hq, int Hkv, int d, int Tq);
+size_t mma_attend_workspace_size(int B, int Hkv, int max_pages, int pages_per_split);
+int mma_attend_launch(const void* q, const void* k_pool, const void* v_pool, int num_pages,
+                      const int32_t* block_table, int max_pages, const int32_t* seq_lens, int B,
+                      int Tq, int Hq, int Hkv, int dtype, float scale, int pages_per_split,
+                      float* out, float* lse, void* ws, size_t ws_bytes, cudaStream_t stream);
+
 // One-shot profiling events for the next decode on this host thread.
 void set_profile_events(cudaEvent_t before, cudaEvent_t after);
 void take_profile_events(cudaEvent_t* before, cudaEvent_t* after);

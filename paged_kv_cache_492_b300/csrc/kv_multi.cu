@@ -4,10 +4,12 @@
 // sequence b are its last T cached tokens (their K/V already appended), and
 // query i attends causally to tokens [0, L_b - T + 1 + i).
 //
-// This first form runs the decode kernel unchanged on B*T virtual sequences:
-// virtual sequence b*T + i has length max(0, L_b - T + 1 + i), reads block-
-// table row b, query row q[b][i] and output row out[b][i].  Each page is
-// therefore streamed once per query token (T times in all).
+// Two forms.  Where T * G <= 16 rows per KV head fit one tensor-core tile
+// (d = 128, page size 16) and T >= 2 or G >= 8, the tensor-core kernel
+// (kv_mma.cu) streams each page once for all T tokens.  Otherwise the decode kernel runs unchanged on
+// B*T virtual sequences: virtual sequence b*T + i has length
+// max(0, L_b - T + 1 + i), reads block-table row b, query row q[b][i] and
+// output row out[b][i], so each page is streamed once per query token.
 #include "kv_internal.h"
 
 namespace kvb {
@@ -33,6 +35,13 @@ __global__ void multi_lens_kernel(const MultiLensArgs a) {
 
 size_t lens_offset(size_t decode_bytes) { return align_up(decode_bytes, 256); }
 
+// The tensor-core form wherever it applies and streams less than the decode
+// kernel would: several tokens (the views would stream each page T times) or
+// a group of 8+ heads (more rows than the decode kernel keeps in registers).
+bool use_mma(int page_size, int Hq, int Hkv, int d, int T) {
+  return page_size == 16 && mma_attend_supported(Hq, Hkv, d, T) && (T >= 2 || Hq / Hkv >= 8);
+}
+
 }  // namespace
 }  // namespace kvb
 
@@ -43,6 +52,8 @@ extern "C" {
 size_t kv_attend_multi_workspace_size(int B, int T, int Hq, int Hkv, int d, int max_pages,
                                       int page_size, int pages_per_split) {
   if (B < 0 || T < 1) return 0;
+  if (use_mma(page_size, Hq, Hkv, d, T))
+    return mma_attend_workspace_size(B, Hkv, max_pages, pages_per_split);
   const size_t base = kv_decode_workspace_size(B * T, Hq, Hkv, d, max_pages, page_size,
                                                pages_per_split);
   if (!base) return 0;
@@ -57,13 +68,17 @@ int kv_attend_multi(const void* q, const void* k_pool, const void* v_pool, int n
   if (B < 0 || T < 1 || (long long)B * T > 0x7fffffffll) return KV_EINVAL;
   if (B == 0) return KV_OK;
   if (!seq_lens || !ws) return KV_EINVAL;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (use_mma(page_size, Hq, Hkv, d, T)) {
+    return mma_attend_launch(q, k_pool, v_pool, num_pages, block_table, max_pages, seq_lens, B, T,
+                             Hq, Hkv, dtype, scale, pages_per_split, out, lse, ws, ws_bytes, s);
+  }
   const size_t base = kv_decode_workspace_size(B * T, Hq, Hkv, d, max_pages, page_size,
                                                pages_per_split);
   if (!base) return KV_EINVAL;
   if (ws_bytes < kv_attend_multi_workspace_size(B, T, Hq, Hkv, d, max_pages, page_size,
                                                 pages_per_split))
     return KV_EWORKSPACE;
-  cudaStream_t s = static_cast<cudaStream_t>(stream);
   MultiLensArgs a{};
   a.seq_lens = seq_lens;
   a.B = B;
