@@ -73,6 +73,10 @@ extern "C" {
 #define KV_F16 0
 #define KV_BF16 1
 
+/* pages_per_split value that selects the tensor-core decode engine (see
+ * kv_decode). */
+#define KV_DECODE_TENSOR_CORE (-1)
+
 /* Text for a status code (static storage). */
 const char *kv_status_string(int code);
 
@@ -104,7 +108,10 @@ int kv_get_status(void *ws, void *stream);
 int kv_decode_num_workers(int Hq, int Hkv, int d, int page_size, int dtype);
 
 /* Workspace bytes kv_decode needs for a batch of B sequences whose tables are
- * max_pages wide.  pages_per_split as passed to kv_decode (0 = automatic).
+ * max_pages wide.  pages_per_split as passed to kv_decode (0 = automatic;
+ * KV_DECODE_TENSOR_CORE: the tensor-core engine, whose size also covers the
+ * fused kernel with the automatic split, and whose scratch lies past the
+ * fused kernel's merge tickets for every split size).
  * Besides scratch, a decode workspace keeps one merge ticket per (sequence,
  * KV head) that must read zero when a call starts: every kv_decode that
  * completes leaves them zero, so a decode workspace stays valid across
@@ -127,7 +134,14 @@ size_t kv_decode_workspace_size(int B, int Hq, int Hkv, int d, int max_pages, in
  * materialises).  A task streams each (page, KV head) tile once from HBM and
  * reuses it for all G = Hq/Hkv query heads; splits of one sequence are
  * recombined by a log-sum-exp merge done by whichever split finishes last.
- * One kernel launch (two for B > 1024: a page-offset pass first). 
+ * One kernel launch (two for B > 1024: a page-offset pass first).
+ * pages_per_split = KV_DECODE_TENSOR_CORE selects the tensor-core engine
+ * instead (d = 128, page_size 16, G <= 16; else KV_EINVAL): the same split
+ * rule with the automatic chunk, one CTA per chunk streaming whole pages by
+ * TMA tensor copies, Q K^T and P V on mma.sync (fp32 accumulation), and a
+ * merge kernel for the split sequences (kv_attend_multi with T = 1).  Both
+ * engines compute the same function; which is faster depends on the
+ * workload (kv_decode_tune).
  * Device errors: KV_EBADPAGE (an entry in [0, ceil(L_b/16)) outside
  * [0, num_pages); page 0 is read in its place), KV_EINVAL (L_b < 0 or more
  * pages than max_pages), KV_EWORKSPACE, KV_ETIMEOUT. */
@@ -146,10 +160,12 @@ int kv_decode(const void *q, const void *k_pool, const void *v_pool, int num_pag
  * a query with no token to attend to gets out = 0 and lse = -inf.
  * q [B][T][Hq][d] 16-bit, out [B][T][Hq][d] fp32, lse [B][T][Hq] fp32
  * (device).  Other arguments and errors as kv_decode; the workspace is
- * kv_attend_multi_workspace_size bytes and, as for kv_decode, keeps merge
- * tickets between calls (give it its own).  This form runs the decode
- * kernel on B*T causal views of the batch, so each page is streamed once per
- * query token. */
+ * kv_attend_multi_workspace_size bytes (give it its own).  Where T * G <= 16
+ * (d = 128, page_size 16) the tensor-core engine streams each page once for
+ * all T tokens (T = 1 is kv_decode's KV_DECODE_TENSOR_CORE engine);
+ * otherwise the fused decode kernel runs on B*T causal views of the batch,
+ * streaming each page once per query token, and the workspace keeps its
+ * merge tickets between calls as kv_decode's does. */
 size_t kv_attend_multi_workspace_size(int B, int T, int Hq, int Hkv, int d, int max_pages,
                                       int page_size, int pages_per_split);
 int kv_attend_multi(const void *q, const void *k_pool, const void *v_pool, int num_pages,
@@ -160,14 +176,15 @@ int kv_attend_multi(const void *q, const void *k_pool, const void *v_pool, int n
 
 /* Calibration among this library's own decode variants (the adaptive policy
  * of [PKV] Summary picks an engine per workload by measurement; here the
- * variants are split sizes): runs kv_decode on the given inputs once per
- * candidate pages_per_split (0 = automatic) untimed, then `reps` (<= 64)
+ * variants are the fused kernel's split sizes and the tensor-core engine):
+ * runs kv_decode on the given inputs once per candidate pages_per_split
+ * (0 = automatic, KV_DECODE_TENSOR_CORE = tensor-core engine) untimed, then `reps` (<= 64)
  * times timed with CUDA events on `stream`, writes the median microseconds
  * per candidate to us[n_candidates] (host) and the fastest candidate to
  * *best (host).  Synchronises `stream`; out/lse hold the last call's result.
  * `ws` must be sized for every candidate (kv_decode_workspace_size with the
- * smallest positive candidate covers all of them and the automatic one is
- * covered by its own size: pass the larger). */
+ * smallest positive candidate covers all positive ones, and the size for
+ * KV_DECODE_TENSOR_CORE covers it and the automatic one: pass the larger). */
 int kv_decode_tune(const void *q, const void *k_pool, const void *v_pool, int num_pages,
                    const int32_t *block_table, int max_pages, const int32_t *seq_lens, int B,
                    int page_size, int Hq, int Hkv, int d, int dtype, float scale,

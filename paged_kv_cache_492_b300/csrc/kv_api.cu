@@ -68,12 +68,65 @@ int kv_decode_num_workers(int Hq, int Hkv, int d, int page_size, int dtype) {
   return decode_num_workers(Hq, Hkv, d, page_size, dtype);
 }
 
+namespace {
+
+int decode_workers_both(int Hq, int Hkv, int d, int page_size) {
+  // the worker count can differ between the fp16 and bf16 kernels: size for both
+  return std::max(decode_num_workers(Hq, Hkv, d, page_size, KV_F16),
+                  decode_num_workers(Hq, Hkv, d, page_size, KV_BF16));
+}
+
+bool tensor_core_ok(int page_size, int Hq, int Hkv, int d) {
+  return page_size == 16 && mma_attend_supported(Hq, Hkv, d, 1);
+}
+
+// Where the tensor-core engine's scratch starts inside a decode workspace:
+// past the decode kernel's merge tickets for every split size (the finest
+// split, one page, has the most) and past its whole automatic-split layout,
+// so the two engines can take turns on one workspace (as kv_decode_tune
+// does) without touching each other's state.  Shapes the fused kernel does
+// not support need no room for it.
+size_t tensor_core_region(int B, int Hq, int Hkv, int d, int max_pages, int page_size) {
+  const int nw = decode_workers_both(Hq, Hkv, d, page_size);
+  if (nw <= 0) return kHeaderBytes;
+  const DecodeLayout a = decode_layout(B, Hq, Hkv, d, max_pages, page_size, 0, nw);
+  const DecodeLayout f = decode_layout(B, Hq, Hkv, d, max_pages, page_size, 1, nw);
+  return align_up(std::max(a.total, f.page_off), 256);
+}
+
+// One decode step with the engine `pages_per_split` names: >= 0 the fused
+// decode kernel with that split size, KV_DECODE_TENSOR_CORE the tensor-core
+// engine (automatic split).
+int engine_launch(const void* q, const void* k_pool, const void* v_pool, int num_pages,
+                  const int32_t* block_table, int max_pages, const int32_t* seq_lens, int B,
+                  int page_size, int Hq, int Hkv, int d, int dtype, float scale,
+                  int pages_per_split, float* out, float* lse, void* ws, size_t ws_bytes,
+                  cudaStream_t s) {
+  if (pages_per_split != KV_DECODE_TENSOR_CORE)
+    return decode_launch(q, k_pool, v_pool, num_pages, block_table, max_pages, seq_lens, B,
+                         page_size, Hq, Hkv, d, dtype, scale, pages_per_split, out, lse, ws,
+                         ws_bytes, s);
+  if (B < 0 || max_pages < 0 || Hq <= 0 || Hkv <= 0) return KV_EINVAL;
+  if (!tensor_core_ok(page_size, Hq, Hkv, d)) return KV_EINVAL;
+  if (B == 0) return KV_OK;
+  const size_t region = tensor_core_region(B, Hq, Hkv, d, max_pages, page_size);
+  if (!region) return KV_EINVAL;
+  return mma_attend_launch(q, k_pool, v_pool, num_pages, block_table, max_pages, seq_lens, B, 1,
+                           Hq, Hkv, dtype, scale, 0, out, lse, ws, ws_bytes, region, s);
+}
+
+}  // namespace
+
 size_t kv_decode_workspace_size(int B, int Hq, int Hkv, int d, int max_pages, int page_size,
                                 int pages_per_split) {
-  if (B < 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv || max_pages < 0 || pages_per_split < 0) return 0;
-  // the worker count can differ between the fp16 and bf16 kernels: size for both
-  const int nw = std::max(decode_num_workers(Hq, Hkv, d, page_size, KV_F16),
-                          decode_num_workers(Hq, Hkv, d, page_size, KV_BF16));
+  if (B < 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv || max_pages < 0) return 0;
+  if (pages_per_split == KV_DECODE_TENSOR_CORE) {
+    if (!tensor_core_ok(page_size, Hq, Hkv, d)) return 0;
+    const size_t region = tensor_core_region(B, Hq, Hkv, d, max_pages, page_size);
+    return region ? mma_attend_workspace_size(B, Hkv, max_pages, 0, region) : 0;
+  }
+  if (pages_per_split < 0) return 0;
+  const int nw = decode_workers_both(Hq, Hkv, d, page_size);
   if (nw <= 0) return 0;
   return decode_layout(B, Hq, Hkv, d, max_pages, page_size, pages_per_split, nw).total;
 }
@@ -82,7 +135,7 @@ int kv_decode(const void* q, const void* k_pool, const void* v_pool, int num_pag
               const int32_t* block_table, int max_pages, const int32_t* seq_lens, int B,
               int page_size, int Hq, int Hkv, int d, int dtype, float scale, int pages_per_split,
               float* out, float* lse, void* ws, size_t ws_bytes, void* stream) {
-  return decode_launch(q, k_pool, v_pool, num_pages, block_table, max_pages, seq_lens, B,
+  return engine_launch(q, k_pool, v_pool, num_pages, block_table, max_pages, seq_lens, B,
                        page_size, Hq, Hkv, d, dtype, scale, pages_per_split, out, lse, ws, ws_bytes,
                        static_cast<cudaStream_t>(stream));
 }
@@ -134,7 +187,7 @@ int kv_decode_hostio(const void* h_q, const void* k_pool, const void* v_pool, in
   KV_CUDA_CHECK(cudaMemcpyAsync(w + L.q, h_q, qb, cudaMemcpyHostToDevice, s));
   KV_CUDA_CHECK(cudaMemcpyAsync(w + L.table, h_block_table, tb, cudaMemcpyHostToDevice, s));
   KV_CUDA_CHECK(cudaMemcpyAsync(w + L.seq_lens, h_seq_lens, sb, cudaMemcpyHostToDevice, s));
-  int rc = decode_launch(w + L.q, k_pool, v_pool, num_pages,
+  int rc = engine_launch(w + L.q, k_pool, v_pool, num_pages,
                          reinterpret_cast<const int32_t*>(w + L.table), max_pages,
                          reinterpret_cast<const int32_t*>(w + L.seq_lens), B, page_size, Hq, Hkv, d,
                          dtype, scale, pages_per_split, reinterpret_cast<float*>(w + L.out),
@@ -200,12 +253,12 @@ int kv_decode_tune(const void* q, const void* k_pool, const void* v_pool, int nu
     float times[64];
     const int n = reps < 64 ? reps : 64;
     // one untimed call first (launch shape set-up, caches)
-    rc = decode_launch(q, k_pool, v_pool, num_pages, block_table, max_pages, seq_lens, B,
+    rc = engine_launch(q, k_pool, v_pool, num_pages, block_table, max_pages, seq_lens, B,
                        page_size, Hq, Hkv, d, dtype, scale, candidates[c], out, lse, ws, ws_bytes,
                        s);
     for (int r = 0; r < n && rc == KV_OK; ++r) {
       if (cudaEventRecord(e0, s) != cudaSuccess) { rc = cuda_failed(cudaErrorUnknown, "cudaEventRecord"); break; }
-      rc = decode_launch(q, k_pool, v_pool, num_pages, block_table, max_pages, seq_lens, B,
+      rc = engine_launch(q, k_pool, v_pool, num_pages, block_table, max_pages, seq_lens, B,
                          page_size, Hq, Hkv, d, dtype, scale, candidates[c], out, lse, ws,
                          ws_bytes, s);
       if (rc) break;

@@ -100,13 +100,17 @@ int decode_launch(const void* q, const void* k_pool, const void* v_pool, int num
 int decode_num_workers(int Hq, int Hkv, int d, int page_size, int dtype);
 
 // Tensor-core attention of T * G <= 16 query rows per KV head (d = 128,
-// page_size 16): one TMA-fed warp per workqueue task and a merge kernel.
+// page_size 16): one TMA-fed CTA per chunk of the batch's pages and a merge
+// kernel.  Its scratch starts `region` bytes into the workspace (the status
+// word stays at the workspace's start), so it can share a workspace with
+// the decode kernel's merge tickets.
 bool mma_attend_supported(int Hq, int Hkv, int d, int Tq);
-size_t mma_attend_workspace_size(int B, int Hkv, int max_pages, int pages_per_split);
+size_t mma_attend_workspace_size(int B, int Hkv, int max_pages, int pages_per_split, size_t region);
 int mma_attend_launch(const void* q, const void* k_pool, const void* v_pool, int num_pages,
                       const int32_t* block_table, int max_pages, const int32_t* seq_lens, int B,
                       int Tq, int Hq, int Hkv, int dtype, float scale, int pages_per_split,
-                      float* out, float* lse, void* ws, size_t ws_bytes, cudaStream_t stream);
+                      float* out, float* lse, void* ws, size_t ws_bytes, size_t region,
+                      cudaStream_t stream);
 
 // One-shot profiling events for the next decode on this host thread.
 void set_profile_events(cudaEvent_t before, cudaEvent_t after);

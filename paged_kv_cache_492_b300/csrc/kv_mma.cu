@@ -618,13 +618,14 @@ struct MmaLayout {
   long long max_chunks;
 };
 
-MmaLayout mma_layout(int B, int Hkv, int max_pages, int pages_per_split, long long n_chunks) {
+MmaLayout mma_layout(int B, int Hkv, int max_pages, int pages_per_split, long long n_chunks,
+                     size_t region) {
   MmaLayout L{};
   L.max_chunks = pages_per_split > 0 ? ceil_div_ll((long long)B * max_pages, pages_per_split)
                                      : n_chunks;
   if (L.max_chunks < 1) L.max_chunks = 1;
   const long long slots = 2 * L.max_chunks;
-  size_t off = kHeaderBytes;
+  size_t off = align_up(region < kHeaderBytes ? kHeaderBytes : region, 256);
   auto take = [&](size_t bytes) {
     size_t o = off;
     off = align_up(off + bytes, 256);
@@ -672,16 +673,18 @@ bool mma_attend_supported(int Hq, int Hkv, int d, int Tq) {
   return d == kMmaD && Hkv > 0 && Hq % Hkv == 0 && Tq >= 1 && (Hq / Hkv) * Tq <= kMmaRows;
 }
 
-size_t mma_attend_workspace_size(int B, int Hkv, int max_pages, int pages_per_split) {
+size_t mma_attend_workspace_size(int B, int Hkv, int max_pages, int pages_per_split,
+                                 size_t region) {
   long long chunks = 0;
-  if (Hkv < 1 || mma_chunks(Hkv, &chunks)) return 0;
-  return mma_layout(B, Hkv, max_pages, pages_per_split, chunks).total;
+  if (B < 0 || Hkv < 1 || max_pages < 0 || pages_per_split < 0 || mma_chunks(Hkv, &chunks)) return 0;
+  return mma_layout(B, Hkv, max_pages, pages_per_split, chunks, region).total;
 }
 
 int mma_attend_launch(const void* q, const void* k_pool, const void* v_pool, int num_pages,
                       const int32_t* block_table, int max_pages, const int32_t* seq_lens, int B,
                       int Tq, int Hq, int Hkv, int dtype, float scale, int pages_per_split,
-                      float* out, float* lse, void* ws, size_t ws_bytes, cudaStream_t stream) {
+                      float* out, float* lse, void* ws, size_t ws_bytes, size_t region,
+                      cudaStream_t stream) {
   if (!mma_attend_supported(Hq, Hkv, kMmaD, Tq) || (dtype != KV_F16 && dtype != KV_BF16))
     return KV_EINVAL;
   if (B < 0 || num_pages < 1 || max_pages < 0 || pages_per_split < 0) return KV_EINVAL;
@@ -695,7 +698,7 @@ int mma_attend_launch(const void* q, const void* k_pool, const void* v_pool, int
   long long chunks = 0;
   int rc = mma_chunks(Hkv, &chunks);
   if (rc) return rc;
-  const MmaLayout L = mma_layout(B, Hkv, max_pages, pages_per_split, chunks);
+  const MmaLayout L = mma_layout(B, Hkv, max_pages, pages_per_split, chunks, region);
   if (ws_bytes < L.total) return KV_EWORKSPACE;
   uint8_t* w = static_cast<uint8_t*>(ws);
   const int hb = head_block(Hkv), nhb = Hkv / hb;

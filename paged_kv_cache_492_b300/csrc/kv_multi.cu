@@ -5,8 +5,8 @@
 // query i attends causally to tokens [0, L_b - T + 1 + i).
 //
 // Two forms.  Where T * G <= 16 rows per KV head fit one tensor-core tile
-// (d = 128, page size 16) and T >= 2 or G >= 8, the tensor-core kernel
-// (kv_mma.cu) streams each page once for all T tokens.  Otherwise the decode kernel runs unchanged on
+// (d = 128, page size 16), the tensor-core kernel (kv_mma.cu) streams each
+// page once for all T tokens.  Otherwise the decode kernel runs unchanged on
 // B*T virtual sequences: virtual sequence b*T + i has length
 // max(0, L_b - T + 1 + i), reads block-table row b, query row q[b][i] and
 // output row out[b][i], so each page is streamed once per query token.
@@ -35,11 +35,10 @@ __global__ void multi_lens_kernel(const MultiLensArgs a) {
 
 size_t lens_offset(size_t decode_bytes) { return align_up(decode_bytes, 256); }
 
-// The tensor-core form wherever it applies and streams less than the decode
-// kernel would: several tokens (the views would stream each page T times) or
-// a group of 8+ heads (more rows than the decode kernel keeps in registers).
+// The tensor-core form wherever it applies: it streams each page once for
+// all T tokens, and at T = 1 it is the tensor-core decode engine.
 bool use_mma(int page_size, int Hq, int Hkv, int d, int T) {
-  return page_size == 16 && mma_attend_supported(Hq, Hkv, d, T) && (T >= 2 || Hq / Hkv >= 8);
+  return page_size == 16 && mma_attend_supported(Hq, Hkv, d, T);
 }
 
 }  // namespace
@@ -53,7 +52,7 @@ size_t kv_attend_multi_workspace_size(int B, int T, int Hq, int Hkv, int d, int 
                                       int page_size, int pages_per_split) {
   if (B < 0 || T < 1) return 0;
   if (use_mma(page_size, Hq, Hkv, d, T))
-    return mma_attend_workspace_size(B, Hkv, max_pages, pages_per_split);
+    return mma_attend_workspace_size(B, Hkv, max_pages, pages_per_split, kHeaderBytes);
   const size_t base = kv_decode_workspace_size(B * T, Hq, Hkv, d, max_pages, page_size,
                                                pages_per_split);
   if (!base) return 0;
@@ -71,7 +70,8 @@ int kv_attend_multi(const void* q, const void* k_pool, const void* v_pool, int n
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (use_mma(page_size, Hq, Hkv, d, T)) {
     return mma_attend_launch(q, k_pool, v_pool, num_pages, block_table, max_pages, seq_lens, B, T,
-                             Hq, Hkv, dtype, scale, pages_per_split, out, lse, ws, ws_bytes, s);
+                             Hq, Hkv, dtype, scale, pages_per_split, out, lse, ws, ws_bytes,
+                             kHeaderBytes, s);
   }
   const size_t base = kv_decode_workspace_size(B * T, Hq, Hkv, d, max_pages, page_size,
                                                pages_per_split);

@@ -21,6 +21,8 @@ from . import build as _build
 KV_OK, KV_EINVAL, KV_EBADPAGE, KV_ENOSPACE, KV_EWORKSPACE, KV_ECUDA, KV_EFULL, KV_ETIMEOUT = (
     0, -1, -2, -3, -4, -5, -6, -7)
 KV_F16, KV_BF16 = 0, 1
+# pages_per_split value selecting the tensor-core decode engine
+KV_DECODE_TENSOR_CORE = -1
 KV_SELECT_TOPK, KV_SELECT_BOUNDARY = 0, 1
 
 HEADER = os.path.join(_build.INCLUDE, "kv.h")
@@ -273,8 +275,9 @@ def kv_attend_multi(q, k_pool, v_pool, block_table, seq_lens, scale, out, lse, w
 
 def kv_decode_tune(q, k_pool, v_pool, block_table, seq_lens, scale, out, lse, ws, candidates,
                    reps=5, stream=None):
-    """Time kv_decode for each candidate pages_per_split (0 = automatic) on
-    these inputs -> (best candidate, [median us per candidate])."""
+    """Time kv_decode for each candidate pages_per_split (0 = automatic,
+    KV_DECODE_TENSOR_CORE = the tensor-core engine) on these inputs ->
+    (best candidate, [median us per candidate])."""
     B, Hq, d = q.shape
     P_, Hkv, ps, _ = k_pool.shape
     cand = (C.c_int32 * len(candidates))(*[int(c) for c in candidates])
@@ -289,17 +292,25 @@ def kv_decode_tune(q, k_pool, v_pool, block_table, seq_lens, scale, out, lse, ws
 
 
 class DecodePolicy:
-    """Per-workload choice of the split size, calibrated on first sight
-    (PersistentKV's adaptive policy, aissential.tech, Summary, restated among
-    this library's own variants).  A workload's signature is its batch size,
-    log2 of its page count and its long-to-mean length ratio (rounded); the
-    first batch with a new signature is timed with kv_decode_tune and the
-    fastest split size is reused for every later batch with that signature."""
+    """Per-workload choice of the decode engine and split size, calibrated on
+    first sight (PersistentKV's adaptive policy, aissential.tech, Summary,
+    restated among this library's own variants: the fused kernel's split
+    sizes and the tensor-core engine).  A workload's signature is its batch
+    size, log2 of its page count and its long-to-mean length ratio (rounded);
+    the first batch with a new signature is timed with kv_decode_tune and the
+    fastest variant is reused for every later batch with that signature.  The
+    workspace must be sized for every candidate (workspace_size)."""
 
-    def __init__(self, candidates=(0, 8, 16, 32, 64, 128), reps=5):
+    def __init__(self, candidates=(0, 8, 16, 32, 64, 128, KV_DECODE_TENSOR_CORE), reps=5):
         self.candidates = tuple(int(c) for c in candidates)
         self.reps = reps
         self.table = {}
+
+    def workspace_size(self, B, Hq, Hkv, d, max_pages, page_size=16):
+        """Bytes a workspace needs to run every candidate (0 when none fits)."""
+        sizes = [kv_decode_workspace_size(B, Hq, Hkv, d, max_pages, page_size, c)
+                 for c in self.candidates]
+        return 0 if not sizes or min(sizes) == 0 else max(sizes)
 
     @staticmethod
     def signature(seq_lens_host, page_size=16):
