@@ -195,9 +195,21 @@ def run_ours(args, x, name, rank, world):
     lens = torch.from_numpy(x.seq_lens).to(dev)
     out = torch.empty((x.B, x.Hq, x.d), dtype=torch.float32, device=dev)
     lse = torch.empty((x.B, x.Hq), dtype=torch.float32, device=dev)
-    ws = kv.alloc_workspace(kv.kv_decode_hostio_workspace_size(x.B, x.Hq, x.Hkv, x.d, x.max_pages),
-                            device=dev)
     flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
+
+    # The engine: PersistentKV's adaptive policy among this library's own
+    # variants (the fused kernel's split sizes and the tensor-core engine),
+    # calibrated once for the workload before any timing, as a server would
+    # on first sight of a batch shape.
+    policy = kv.DecodePolicy()
+    cands = list(policy.candidates)
+    ws_t = kv.alloc_workspace(policy.workspace_size(x.B, x.Hq, x.Hkv, x.d, x.max_pages), device=dev)
+    best, us = kv.kv_decode_tune(q, k, v, table, lens, x.scale, out, lse, ws_t, cands, reps=7)
+    del ws_t
+    pps = {"policy": best, "fused": 0, "tensor-core": kv.KV_DECODE_TENSOR_CORE}[args.engine]
+    tensor_core = pps == kv.KV_DECODE_TENSOR_CORE
+    ws = kv.alloc_workspace(kv.kv_decode_hostio_workspace_size(x.B, x.Hq, x.Hkv, x.d, x.max_pages,
+                                                               16, pps), device=dev)
 
     # host-side copies for the end-to-end (host buffers) leg
     hq = torch.from_numpy(x.q.view(np.int16).copy()).view(q.dtype).pin_memory()
@@ -206,7 +218,8 @@ def run_ours(args, x, name, rank, world):
     ho = torch.empty((x.B, x.Hq, x.d), dtype=torch.float32).pin_memory()
     hls = torch.empty((x.B, x.Hq), dtype=torch.float32).pin_memory()
 
-    decode = kv.prepare_decode(q, k, v, table, lens, x.scale, out, lse, ws, stream=stream)
+    decode = kv.prepare_decode(q, k, v, table, lens, x.scale, out, lse, ws, pages_per_split=pps,
+                               stream=stream)
 
     def step():
         rc = decode()
@@ -251,7 +264,8 @@ def run_ours(args, x, name, rank, world):
         torch.cuda.synchronize()
         # end-to-end through the host-buffer entry point (inputs copied in and
         # outputs copied back every step, the host waits for the result)
-        hostio = kv.prepare_decode_hostio(hq, k, v, ht, hl, x.scale, ho, hls, ws, stream=stream)
+        hostio = kv.prepare_decode_hostio(hq, k, v, ht, hl, x.scale, ho, hls, ws,
+                                          pages_per_split=pps, stream=stream)
         e2e_t = []
         for i in range(max(3, n // 2)):
             flush.zero_()
@@ -276,13 +290,16 @@ def run_ours(args, x, name, rank, world):
     peak, peak_kind = measured_peaks()
     value = whole_job_gbs(nbytes, t_step, world)
     achieved = nbytes / t_kern / 1e9
+    engine = "tensor_core" if tensor_core else "fused"
     traffic = None
-    prof = os.path.join(ROOT, "profiles", f"decode_{name}_traffic.txt")
+    prof = os.path.join(ROOT, "profiles", f"{engine}_{name}_traffic.txt")
     if os.path.exists(prof):
         with open(prof) as f:
             tj = dict(line.split(": ", 1) for line in f.read().splitlines() if ": " in line)
-        if tj.get("kernel_source_hash") == kernel_hash():  # null once the kernel changed
+        if tj.get("kernel_source_hash") == kernel_hash(engine):  # null once the kernel changed
             traffic = float(tj["dram_bytes_per_launch"])
+    tname = W.DTYPE_NAMES[x.dtype].upper()
+    kernel = f"mma_attend_kernel<{tname}>" if tensor_core else f"decode_kernel<128,{x.Hq // x.Hkv},{tname}>"
     h2d = x.q.nbytes + x.block_table.nbytes + x.seq_lens.nbytes
     d2h = x.B * x.Hq * x.d * 4 + x.B * x.Hq * 4
     line = {
@@ -297,23 +314,24 @@ def run_ours(args, x, name, rank, world):
                 "d2h_bytes_per_step": d2h, "ms_per_step": t_e2e * 1e3,
                 "entry": "kv_decode_hostio (pinned host q/table/lens in, out/lse out)"},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
-                     "frac": achieved / peak, "traffic": traffic,
-                     "kernel": "decode_kernel<128,4,F16>" if x.dtype == W.F16 else "decode_kernel<128,4,BF16>",
-                     "units": f"{int(x.seq_lens.sum())} K/V tokens x 4096 B + q + table entries per launch",
+                     "frac": achieved / peak, "traffic": traffic, "kernel": kernel,
+                     "units": f"{int(x.seq_lens.sum())} K/V tokens x {2 * x.Hkv * x.d * 2} B + q "
+                              "+ table entries per launch",
                      "kernel_ms": t_kern * 1e3, "peak_source": f"MEASURED_PEAKS.json hbm_gbs ({peak_kind})"},
-        "gpu_launches": launches_per_step(x.B) * n,
-        "gpu_launches_note": "per step: one decode kernel (workqueue slice, split-KV decode and "
-                             "LSE merge fused); a page-offset pass is added above 1024 sequences",
+        "gpu_launches": launches_per_step(x.B, tensor_core) * n,
+        "gpu_launches_note": ("per step: the tensor-core attention kernel and the split merge "
+                              "kernel" if tensor_core else
+                              "per step: one decode kernel (workqueue slice, split-KV decode and "
+                              "LSE merge fused)") + "; a page-offset pass is added above 1024 sequences",
         "clocks": clocks,
     }
-    # the calibrated split-size choice for this workload (own variants only)
-    cands = [0, 8, 16, 32, 64, 128]
-    ws_t = kv.alloc_workspace(max(
-        kv.kv_decode_workspace_size(x.B, x.Hq, x.Hkv, x.d, x.max_pages, 16, 8),
-        kv.kv_decode_workspace_size(x.B, x.Hq, x.Hkv, x.d, x.max_pages, 16, 0)), device=dev)
-    best, us = kv.kv_decode_tune(q, k, v, table, lens, x.scale, out, lse, ws_t, cands, reps=5)
+    line["config"]["engine"] = ("tensor-core engine" if tensor_core else
+                                f"fused decode kernel, pages_per_split={pps} (0 = automatic)")
     line["policy"] = {"candidates_pages_per_split": cands, "median_us": us, "best": best,
-                      "note": "0 = automatic split rule; L2 not flushed between these calls"}
+                      "chosen": pps,
+                      "note": f"0 = automatic split rule, {kv.KV_DECODE_TENSOR_CORE} = tensor-core "
+                              "engine; calibrated once before timing, L2 not flushed between "
+                              "these calls"}
     if not args.no_budget:
         line["multi_token"] = measure_multi(x, dev, peak)
         line["budget_step"] = measure_budget(dev, peak, peak_kind, args.budget_steps,
@@ -342,8 +360,8 @@ def whole_job_gbs(bytes_per_replica, t_step_max, world):
     return world * bytes_per_replica / t_step_max / 1e9
 
 
-def launches_per_step(B):
-    return 1 if B <= 1024 else 2
+def launches_per_step(B, tensor_core=False):
+    return (2 if tensor_core else 1) + (0 if B <= 1024 else 1)
 
 
 def measure_budget(dev, peak, peak_kind, steps, warmup):
@@ -466,18 +484,18 @@ def measure_multi(x, dev, peak, T=4, steps=10):
         raise SystemExit("device error in kv_attend_multi")
     t = statistics.median(ms) / 1e3
     algo = x.kv_bytes() + x.B * T * x.Hq * x.d * 2 + 4 * sum(-(-int(L) // 16) for L in x.seq_lens)
-    streamed = T * x.kv_bytes()
+    streamed = x.kv_bytes()
     return {"T": T, "ms_per_step": t * 1e3, "tokens_per_s": x.B * T / t,
             "algorithmic_gbs": algo / t / 1e9, "algorithmic_frac_of_peak": algo / t / 1e9 / peak,
             "streamed_gbs": streamed / t / 1e9,
-            "note": "each page is streamed once per query token (T times)"}
+            "note": "tensor-core engine: each page is streamed once for all T query tokens"}
 
 
-def kernel_hash():
+def kernel_hash(engine="fused"):
     import hashlib
 
     h = hashlib.sha256()
-    for f in ("kv_decode.cu", "kv_common.cuh"):
+    for f in ("kv_mma.cu" if engine == "tensor_core" else "kv_decode.cu", "kv_common.cuh"):
         with open(os.path.join(ROOT, "paged_kv_cache_492_b300", "csrc", f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]
@@ -494,6 +512,9 @@ def main():
     ap.add_argument("--no-budget", action="store_true", help="skip the budgeted-step leg")
     ap.add_argument("--budget-steps", type=int, default=64)
     ap.add_argument("--budget-warmup", type=int, default=8)
+    ap.add_argument("--engine", default="policy", choices=["policy", "fused", "tensor-core"],
+                    help="decode engine: the calibrated choice (default), the fused decode "
+                         "kernel with the automatic split, or the tensor-core engine")
     args = ap.parse_args()
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))

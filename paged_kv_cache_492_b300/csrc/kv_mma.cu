@@ -711,9 +711,6 @@ int mma_attend_launch(const void* q, const void* k_pool, const void* v_pool, int
   int* status = reinterpret_cast<int*>(w);
   int32_t* page_off = reinterpret_cast<int32_t*>(w + L.page_off);
 
-  cudaEvent_t ev_before = nullptr, ev_after = nullptr;
-  take_profile_events(&ev_before, &ev_after);
-  if (ev_before) KV_CUDA_CHECK(cudaEventRecord(ev_before, stream));
   const bool fused_offsets = B <= kFusedMaxB;
   if (!fused_offsets) {
     OffsetsArgs oa{};
@@ -754,6 +751,9 @@ int mma_attend_launch(const void* q, const void* k_pool, const void* v_pool, int
   // one CTA per (chunk, head block); chunks beyond the batch's count exit
   const long long grid = L.max_chunks * nhb;
   if (grid > 0x7fffffffll) return KV_EINVAL;
+  cudaEvent_t ev_before = nullptr, ev_after = nullptr;
+  take_profile_events(&ev_before, &ev_after);
+  if (ev_before) KV_CUDA_CHECK(cudaEventRecord(ev_before, stream));
   const dim3 block(32 * (1 + hb));
   if (dtype == KV_BF16)
     KV_CUDA_CHECK(launch(mma_attend_kernel<BF16>, dim3((unsigned)grid), block, mma_smem(hb), stream,
@@ -761,6 +761,7 @@ int mma_attend_launch(const void* q, const void* k_pool, const void* v_pool, int
   else
     KV_CUDA_CHECK(launch(mma_attend_kernel<F16>, dim3((unsigned)grid), block, mma_smem(hb), stream,
                          true, tmk, tmv, mp));
+  if (ev_after) KV_CUDA_CHECK(cudaEventRecord(ev_after, stream));  // the attention kernel alone
   MmaMergeParams gp{};
   gp.page_off = page_off;
   gp.chunk = mp.chunk_out;
@@ -776,7 +777,6 @@ int mma_attend_launch(const void* q, const void* k_pool, const void* v_pool, int
   gp.rows = mp.rows;
   KV_CUDA_CHECK(launch(mma_merge_kernel, dim3((unsigned)((long long)B * Hkv), (unsigned)mp.rows),
                        dim3(kMergeWarps * 32), 0, stream, true, gp));
-  if (ev_after) KV_CUDA_CHECK(cudaEventRecord(ev_after, stream));
   return KV_OK;
 }
 
