@@ -397,28 +397,41 @@ def measure_budget(dev, peak, peak_kind, steps, warmup):
     dec.fit(q0)
     flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream()
+    eager_steps = 32
+    assert warmup + steps + eager_steps <= c["steps"], "the workload is 128 steps long"
+    toks += [tuple(dev_bits(a) for a in W.step_tokens(c["seed"], t, x.B, x.Hq, x.Hkv, x.d, x.dtype))
+             for t in range(warmup + steps, warmup + steps + eager_steps)]
     for t in range(warmup):
         dec.step(*toks[t], t)
+    dec.capture()  # the steady-state step as two CUDA graphs (budgeting, decode)
     torch.cuda.synchronize()
     setup_s = time.perf_counter() - t0
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
           for _ in range(steps)]
     evk = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
            for _ in range(steps)]
-    for a, b in evk:
-        a.record(stream)
-        b.record(stream)
     lens_after = []
     torch.cuda.synchronize()
     for i in range(steps):
         t = warmup + i
         flush.zero_()
-        kv.kv_profile_next_decode(evk[i][0], evk[i][1])
         ev[i][0].record(stream)
-        dec.step(*toks[t], t)
+        dec.step_graphed(*toks[t], between=evk[i][0].record)
+        evk[i][1].record(stream)
         ev[i][1].record(stream)
         lens_after.append(dec.lens.clone())
     torch.cuda.synchronize()
+    # the same step issued call by call (host-bound) on the next steps
+    eager_ms = []
+    for i in range(eager_steps):
+        t = warmup + steps + i
+        flush.zero_()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        dec.step(*toks[t], t)
+        b.record(stream)
+        torch.cuda.synchronize()
+        eager_ms.append(a.elapsed_time(b))
     st = [kv.kv_get_status(dec.ws), kv.kv_get_status(dec.decode_ws)]
     if any(st):
         raise SystemExit(f"device error in the budgeted step: {st}")
@@ -436,6 +449,10 @@ def measure_budget(dev, peak, peak_kind, steps, warmup):
         "workload": "budgeted_b64_bf16 (Hq=32, Hkv=8, d=128, L~U[2048,16384], budgets U[32,256])",
         "steps_timed": steps, "warmup_steps": warmup,
         "ms_per_step": t_step / steps * 1e3, "decode_ms_per_step": t_dec / steps * 1e3,
+        "issue": "CUDA graphs (budgeting part, decode) replayed per step; inputs copied into "
+                 "static buffers inside the timed region",
+        "eager_ms_per_step": statistics.median(eager_ms),
+        "eager_note": f"median of {eager_steps} further steps issued call by call from Python",
         "step_gbs": tot_b / t_step / 1e9, "decode_gbs": tot_b / t_dec / 1e9,
         "decode_frac_of_peak": tot_b / t_dec / 1e9 / peak, "peak_gbs": peak,
         "peak_source": f"MEASURED_PEAKS.json hbm_gbs ({peak_kind})",

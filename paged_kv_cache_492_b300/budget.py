@@ -116,11 +116,60 @@ class BudgetedDecoder:
 
     def step(self, q, k_new, v_new, t: int):
         """One decode step for token t (q [B, Hq, d], k_new/v_new [B, Hkv, d])."""
-        if t > 0:
+        self._budget_part(q, k_new, v_new, t > 0)
+        self._decode_part(q)
+
+    def _budget_part(self, q, k_new, v_new, update_ema: bool):
+        if update_ema:
             self.update_summaries(q, False)
         self.boundary()
         kv.kv_append(k_new, v_new, self.k_pool, self.v_pool, self.table, self.lens,
                      self.free_list, self.free_top, self.ws, stream=self.stream,
                      refcnt=self.refcnt)
+
+    def _decode_part(self, q):
         kv.kv_decode(q, self.k_pool, self.v_pool, self.table, self.lens, self.scale, self.out,
                      self.lse, self.decode_ws, stream=self.stream)
+
+    # -- the step as CUDA graphs ----------------------------------------
+    def capture(self):
+        """Record the steady-state step (t > 0) as two CUDA graphs -- the
+        budgeting part (EMA, boundary compress-or-grow, append) and the
+        decode -- over static input buffers, so a step costs two graph
+        launches instead of a dozen host calls.  Every kernel reads its
+        state from device memory, so replays follow the batch as it evolves.
+        Capture issues no work; call after at least one eager step (the
+        library sets up its kernels on first use)."""
+        import torch
+
+        B, Hq, Hkv, d = self.B, self.Hq, self.Hkv, self.d
+        dt = self.k_pool.dtype
+        dev = self.k_pool.device
+        self.q_in = torch.zeros((B, Hq, d), dtype=dt, device=dev)
+        self.k_in = torch.zeros((B, Hkv, d), dtype=dt, device=dev)
+        self.v_in = torch.zeros((B, Hkv, d), dtype=dt, device=dev)
+        saved = self.stream
+        side = torch.cuda.Stream(device=dev)
+        self.g_budget, self.g_decode = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
+        try:
+            self.stream = None  # the capturing stream is the current one
+            with torch.cuda.graph(self.g_budget, stream=side):
+                self._budget_part(self.q_in, self.k_in, self.v_in, True)
+            with torch.cuda.graph(self.g_decode, stream=side):
+                self._decode_part(self.q_in)
+        finally:
+            self.stream = saved
+
+    def step_graphed(self, q, k_new, v_new, between=None):
+        """One steady-state step (t > 0) by graph replay on the current
+        stream: copies the token's q/k/v into the static buffers, replays the
+        budgeting graph, calls `between()` if given (e.g. to record an
+        event), then replays the decode graph.  Same kernels, order and
+        results as step()."""
+        self.q_in.copy_(q)
+        self.k_in.copy_(k_new)
+        self.v_in.copy_(v_new)
+        self.g_budget.replay()
+        if between is not None:
+            between()
+        self.g_decode.replay()

@@ -169,6 +169,64 @@ __device__ __forceinline__ int rank_of(const float* key, const uint8_t* is_cand,
   return r;
 }
 
+// The order rank_of counts in: candidates first, then the larger key, then
+// the lower index (equal keys, -0 and +0 included, tie on the index);
+// non-candidates and padding after, by index.  A strict total order when no
+// candidate key is NaN.
+__device__ __forceinline__ bool rank_before(const float* key, const uint8_t* is_cand, int n, int x,
+                                            int y) {
+  const bool cx = x < n && is_cand[x], cy = y < n && is_cand[y];
+  if (cx != cy) return cx;
+  if (cx) {
+    const float kx = key[x], ky = key[y];
+    if (kx > ky) return true;
+    if (kx < ky) return false;
+  }
+  return x < y;
+}
+
+// rank[j] = rank_of(key, is_cand, n, j) for every candidate j, by a
+// block-wide bitonic sort of the indices (idx holds next_pow2(n) entries);
+// with a NaN key among the candidates the order is not total, so the
+// counting definition is applied directly instead.
+__device__ void rank_candidates(const float* key, const uint8_t* is_cand, int n, uint16_t* idx,
+                                uint16_t* rank) {
+  int bad = 0;
+  for (int j = threadIdx.x; j < n; j += blockDim.x) bad |= is_cand[j] && isnan(key[j]);
+  if (__syncthreads_or(bad)) {
+    for (int j = threadIdx.x; j < n; j += blockDim.x)
+      if (is_cand[j]) rank[j] = (uint16_t)rank_of(key, is_cand, n, j);
+    __syncthreads();
+    return;
+  }
+  int P2 = 1;
+  while (P2 < n) P2 <<= 1;
+  for (int i = threadIdx.x; i < P2; i += blockDim.x) idx[i] = (uint16_t)i;
+  __syncthreads();
+  for (int k = 2; k <= P2; k <<= 1) {
+    for (int j = k >> 1; j > 0; j >>= 1) {
+      for (int i = threadIdx.x; i < P2; i += blockDim.x) {
+        const int l = i ^ j;
+        if (l > i) {
+          const int x = idx[i], y = idx[l];
+          const bool asc = (i & k) == 0;
+          if (asc ? rank_before(key, is_cand, n, y, x) : rank_before(key, is_cand, n, x, y)) {
+            idx[i] = (uint16_t)y;
+            idx[l] = (uint16_t)x;
+          }
+        }
+      }
+      __syncthreads();
+    }
+  }
+  // candidates come first, in rank order
+  for (int p = threadIdx.x; p < P2; p += blockDim.x) {
+    const int j = idx[p];
+    if (j < n && is_cand[j]) rank[j] = (uint16_t)p;
+  }
+  __syncthreads();
+}
+
 struct SelectArgs {
   const float* scores;
   const int32_t* seq_lens;
@@ -204,7 +262,12 @@ __global__ void __launch_bounds__(kSelThreads) select_rank_kernel(const SelectAr
   float* sf = sel_sm;
   float* ss = sf + n;
   float* rr = ss + n;
-  uint8_t* cand = reinterpret_cast<uint8_t*>(rr + n);
+  uint16_t* idx = reinterpret_cast<uint16_t*>(rr + n);  // [next_pow2(n)]
+  int P2 = 1;
+  while (P2 < n) P2 <<= 1;
+  uint16_t* rank = idx + P2;                               // [n]
+  uint8_t* in_f = reinterpret_cast<uint8_t*>(rank + n);    // [n]
+  uint8_t* cand = in_f + n;                                // [n]
   int my_forced = 0;
   for (int j = threadIdx.x; j < n; j += blockDim.x) {
     const float2 s = reinterpret_cast<const float2*>(a.scores + (size_t)b * a.max_pages * 2)[j];
@@ -229,12 +292,15 @@ __global__ void __launch_bounds__(kSelThreads) select_rank_kernel(const SelectAr
     } else {
       int w = (int)ceilf(__fmul_rn(a.ws_frac, (float)nc));
       w = max(1, min(w, nc));
+      rank_candidates(sf, cand, n, idx, rank);
+      for (int j = threadIdx.x; j < n; j += blockDim.x) in_f[j] = cand[j] && rank[j] < w;
+      __syncthreads();
+      rank_candidates(ss, cand, n, idx, rank);
       int my_d = 0;
       for (int j = threadIdx.x; j < n; j += blockDim.x) {
         if (!cand[j]) continue;
-        const bool in_f = rank_of(sf, cand, n, j) < w;
-        const bool in_s = rank_of(ss, cand, n, j) < w;
-        my_d += in_f && !in_s;
+        const bool in_s = rank[j] < w;
+        my_d += in_f[j] && !in_s;
       }
       const int D = block_sum_int(my_d, red);
       wants = (float)D > __fmul_rn(a.delta, (float)w);
@@ -242,9 +308,10 @@ __global__ void __launch_bounds__(kSelThreads) select_rank_kernel(const SelectAr
     }
   }
   if (k < 0) k = 0;
+  rank_candidates(rr, cand, n, idx, rank);
   for (int j = threadIdx.x; j < a.max_pages; j += blockDim.x) {
     uint8_t kp = 0;
-    if (j < n) kp = cand[j] ? (rank_of(rr, cand, n, j) < k) : 1;
+    if (j < n) kp = cand[j] ? (rank[j] < k) : 1;
     keep[j] = kp;
   }
   if (threadIdx.x == 0) a.wants[b] = wants;
@@ -325,6 +392,11 @@ __device__ __forceinline__ bool kept_token(const CompactArgs& a, int b, long lon
 __device__ __forceinline__ void page_keep_info(const CompactArgs& a, int b, int j, int L, int* c,
                                                bool* prefix) {
   const int lo = j * a.ps, hi = min(L, lo + a.ps);
+  if (!a.token_granular) {  // one keep bit for the whole page: all or none, a prefix either way
+    *c = a.keep[(size_t)b * a.max_pages + j] != 0 ? hi - lo : 0;
+    *prefix = true;
+    return;
+  }
   int cnt = 0;
   bool pre = true, gap = false;
   for (int t = lo; t < hi; ++t) {
@@ -340,93 +412,115 @@ __device__ __forceinline__ void page_keep_info(const CompactArgs& a, int b, int 
   *prefix = pre;
 }
 
-// Plan: one warp per sequence computes kept tokens, fresh and freed page
-// counts; one block scans them, checks the free list, copies the popped ids.
-__global__ void __launch_bounds__(1024) compact_plan_kernel(const CompactArgs a) {
+// Plan, in three steps (four with shared pages):
+//  count  -- one block per sequence: kept tokens K, pages reused in place,
+//            fresh and freed page counts (block-wide scan over its pages);
+//  free   -- shared pages only: which freed reference returns each page to
+//            the free list (the last one in (b, j) order, when the call frees
+//            every reference), and the reference counts after the call;
+//  scan   -- one block: exclusive scans of the counts over b, the free-list
+//            check, the popped page ids.
+constexpr int kCountThreads = 256;
+
+__global__ void __launch_bounds__(kCountThreads) compact_count_kernel(const CompactArgs a) {
+  __shared__ int sm[kCountThreads / 32];
+  __shared__ int s_carry;
+  const int b = blockIdx.x;
+  const int L = a.seq_lens[b];
+  const int np = (int)ceil_div_ll(L, a.ps);
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  int mine = 0;
+  for (int j = threadIdx.x; j < np; j += blockDim.x) {
+    int c = 0;
+    bool pre = true;
+    page_keep_info(a, b, j, L, &c, &pre);
+    mine += c;
+  }
+  const int K = block_sum_int(mine, sm);
+  if (threadIdx.x == 0) s_carry = 0;
+  __syncthreads();
+  int reused_mine = 0;
+  for (int base = 0; base < np; base += blockDim.x) {
+    const int j = base + threadIdx.x;
+    int c = 0;
+    bool pre = true;
+    if (j < np) page_keep_info(a, b, j, L, &c, &pre);
+    int x = c;
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(FULL, x, o);
+      if (lane >= o) x += y;
+    }
+    if (lane == 31) sm[warp] = x;
+    __syncthreads();
+    int before = 0;
+    for (int i = 0; i < warp; ++i) before += sm[i];
+    const int carry = s_carry;
+    const int kb = carry + before + x - c;  // kept tokens before page j
+    const bool reuse = j < np && c > 0 && pre && (kb % a.ps == 0) && (c == a.ps || kb + c == K);
+    reused_mine += reuse ? 1 : 0;
+    if (a.refcnt && j < np) {
+      a.freed_flag[(size_t)b * a.max_pages + j] = reuse ? 0 : 1;
+      if (!reuse) {
+        const int pg = a.table[(size_t)b * a.max_pages + j];
+        if (pg >= 0 && pg < a.num_pages) {
+          atomicAdd(&a.page_cnt[pg], 1);
+          atomicMax(&a.page_key[pg], b * a.max_pages + j);
+        } else {
+          set_status(a.status, KV_EBADPAGE);
+        }
+      }
+    }
+    __syncthreads();
+    if (threadIdx.x == blockDim.x - 1) s_carry = carry + before + x;
+    __syncthreads();
+  }
+  const int reused = block_sum_int(reused_mine, sm);
+  if (threadIdx.x == 0) {
+    const int n_new = (int)ceil_div_ll(K, a.ps);
+    a.new_len[b] = K;
+    a.pop_base[b] = n_new - reused;  // fresh pages (scanned below)
+    a.push_base[b] = np - reused;    // freed pages (scanned below)
+  }
+}
+
+// Shared pages: per-call reference tallies start empty.
+__global__ void compact_clear_kernel(const CompactArgs a) {
+  for (long long pg = (long long)blockIdx.x * blockDim.x + threadIdx.x; pg < a.num_pages;
+       pg += (long long)gridDim.x * blockDim.x) {
+    a.page_cnt[pg] = 0;
+    a.page_key[pg] = -1;
+  }
+}
+
+// Shared pages: a freed page goes back on the free list with the reference
+// that takes its count to zero -- the last one in (b, j) order, if the call
+// frees all of them.  That reference also lowers the count by the call's
+// total.  One block per sequence.
+__global__ void __launch_bounds__(kCountThreads) compact_free_kernel(const CompactArgs a) {
+  __shared__ int sm[kCountThreads / 32];
+  const int b = blockIdx.x;
+  const int np = (int)ceil_div_ll(a.seq_lens[b], a.ps);
+  int pushed = 0;
+  for (int j = threadIdx.x; j < np; j += blockDim.x) {
+    if (!a.freed_flag[(size_t)b * a.max_pages + j]) continue;
+    const int pg = a.table[(size_t)b * a.max_pages + j];
+    if (pg >= 0 && pg < a.num_pages && a.page_key[pg] == b * a.max_pages + j) {
+      const bool push = a.page_cnt[pg] == a.refcnt[pg];
+      a.refcnt[pg] -= a.page_cnt[pg];
+      if (push) {
+        a.freed_flag[(size_t)b * a.max_pages + j] = 2;
+        ++pushed;
+      }
+    }
+  }
+  const int total = block_sum_int(pushed, sm);
+  if (threadIdx.x == 0) a.push_base[b] = total;
+}
+
+__global__ void __launch_bounds__(1024) compact_scan_kernel(const CompactArgs a) {
   __shared__ long long sm[32];
   __shared__ int s_info[4];
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
-  if (a.refcnt) {
-    for (int pg = threadIdx.x; pg < a.num_pages; pg += blockDim.x) {
-      a.page_cnt[pg] = 0;
-      a.page_key[pg] = -1;
-    }
-    __syncthreads();
-  }
-  // per-sequence counts into the workspace (new_len, pop_base <- fresh, push_base <- freed)
-  for (int b = warp; b < a.B; b += nw) {
-    const int L = a.seq_lens[b];
-    const int np = (int)ceil_div_ll(L, a.ps);
-    int kept_before = 0, reused = 0;
-    for (int j0 = 0; j0 < np; j0 += 32) {
-      const int j = j0 + lane;
-      int c = 0;
-      bool pre = true;
-      if (j < np) page_keep_info(a, b, j, L, &c, &pre);
-      for (int o = 16; o; o >>= 1) c += __shfl_xor_sync(FULL, c, o);
-      kept_before += c;
-    }
-    const int K = kept_before;
-    kept_before = 0;
-    for (int j0 = 0; j0 < np; j0 += 32) {
-      const int j = j0 + lane;
-      int c = 0;
-      bool pre = true;
-      if (j < np) page_keep_info(a, b, j, L, &c, &pre);
-      int x = c;
-      for (int o = 1; o < 32; o <<= 1) {
-        const int y = __shfl_up_sync(FULL, x, o);
-        if (lane >= o) x += y;
-      }
-      const int kb = kept_before + x - c;
-      const bool reuse = j < np && c > 0 && pre && (kb % a.ps == 0) && (c == a.ps || kb + c == K);
-      reused += __popc(__ballot_sync(FULL, reuse));
-      kept_before += __shfl_sync(FULL, x, 31);
-      if (a.refcnt && j < np) {
-        a.freed_flag[(size_t)b * a.max_pages + j] = reuse ? 0 : 1;
-        if (!reuse) {
-          const int pg = a.table[(size_t)b * a.max_pages + j];
-          if (pg >= 0 && pg < a.num_pages) {
-            atomicAdd(&a.page_cnt[pg], 1);
-            atomicMax(&a.page_key[pg], b * a.max_pages + j);
-          } else {
-            set_status(a.status, KV_EBADPAGE);
-          }
-        }
-      }
-    }
-    if (lane == 0) {
-      const int n_new = (int)ceil_div_ll(K, a.ps);
-      a.new_len[b] = K;
-      a.pop_base[b] = n_new - reused;  // fresh pages (scanned below)
-      a.push_base[b] = np - reused;    // freed pages (scanned below)
-    }
-  }
-  __syncthreads();
-  if (a.refcnt) {
-    // A freed page goes back on the free list with the reference that takes
-    // its count to zero: the last one in (b, j) order, if the call frees all
-    // of them.  That reference also lowers the count by the call's total.
-    for (int b = warp; b < a.B; b += nw) {
-      const int np = (int)ceil_div_ll(a.seq_lens[b], a.ps);
-      int pushed = 0;
-      for (int j0 = 0; j0 < np; j0 += 32) {
-        const int j = j0 + lane;
-        bool push = false;
-        if (j < np && a.freed_flag[(size_t)b * a.max_pages + j]) {
-          const int pg = a.table[(size_t)b * a.max_pages + j];
-          if (pg >= 0 && pg < a.num_pages && a.page_key[pg] == b * a.max_pages + j) {
-            push = a.page_cnt[pg] == a.refcnt[pg];
-            a.refcnt[pg] -= a.page_cnt[pg];
-            if (push) a.freed_flag[(size_t)b * a.max_pages + j] = 2;
-          }
-        }
-        pushed += __popc(__ballot_sync(FULL, push));
-      }
-      if (lane == 0) a.push_base[b] = pushed;
-    }
-    __syncthreads();
-  }
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   // exclusive scans over b (single block, sequential chunks)
   if (threadIdx.x == 0) {
     s_info[0] = 0;
@@ -918,6 +1012,14 @@ size_t kv_select_workspace_size(int B, int max_pages) {
   return off;
 }
 
+// Shared memory of select_rank_kernel for rows of max_pages pages: three
+// float keys, the sort's index array (next power of two), ranks, two flags.
+static size_t select_smem(int max_pages) {
+  size_t p2 = 1;
+  while (p2 < (size_t)max_pages) p2 <<= 1;
+  return (size_t)max_pages * (3 * sizeof(float) + 2 + 2) + p2 * 2 + 16;
+}
+
 int kv_select_pages(const float* scores, const int32_t* seq_lens, const uint8_t* active,
                     int32_t* budget, int B, int max_pages, int page_size, int n_first, int n_last,
                     float delta, float ws_frac, int mode, const int32_t* free_top,
@@ -949,9 +1051,9 @@ int kv_select_pages(const float* scores, const int32_t* seq_lens, const uint8_t*
   a.status = static_cast<int*>(ws);
   a.wants = reinterpret_cast<int32_t*>(static_cast<uint8_t*>(ws) + kHeaderBytes);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  const size_t smem = (size_t)max_pages * (3 * sizeof(float) + 1) + 16;
+  const size_t smem = select_smem(max_pages);
   KV_CUDA_CHECK(cudaFuncSetAttribute(select_rank_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                     (int)((size_t)kMaxSelectPages * 13 + 16)));
+                                     (int)select_smem(kMaxSelectPages)));
   KV_CUDA_CHECK(launch(select_rank_kernel, dim3(B), dim3(kSelThreads), smem, s, false, a));
   if (mode == KV_SELECT_BOUNDARY)
     KV_CUDA_CHECK(launch(select_grant_kernel, dim3(1), dim3(1024), 0, s, false, a, free_top));
@@ -1028,7 +1130,14 @@ int kv_compact(int32_t* block_table, int max_pages, int32_t* seq_lens, const uin
   a.page_cnt = reinterpret_cast<int32_t*>(w + CL.page_cnt);
   a.page_key = reinterpret_cast<int32_t*>(w + CL.page_key);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  KV_CUDA_CHECK(launch(compact_plan_kernel, dim3(1), dim3(1024), 0, s, false, a));
+  if (refcnt) {
+    const long long blocks = std::min<long long>(1024, ((long long)num_pages + 255) / 256);
+    KV_CUDA_CHECK(launch(compact_clear_kernel, dim3((unsigned)blocks), dim3(256), 0, s, false, a));
+  }
+  KV_CUDA_CHECK(launch(compact_count_kernel, dim3(B), dim3(kCountThreads), 0, s, false, a));
+  if (refcnt)
+    KV_CUDA_CHECK(launch(compact_free_kernel, dim3(B), dim3(kCountThreads), 0, s, false, a));
+  KV_CUDA_CHECK(launch(compact_scan_kernel, dim3(1), dim3(1024), 0, s, false, a));
   if (smem > 48 * 1024)  // one fixed limit for every call (the attribute is per function)
     KV_CUDA_CHECK(cudaFuncSetAttribute(compact_apply_kernel,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, kCompactMaxSmem));

@@ -431,3 +431,41 @@ def test_budgeted_shared_prefix_trajectory():
             assert_decode_close(y, dec.out.cpu().numpy().astype(np.float64),
                                 dec.lse.cpu().numpy().astype(np.float64), ref_out, ref_lse)
     assert (orc.refcnt > 1).any()  # some pages are still shared at the end
+
+
+def test_budgeted_step_graphed_matches_eager():
+    """The steady-state step replayed from CUDA graphs gives the same state
+    and outputs, bit for bit, as the same steps issued call by call."""
+    steps = 24
+    c = W.budgeted_serving(steps=steps + 1)
+    x = c["decode"]
+    cfg = BG.BudgetConfig(a_fast=c["a_fast"], a_slow=c["a_slow"], n_first=c["n_first"],
+                          n_last=c["n_last"], delta=c["delta"])
+    decs = []
+    for _ in range(2):
+        dd = DeviceDecode(x)
+        dec = BG.BudgetedDecoder(dd.k, dd.v, dd.table, dd.lens, i32(x.free_list),
+                                 i32([x.free_top]), i32(c["budget"]), x.Hq, cfg)
+        dec.summarize_pages(i32(np.arange(x.num_pages)))
+        q0, _, _ = W.step_tokens(c["seed"], 0, x.B, x.Hq, x.Hkv, x.d, x.dtype)
+        dec.fit(bits_to_dev(q0, x.dtype))
+        decs.append(dec)
+    eager, graphed = decs
+    toks = [tuple(bits_to_dev(a, x.dtype) for a in W.step_tokens(c["seed"], t, x.B, x.Hq, x.Hkv,
+                                                                   x.d, x.dtype))
+            for t in range(steps + 1)]
+    for dec in decs:
+        dec.step(*toks[0], 0)
+    graphed.capture()
+    for t in range(1, steps + 1):
+        eager.step(*toks[t], t)
+        graphed.step_graphed(*toks[t])
+        torch.cuda.synchronize()
+        for name in ("table", "lens", "free_top", "ema", "keep", "grow", "active", "out", "lse"):
+            a, b = getattr(eager, name), getattr(graphed, name)
+            assert torch.equal(a, b), (t, name)
+        top = int(eager.free_top.item())
+        assert torch.equal(eager.free_list[:top], graphed.free_list[:top]), t
+        assert torch.equal(eager.k_pool, graphed.k_pool) and torch.equal(eager.v_pool, graphed.v_pool), t
+    for dec in decs:
+        assert kv.kv_get_status(dec.ws) == 0 and kv.kv_get_status(dec.decode_ws) == 0
