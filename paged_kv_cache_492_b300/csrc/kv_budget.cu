@@ -185,12 +185,34 @@ __device__ __forceinline__ bool rank_before(const float* key, const uint8_t* is_
   return x < y;
 }
 
-// rank[j] = rank_of(key, is_cand, n, j) for every candidate j, by a
-// block-wide bitonic sort of the indices (idx holds next_pow2(n) entries);
-// with a NaN key among the candidates the order is not total, so the
-// counting definition is applied directly instead.
+// rank[j] = rank_of(key, is_cand, n, j) for every candidate j.  Up to 1024
+// pages: the counting definition itself, spread over the block -- a group
+// of up to 32 lanes per candidate counts a strided share of the keys and
+// the group sums by shuffles (the same indicator sum, so the same result,
+// NaN keys included).  Longer rows: a block-wide bitonic sort of the indices
+// (idx holds next_pow2(n) entries) in rank_before's order; with a NaN key
+// among the candidates that order is not total and the counting definition
+// is applied directly instead.
 __device__ void rank_candidates(const float* key, const uint8_t* is_cand, int n, uint16_t* idx,
                                 uint16_t* rank) {
+  if (n <= 1024) {
+    int tpc = 1;  // lanes per candidate
+    while (tpc < 32 && tpc * 2 * n <= (int)blockDim.x) tpc <<= 1;
+    const int per_pass = blockDim.x / tpc, sub = threadIdx.x & (tpc - 1);
+    for (int j0 = 0; j0 < n; j0 += per_pass) {
+      const int j = j0 + threadIdx.x / tpc;
+      const bool mine = j < n && is_cand[j];
+      int r = 0;
+      if (mine) {
+        const float kj = key[j];
+        for (int i = sub; i < n; i += tpc) r += is_cand[i] && (key[i] > kj || (key[i] == kj && i < j));
+      }
+      for (int o = tpc >> 1; o; o >>= 1) r += __shfl_xor_sync(FULL, r, o);
+      if (mine && sub == 0) rank[j] = (uint16_t)r;
+    }
+    __syncthreads();
+    return;
+  }
   int bad = 0;
   for (int j = threadIdx.x; j < n; j += blockDim.x) bad |= is_cand[j] && isnan(key[j]);
   if (__syncthreads_or(bad)) {

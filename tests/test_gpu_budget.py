@@ -148,6 +148,30 @@ def test_select_bit_exact(trial):
                 assert np.array_equal(r, g), (name, mode, free)
 
 
+@pytest.mark.parametrize("trial", range(3))
+def test_select_bit_exact_long_rows(trial):
+    """Rows above 1024 pages (the sorted ranking) and short ones (the counted
+    one) side by side, with exact ties and signed zeros among the keys."""
+    rng = np.random.default_rng(40 + trial)
+    B, maxp = 6, 2500
+    lens = rng.integers(1000 * 16, maxp * 16, size=B).astype(np.int32)
+    lens[0] = 700 * 16
+    lens[1:3] = (lens[1:3] // 16) * 16
+    sc = rng.standard_normal((B, maxp, 2)).astype(np.float32)
+    if trial >= 1:
+        sc = np.round(sc * 2) / 2
+    if trial == 2:
+        zero = rng.random((B, maxp, 2)) < 0.3
+        sc[zero] = np.where(rng.random(zero.sum()) < 0.5, np.float32(-0.0), np.float32(0.0))
+    act = np.ones(B, dtype=np.uint8)
+    budget = rng.integers(100, 2400, size=B).astype(np.int32)
+    for mode, free in ((O.SELECT_TOPK, 0), (O.SELECT_BOUNDARY, 1)):
+        ref = O.select_pages(sc, lens, act, budget, 16, 2, 2, 0.5, mode, free, ws_frac=0.5)
+        got = _run_select(sc, lens, act, budget, mode, free, delta=0.5, ws_frac=0.5)
+        for r, g, name in zip(ref, got, ("keep", "grow", "budget", "drift")):
+            assert np.array_equal(r, g), (name, mode, free)
+
+
 def _compact_case(seed, token_granular, free_top=None):
     rng = np.random.default_rng(seed)
     B = 5
