@@ -136,7 +136,7 @@ size_t kv_decode_workspace_size(int B, int Hq, int Hkv, int d, int max_pages, in
  * recombined by a log-sum-exp merge done by whichever split finishes last.
  * One kernel launch (two for B > 1024: a page-offset pass first).
  * pages_per_split = KV_DECODE_TENSOR_CORE selects the tensor-core engine
- * instead (d = 128, page_size 16, G <= 16; else KV_EINVAL): the same split
+ * instead (d = 128, page_size 16, G <= 64; else KV_EINVAL): the same split
  * rule with the automatic chunk, one CTA per chunk streaming whole pages by
  * TMA tensor copies, Q K^T and P V on mma.sync (fp32 accumulation), and a
  * merge kernel for the split sequences (kv_attend_multi with T = 1).  Both
@@ -160,7 +160,7 @@ int kv_decode(const void *q, const void *k_pool, const void *v_pool, int num_pag
  * a query with no token to attend to gets out = 0 and lse = -inf.
  * q [B][T][Hq][d] 16-bit, out [B][T][Hq][d] fp32, lse [B][T][Hq] fp32
  * (device).  Other arguments and errors as kv_decode; the workspace is
- * kv_attend_multi_workspace_size bytes (give it its own).  Where T * G <= 16
+ * kv_attend_multi_workspace_size bytes (give it its own).  Where T * G <= 64
  * (d = 128, page_size 16) the tensor-core engine streams each page once for
  * all T tokens (T = 1 is kv_decode's KV_DECODE_TENSOR_CORE engine);
  * otherwise the fused decode kernel runs on B*T causal views of the batch,
@@ -206,8 +206,10 @@ size_t kv_decode_hostio_workspace_size(int B, int Hq, int Hkv, int d, int max_pa
 /* kv_decode with the per-step inputs and outputs in host memory: copies
  * h_q, h_block_table, h_seq_lens (host) into the workspace, runs kv_decode
  * against the device-resident pools, and copies out/lse back into h_out and
- * h_lse (host), all enqueued on `stream` (one cudaMemcpyAsync per buffer).
- * The host buffers must stay valid until the stream reaches that point. */
+ * h_lse (host), all enqueued on `stream`.  Page-locked host buffers (which
+ * the device can address) are read and written in place by one copy kernel
+ * on each side; pageable ones take one cudaMemcpyAsync per buffer.  The
+ * host buffers must stay valid until the stream reaches that point. */
 int kv_decode_hostio(const void *h_q, const void *k_pool, const void *v_pool, int num_pages,
                      const int32_t *h_block_table, int max_pages, const int32_t *h_seq_lens,
                      int B, int page_size, int Hq, int Hkv, int d, int dtype, float scale,

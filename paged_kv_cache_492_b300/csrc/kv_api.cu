@@ -8,6 +8,50 @@
 
 #include "kv_internal.h"
 
+namespace kvb {
+namespace {
+
+// Up to three byte ranges copied by one kernel (each a multiple of 4 bytes,
+// 4-byte aligned; 16-byte words where both ends allow).  Used to move the
+// host-buffer call's inputs and outputs through mapped host memory: one
+// launch instead of one DMA operation per buffer.
+struct CopySegs {
+  const void* src[3];
+  void* dst[3];
+  size_t bytes[3];
+  int n;
+};
+
+__global__ void __launch_bounds__(256) segs_copy_kernel(const CopySegs c) {
+  pdl_wait();  // the sources may come from the previous kernel on the stream
+  pdl_launch_dependents();
+  const size_t tid = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
+  const size_t nth = (size_t)gridDim.x * blockDim.x;
+  for (int k = 0; k < c.n; ++k) {
+    const uintptr_t s = reinterpret_cast<uintptr_t>(c.src[k]), d = reinterpret_cast<uintptr_t>(c.dst[k]);
+    if (((s | d | c.bytes[k]) & 15) == 0) {
+      const uint4* src = reinterpret_cast<const uint4*>(s);
+      uint4* dst = reinterpret_cast<uint4*>(d);
+      for (size_t i = tid; i < c.bytes[k] / 16; i += nth) dst[i] = src[i];
+    } else {
+      const uint32_t* src = reinterpret_cast<const uint32_t*>(s);
+      uint32_t* dst = reinterpret_cast<uint32_t*>(d);
+      for (size_t i = tid; i < c.bytes[k] / 4; i += nth) dst[i] = src[i];
+    }
+  }
+}
+
+cudaError_t launch_segs_copy(const CopySegs& c, cudaStream_t s) {
+  size_t total = 0;
+  for (int k = 0; k < c.n; ++k) total += c.bytes[k];
+  const size_t words = (total + 15) / 16;
+  const unsigned blocks = (unsigned)std::min<size_t>(148 * 4, std::max<size_t>(1, (words + 255) / 256));
+  return launch(segs_copy_kernel, dim3(blocks), dim3(256), 0, s, true, c);
+}
+
+}  // namespace
+}  // namespace kvb
+
 using namespace kvb;
 
 namespace kvb {
@@ -123,7 +167,7 @@ size_t kv_decode_workspace_size(int B, int Hq, int Hkv, int d, int max_pages, in
   if (pages_per_split == KV_DECODE_TENSOR_CORE) {
     if (!tensor_core_ok(page_size, Hq, Hkv, d)) return 0;
     const size_t region = tensor_core_region(B, Hq, Hkv, d, max_pages, page_size);
-    return region ? mma_attend_workspace_size(B, Hkv, max_pages, 0, region) : 0;
+    return region ? mma_attend_workspace_size(B, Hkv, Hq / Hkv, max_pages, 0, region) : 0;
   }
   if (pages_per_split < 0) return 0;
   const int nw = decode_workers_both(Hq, Hkv, d, page_size);
@@ -141,6 +185,19 @@ int kv_decode(const void* q, const void* k_pool, const void* v_pool, int num_pag
 }
 
 namespace {
+
+// Device address of a host buffer the GPU can reach directly (page-locked
+// and mapped, as every pinned allocation is under unified addressing), or
+// null for pageable memory.
+void* mapped_host(const void* p) {
+  cudaPointerAttributes at;
+  if (cudaPointerGetAttributes(&at, p) != cudaSuccess) {
+    cudaGetLastError();  // pageable memory on older runtimes reports an error
+    return nullptr;
+  }
+  return at.type == cudaMemoryTypeHost ? at.devicePointer : nullptr;
+}
+
 struct HostIoLayout {
   size_t q, table, seq_lens, out, lse, total;
 };
@@ -184,17 +241,45 @@ int kv_decode_hostio(const void* h_q, const void* k_pool, const void* v_pool, in
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   uint8_t* w = static_cast<uint8_t*>(ws);
   const size_t qb = (size_t)B * Hq * d * 2, tb = (size_t)B * max_pages * 4, sb = (size_t)B * 4;
-  KV_CUDA_CHECK(cudaMemcpyAsync(w + L.q, h_q, qb, cudaMemcpyHostToDevice, s));
-  KV_CUDA_CHECK(cudaMemcpyAsync(w + L.table, h_block_table, tb, cudaMemcpyHostToDevice, s));
-  KV_CUDA_CHECK(cudaMemcpyAsync(w + L.seq_lens, h_seq_lens, sb, cudaMemcpyHostToDevice, s));
+  const size_t ob = (size_t)B * Hq * d * 4, lb = (size_t)B * Hq * 4;
+  // pinned host buffers are read and written in place by copy kernels;
+  // pageable ones take one cudaMemcpyAsync each
+  void* m_q = mapped_host(h_q);
+  void* m_t = mapped_host(h_block_table);
+  void* m_l = mapped_host(h_seq_lens);
+  void* m_o = mapped_host(h_out);
+  void* m_s = mapped_host(h_lse);
+  const bool in_mapped = m_q && m_t && m_l && !((uintptr_t)m_q & 3) && !((uintptr_t)m_t & 3) &&
+                         !((uintptr_t)m_l & 3);
+  const bool out_mapped = m_o && m_s && !((uintptr_t)m_o & 3) && !((uintptr_t)m_s & 3);
+  if (in_mapped) {
+    CopySegs c{};
+    c.src[0] = m_q; c.dst[0] = w + L.q; c.bytes[0] = qb;
+    c.src[1] = m_t; c.dst[1] = w + L.table; c.bytes[1] = tb;
+    c.src[2] = m_l; c.dst[2] = w + L.seq_lens; c.bytes[2] = sb;
+    c.n = 3;
+    KV_CUDA_CHECK(launch_segs_copy(c, s));
+  } else {
+    KV_CUDA_CHECK(cudaMemcpyAsync(w + L.q, h_q, qb, cudaMemcpyHostToDevice, s));
+    KV_CUDA_CHECK(cudaMemcpyAsync(w + L.table, h_block_table, tb, cudaMemcpyHostToDevice, s));
+    KV_CUDA_CHECK(cudaMemcpyAsync(w + L.seq_lens, h_seq_lens, sb, cudaMemcpyHostToDevice, s));
+  }
   int rc = engine_launch(w + L.q, k_pool, v_pool, num_pages,
                          reinterpret_cast<const int32_t*>(w + L.table), max_pages,
                          reinterpret_cast<const int32_t*>(w + L.seq_lens), B, page_size, Hq, Hkv, d,
                          dtype, scale, pages_per_split, reinterpret_cast<float*>(w + L.out),
                          reinterpret_cast<float*>(w + L.lse), ws, base, s);
   if (rc) return rc;
-  KV_CUDA_CHECK(cudaMemcpyAsync(h_out, w + L.out, (size_t)B * Hq * d * 4, cudaMemcpyDeviceToHost, s));
-  KV_CUDA_CHECK(cudaMemcpyAsync(h_lse, w + L.lse, (size_t)B * Hq * 4, cudaMemcpyDeviceToHost, s));
+  if (out_mapped) {
+    CopySegs c{};
+    c.src[0] = w + L.out; c.dst[0] = m_o; c.bytes[0] = ob;
+    c.src[1] = w + L.lse; c.dst[1] = m_s; c.bytes[1] = lb;
+    c.n = 2;
+    KV_CUDA_CHECK(launch_segs_copy(c, s));
+  } else {
+    KV_CUDA_CHECK(cudaMemcpyAsync(h_out, w + L.out, ob, cudaMemcpyDeviceToHost, s));
+    KV_CUDA_CHECK(cudaMemcpyAsync(h_lse, w + L.lse, lb, cudaMemcpyDeviceToHost, s));
+  }
   return KV_OK;
 }
 

@@ -99,13 +99,14 @@ int decode_launch(const void* q, const void* k_pool, const void* v_pool, int num
                   cudaStream_t stream, int seqs_per_row = 1);
 int decode_num_workers(int Hq, int Hkv, int d, int page_size, int dtype);
 
-// Tensor-core attention of T * G <= 16 query rows per KV head (d = 128,
+// Tensor-core attention of T * G <= 64 query rows per KV head (d = 128,
 // page_size 16): one TMA-fed CTA per chunk of the batch's pages and a merge
 // kernel.  Its scratch starts `region` bytes into the workspace (the status
 // word stays at the workspace's start), so it can share a workspace with
 // the decode kernel's merge tickets.
 bool mma_attend_supported(int Hq, int Hkv, int d, int Tq);
-size_t mma_attend_workspace_size(int B, int Hkv, int max_pages, int pages_per_split, size_t region);
+size_t mma_attend_workspace_size(int B, int Hkv, int rows, int max_pages, int pages_per_split,
+                                 size_t region);
 int mma_attend_launch(const void* q, const void* k_pool, const void* v_pool, int num_pages,
                       const int32_t* block_table, int max_pages, const int32_t* seq_lens, int B,
                       int Tq, int Hq, int Hkv, int dtype, float scale, int pages_per_split,

@@ -43,11 +43,13 @@ namespace kvb {
 namespace {
 
 constexpr int kMmaD = 128;              // head dimension of this path
-constexpr int kMmaRows = 16;            // query rows per KV head (one m16 tile)
-constexpr int kMmaStages = 3;           // pages in flight per CTA
+constexpr int kMmaRows = 16;            // query rows of one m16 tile (one consumer warp)
+constexpr int kMaxRowBlocks = 4;        // up to 64 query rows per KV head
+constexpr int kMaxStages = 12;          // pages in flight per CTA (3 at 8 heads .. 12)
+constexpr int kRingBytes = 192 * 1024;  // shared memory for the ring
 constexpr int kMaxHeadBlock = 8;        // KV heads (consumer warps) per CTA
 constexpr int kHalfTile = 16 * 64 * 2;  // 16 tokens x 64 channels, bytes
-constexpr int kBarBytes = 128;          // full[S], empty[S]
+constexpr int kBarBytes = 256;          // full[kMaxStages], empty[kMaxStages]
 constexpr unsigned FULLM = 0xffffffffu;
 
 struct MmaParams {
@@ -62,7 +64,7 @@ struct MmaParams {
   float* part_o;              // [slot][Hkv][16][128]
   float* part_lse;            // [slot][Hkv][16]
   int* status;
-  int B, num_pages, max_pages, Hq, Hkv, G, Tq, rows, hb, nhb, chunk_req;
+  int B, num_pages, max_pages, Hq, Hkv, G, Tq, rows, rows_pad, rb, hb, nhb, chunk_req, stages;
   long long n_chunks;         // chunks of the automatic split (CTAs per head block)
   float scale_log2;
 };
@@ -151,9 +153,9 @@ __global__ void __launch_bounds__(32 * (1 + kMaxHeadBlock), 1)
   __shared__ int32_t s_off[kFusedMaxB + 1];
   __shared__ long long s_scan[32];
   if (threadIdx.x == 0) {
-    for (int s = 0; s < kMmaStages; ++s) {
+    for (int s = 0; s < p.stages; ++s) {
       mbar_init(smem_u32(&bars[s]), 1);
-      mbar_init(smem_u32(&bars[kMmaStages + s]), p.hb);
+      mbar_init(smem_u32(&bars[kMaxStages + s]), p.hb * p.rb);
     }
     fence_mbar_init();
   }
@@ -223,7 +225,7 @@ __global__ void __launch_bounds__(32 * (1 + kMaxHeadBlock), 1)
           const int pid = __shfl_sync(FULLM, id, i);
           if (lane == 0) {
             bool ok = true;
-            if (round > 0) ok = mbar_wait(smem_u32(&bars[kMmaStages + slot]), (round - 1) & 1);
+            if (round > 0) ok = mbar_wait(smem_u32(&bars[kMaxStages + slot]), (round - 1) & 1);
             if (!ok) {
               set_status(p.status, KV_ETIMEOUT);
               aborted = true;
@@ -240,7 +242,7 @@ __global__ void __launch_bounds__(32 * (1 + kMaxHeadBlock), 1)
           }
           aborted = __shfl_sync(FULLM, aborted, 0);
           if (aborted) break;
-          if (++slot == kMmaStages) {
+          if (++slot == p.stages) {
             slot = 0;
             ++round;
           }
@@ -250,7 +252,7 @@ __global__ void __launch_bounds__(32 * (1 + kMaxHeadBlock), 1)
     if (aborted && lane == 0) {
       // let the copies already issued land before the CTA's shared memory
       // goes away: the last phase issued on each slot (bounded waits)
-      for (int s = 0; s < kMmaStages; ++s) {
+      for (int s = 0; s < p.stages; ++s) {
         const int issued = s < slot ? round + 1 : round;
         if (issued > 0) mbar_wait(smem_u32(&bars[s]), (issued - 1) & 1);
       }
@@ -259,9 +261,10 @@ __global__ void __launch_bounds__(32 * (1 + kMaxHeadBlock), 1)
   }
 
   // -------------------------------------------------------------- consumers
-  if (warp > p.hb) return;
-  const int hw = warp - 1, h = hblk * p.hb + hw;
-  const int qr0 = lane >> 2, qr1 = qr0 + 8, qc = (lane & 3) * 2;
+  // consumer warp c: head hw of the block, rows [16 rbi, 16 rbi + 16)
+  const int cw = warp - 1, hw = cw / p.rb, rbi = cw - (cw / p.rb) * p.rb;
+  const int h = hblk * p.hb + hw;
+  const int qr0 = rbi * kMmaRows + (lane >> 2), qr1 = qr0 + 8, qc = (lane & 3) * 2;
   const int mi = lane >> 3, mr = lane & 7;  // ldmatrix: matrix mi, row mr
   int slot = 0, round = 0;
   for (int b = b_first; b < p.B && O[b] < c1; ++b) {
@@ -387,8 +390,8 @@ __global__ void __launch_bounds__(32 * (1 + kMaxHeadBlock), 1)
       }
       // this warp is done with the stage
       __syncwarp();
-      if (lane == 0) mbar_arrive(smem_u32(&bars[kMmaStages + slot]));
-      if (++slot == kMmaStages) {
+      if (lane == 0) mbar_arrive(smem_u32(&bars[kMaxStages + slot]));
+      if (++slot == p.stages) {
         slot = 0;
         ++round;
       }
@@ -411,8 +414,8 @@ __global__ void __launch_bounds__(32 * (1 + kMaxHeadBlock), 1)
         *l_ptr = p.lse + row;
       } else {
         const size_t part = (size_t)slot_id * p.Hkv + h;
-        *o_ptr = p.part_o + (part * kMmaRows + r) * kMmaD;
-        *l_ptr = p.part_lse + part * kMmaRows + r;
+        *o_ptr = p.part_o + (part * p.rows_pad + r) * kMmaD;
+        *l_ptr = p.part_lse + part * p.rows_pad + r;
       }
     };
     if (qr0 < p.rows) {
@@ -451,7 +454,7 @@ struct MmaMergeParams {
   const float* part_lse;
   float* out;
   float* lse;
-  int B, Hq, Hkv, G, Tq, rows;
+  int B, Hq, Hkv, G, Tq, rows, rows_pad;
 };
 
 constexpr int kMergeWarps = 4;
@@ -475,7 +478,7 @@ __global__ void __launch_bounds__(kMergeWarps * 32) mma_merge_kernel(const MmaMe
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, c4 = lane * 4;
   const long long cf = Ob / chunk;
   auto part = [&](long long s) {
-    return ((size_t)(s == 0 ? 2 * cf + 1 : 2 * (cf + s)) * p.Hkv + h) * kMmaRows + r;
+    return ((size_t)(s == 0 ? 2 * cf + 1 : 2 * (cf + s)) * p.Hkv + h) * p.rows_pad + r;
   };
   auto load_o = [&](long long s) {
     return __ldcg(reinterpret_cast<const float4*>(p.part_o + part(s) * kMmaD + c4));
@@ -605,21 +608,33 @@ int encode_pool_map(CUtensorMap* m, const void* pool, int num_pages, int Hkv, in
   return KV_OK;
 }
 
-// Heads per CTA: the largest divisor of Hkv up to 8.
-int head_block(int Hkv) {
-  for (int hb = kMaxHeadBlock; hb > 1; --hb)
+// Row blocks of 16 query rows per KV head.
+int row_blocks(int rows) { return (rows + kMmaRows - 1) / kMmaRows; }
+// Heads per CTA: the largest divisor of Hkv with at most 8 consumer warps
+// (one per head and row block).
+int head_block(int Hkv, int rb) {
+  for (int hb = kMaxHeadBlock / rb; hb > 1; --hb)
     if (Hkv % hb == 0) return hb;
   return 1;
 }
-size_t mma_smem(int hb) { return kBarBytes + 1024 + (size_t)kMmaStages * 4 * hb * kHalfTile; }
+// Ring depth: about kRingBytes in flight whatever the head block (a stage is
+// one page of hb heads, K and V).
+int ring_stages(int hb) {
+  const int s = kRingBytes / (4 * hb * kHalfTile);
+  return s < 3 ? 3 : (s > kMaxStages ? kMaxStages : s);
+}
+size_t mma_smem(int hb) {
+  return kBarBytes + 1024 + (size_t)ring_stages(hb) * 4 * hb * kHalfTile;
+}
 
 struct MmaLayout {
   size_t page_off, chunk, part_o, part_lse, total;
   long long max_chunks;
 };
 
-MmaLayout mma_layout(int B, int Hkv, int max_pages, int pages_per_split, long long n_chunks,
-                     size_t region) {
+MmaLayout mma_layout(int B, int Hkv, int rows, int max_pages, int pages_per_split,
+                     long long n_chunks, size_t region) {
+  const size_t rows_pad = (size_t)row_blocks(rows) * kMmaRows;
   MmaLayout L{};
   L.max_chunks = pages_per_split > 0 ? ceil_div_ll((long long)B * max_pages, pages_per_split)
                                      : n_chunks;
@@ -633,22 +648,24 @@ MmaLayout mma_layout(int B, int Hkv, int max_pages, int pages_per_split, long lo
   };
   L.page_off = take((size_t)(B + 1) * 4);
   L.chunk = take(4);
-  L.part_o = take((size_t)slots * Hkv * kMmaRows * kMmaD * 4);
-  L.part_lse = take((size_t)slots * Hkv * kMmaRows * 4);
+  L.part_o = take((size_t)slots * Hkv * rows_pad * kMmaD * 4);
+  L.part_lse = take((size_t)slots * Hkv * rows_pad * 4);
   L.total = off;
   return L;
 }
 
 // Chunks of the automatic split: one per CTA that fits on the device at once.
-int mma_chunks(int Hkv, long long* out) {
+int mma_chunks(int Hkv, int rows, long long* out) {
   static std::mutex mu;
-  static int cached[64][kMaxHeadBlock + 1] = {{0}};
+  static int cached[64][kMaxHeadBlock + 1][kMaxRowBlocks + 1] = {};
   int dev = 0;
   KV_CUDA_CHECK(cudaGetDevice(&dev));
   if (dev < 0 || dev >= 64) return KV_EINVAL;
-  const int hb = head_block(Hkv);
+  const int rb = row_blocks(rows);
+  if (rb < 1 || rb > kMaxRowBlocks) return KV_EINVAL;
+  const int hb = head_block(Hkv, rb);
   std::lock_guard<std::mutex> lk(mu);
-  if (!cached[dev][hb]) {
+  if (!cached[dev][hb][rb]) {
     int sms = 0, per = 0;
     KV_CUDA_CHECK(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev));
     for (auto fn : {mma_attend_kernel<F16>, mma_attend_kernel<BF16>}) {
@@ -656,28 +673,31 @@ int mma_chunks(int Hkv, long long* out) {
                                          (int)mma_smem(kMaxHeadBlock)));
       int n = 0;
       KV_CUDA_CHECK(
-          cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, fn, 32 * (1 + hb), mma_smem(hb)));
+          cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, fn, 32 * (1 + hb * rb), mma_smem(hb)));
       per = per == 0 ? n : min(per, n);
     }
     if (per < 1) return cuda_failed(cudaErrorInvalidConfiguration, "tensor-core attend occupancy");
-    cached[dev][hb] = sms * per;
+    cached[dev][hb][rb] = sms * per;
   }
   const int nhb = Hkv / hb;
-  *out = (cached[dev][hb] + nhb - 1) / nhb;
+  *out = (cached[dev][hb][rb] + nhb - 1) / nhb;
   return KV_OK;
 }
 
 }  // namespace
 
 bool mma_attend_supported(int Hq, int Hkv, int d, int Tq) {
-  return d == kMmaD && Hkv > 0 && Hq % Hkv == 0 && Tq >= 1 && (Hq / Hkv) * Tq <= kMmaRows;
+  return d == kMmaD && Hkv > 0 && Hq % Hkv == 0 && Tq >= 1 &&
+         (long long)(Hq / Hkv) * Tq <= (long long)kMmaRows * kMaxRowBlocks;
 }
 
-size_t mma_attend_workspace_size(int B, int Hkv, int max_pages, int pages_per_split,
+size_t mma_attend_workspace_size(int B, int Hkv, int rows, int max_pages, int pages_per_split,
                                  size_t region) {
   long long chunks = 0;
-  if (B < 0 || Hkv < 1 || max_pages < 0 || pages_per_split < 0 || mma_chunks(Hkv, &chunks)) return 0;
-  return mma_layout(B, Hkv, max_pages, pages_per_split, chunks, region).total;
+  if (B < 0 || Hkv < 1 || rows < 1 || rows > kMmaRows * kMaxRowBlocks || max_pages < 0 ||
+      pages_per_split < 0 || mma_chunks(Hkv, rows, &chunks))
+    return 0;
+  return mma_layout(B, Hkv, rows, max_pages, pages_per_split, chunks, region).total;
 }
 
 int mma_attend_launch(const void* q, const void* k_pool, const void* v_pool, int num_pages,
@@ -696,12 +716,13 @@ int mma_attend_launch(const void* q, const void* k_pool, const void* v_pool, int
       ((uintptr_t)out & 15) || ((uintptr_t)ws & 255))
     return KV_EINVAL;
   long long chunks = 0;
-  int rc = mma_chunks(Hkv, &chunks);
+  const int rows = (Hq / Hkv) * Tq, rb = row_blocks(rows);
+  int rc = mma_chunks(Hkv, rows, &chunks);
   if (rc) return rc;
-  const MmaLayout L = mma_layout(B, Hkv, max_pages, pages_per_split, chunks, region);
+  const MmaLayout L = mma_layout(B, Hkv, rows, max_pages, pages_per_split, chunks, region);
   if (ws_bytes < L.total) return KV_EWORKSPACE;
   uint8_t* w = static_cast<uint8_t*>(ws);
-  const int hb = head_block(Hkv), nhb = Hkv / hb;
+  const int hb = head_block(Hkv, rb), nhb = Hkv / hb;
   CUtensorMap tmk, tmv;
   rc = encode_pool_map(&tmk, k_pool, num_pages, Hkv, hb, dtype);
   if (rc) return rc;
@@ -742,7 +763,10 @@ int mma_attend_launch(const void* q, const void* k_pool, const void* v_pool, int
   mp.Hkv = Hkv;
   mp.G = Hq / Hkv;
   mp.Tq = Tq;
-  mp.rows = mp.G * Tq;
+  mp.rows = rows;
+  mp.rows_pad = rb * kMmaRows;
+  mp.stages = ring_stages(hb);
+  mp.rb = rb;
   mp.hb = hb;
   mp.nhb = nhb;
   mp.chunk_req = pages_per_split;
@@ -754,7 +778,7 @@ int mma_attend_launch(const void* q, const void* k_pool, const void* v_pool, int
   cudaEvent_t ev_before = nullptr, ev_after = nullptr;
   take_profile_events(&ev_before, &ev_after);
   if (ev_before) KV_CUDA_CHECK(cudaEventRecord(ev_before, stream));
-  const dim3 block(32 * (1 + hb));
+  const dim3 block(32 * (1 + hb * rb));
   if (dtype == KV_BF16)
     KV_CUDA_CHECK(launch(mma_attend_kernel<BF16>, dim3((unsigned)grid), block, mma_smem(hb), stream,
                          true, tmk, tmv, mp));
@@ -775,6 +799,7 @@ int mma_attend_launch(const void* q, const void* k_pool, const void* v_pool, int
   gp.G = mp.G;
   gp.Tq = Tq;
   gp.rows = mp.rows;
+  gp.rows_pad = mp.rows_pad;
   KV_CUDA_CHECK(launch(mma_merge_kernel, dim3((unsigned)((long long)B * Hkv), (unsigned)mp.rows),
                        dim3(kMergeWarps * 32), 0, stream, true, gp));
   return KV_OK;

@@ -4,9 +4,9 @@
 // sequence b are its last T cached tokens (their K/V already appended), and
 // query i attends causally to tokens [0, L_b - T + 1 + i).
 //
-// Two forms.  Where T * G <= 16 rows per KV head fit one tensor-core tile
-// (d = 128, page size 16), the tensor-core kernel (kv_mma.cu) streams each
-// page once for all T tokens.  Otherwise the decode kernel runs unchanged on
+// Two forms.  Where T * G <= 64 rows per KV head (d = 128, page size 16),
+// the tensor-core kernel (kv_mma.cu) streams each page once for all T
+// tokens.  Otherwise the decode kernel runs unchanged on
 // B*T virtual sequences: virtual sequence b*T + i has length
 // max(0, L_b - T + 1 + i), reads block-table row b, query row q[b][i] and
 // output row out[b][i], so each page is streamed once per query token.
@@ -52,7 +52,8 @@ size_t kv_attend_multi_workspace_size(int B, int T, int Hq, int Hkv, int d, int 
                                       int page_size, int pages_per_split) {
   if (B < 0 || T < 1) return 0;
   if (use_mma(page_size, Hq, Hkv, d, T))
-    return mma_attend_workspace_size(B, Hkv, max_pages, pages_per_split, kHeaderBytes);
+    return mma_attend_workspace_size(B, Hkv, (Hq / Hkv) * T, max_pages, pages_per_split,
+                                     kHeaderBytes);
   const size_t base = kv_decode_workspace_size(B * T, Hq, Hkv, d, max_pages, page_size,
                                                pages_per_split);
   if (!base) return 0;

@@ -31,6 +31,8 @@ SMALL = [
     (49, 5, 16, 16, 128, [0, 0, 64, 0, 31], W.F16),            # two blocks of 8, mostly empty
     (50, 8, 32, 8, 128, [4000, 16, 17, 2048, 0, 1, 777, 3000], W.BF16),
     (51, 1, 32, 8, 128, [20000], W.F16),                       # one sequence over every chunk
+    (60, 3, 64, 2, 128, [900, 0, 2500], W.BF16),               # G = 32: two row blocks
+    (61, 2, 128, 2, 128, [3000, 77], W.F16),                   # G = 64: four row blocks
 ]
 
 
@@ -141,6 +143,31 @@ def test_hostio_engine_matches_device_call():
     assert np.array_equal(hls.numpy(), l_dev.astype(np.float32))
 
 
+def test_hostio_pageable_buffers():
+    """Pinned host buffers go through copy kernels on mapped memory, pageable
+    ones through per-buffer copies: both give the device call's result."""
+    x = W.small_decode(62, 3, 32, 8, 128, [900, 0, 2500])
+    o_dev, l_dev, rc = DeviceDecode(x).run(pages_per_split=TC, ws=_ws(x))
+    assert rc == 0
+    dd = DeviceDecode(x)
+    for pinned in (False, True):
+        mk = (lambda t: t.pin_memory()) if pinned else (lambda t: t)
+        hq = mk(torch.from_numpy(x.q.view(np.int16).copy()).view(dd.q.dtype))
+        ht = mk(torch.from_numpy(x.block_table.copy()))
+        hl = mk(torch.from_numpy(x.seq_lens.copy()))
+        ho = mk(torch.full((x.B, x.Hq, x.d), float("nan"), dtype=torch.float32))
+        hls = mk(torch.full((x.B, x.Hq), float("nan"), dtype=torch.float32))
+        ws = kv.alloc_workspace(kv.kv_decode_hostio_workspace_size(x.B, x.Hq, x.Hkv, x.d,
+                                                                   x.max_pages, 16, TC))
+        call = kv.prepare_decode_hostio(hq, dd.k, dd.v, ht, hl, x.scale, ho, hls, ws,
+                                        pages_per_split=TC)
+        assert call() == 0
+        torch.cuda.synchronize()
+        assert kv.kv_get_status(ws) == 0
+        assert np.array_equal(ho.numpy(), o_dev.astype(np.float32)), pinned
+        assert np.array_equal(hls.numpy(), l_dev.astype(np.float32)), pinned
+
+
 def test_tune_and_policy_include_the_engine():
     x = W.bimodal_b4()
     dd = DeviceDecode(x)
@@ -185,9 +212,9 @@ def test_engine_device_errors():
 
 
 def test_engine_argument_checks():
-    # d = 64 and groups above 16 have no tensor-core form
+    # d = 64 and groups above 64 have no tensor-core form
     assert kv.kv_decode_workspace_size(2, 8, 2, 64, 4, 16, TC) == 0
-    assert kv.kv_decode_workspace_size(2, 64, 2, 128, 4, 16, TC) == 0
+    assert kv.kv_decode_workspace_size(2, 256, 2, 128, 4, 16, TC) == 0
     assert kv.kv_decode_workspace_size(2, 8, 2, 128, 4, 16, -2) == 0
     x = W.small_decode(58, 1, 8, 2, 64, [40])
     dd = DeviceDecode(x)

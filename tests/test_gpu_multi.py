@@ -40,8 +40,8 @@ def _check(x, T, out, lse, ref_out, ref_lse):
             assert np.abs(lse[b, i] - ref_lse[b, i]).max() <= 1e-3, (b, i)
 
 
-# T * G <= 16 (d = 128) runs on the tensor-core kernel; the rest on the
-# decode kernel over causal views.
+# T * G <= 64 (d = 128) runs on the tensor-core kernel (one consumer warp per
+# 16 rows); the rest on the decode kernel over causal views.
 @pytest.mark.parametrize("T,dtype,G,lens,pps", [
     (4, W.F16, 4, [3000, 17, 0, 2, 900], 0),
     (4, W.BF16, 4, [2500, 3, 0, 16, 48, 4100], 0),
@@ -51,8 +51,13 @@ def _check(x, T, out, lse, ref_out, ref_lse):
     (1, W.BF16, 8, [640, 12], 0),
     (1, W.F16, 16, [900, 31], 0),
     (3, W.F16, 4, [2000, 5], 0),
-    (8, W.F16, 4, [1000, 3, 40], 0),
+    (8, W.F16, 4, [1000, 3, 40], 0),            # 32 rows: two row blocks
     (2, W.F16, 8, [5000], 1),
+    (5, W.F16, 4, [1500, 4, 0, 333], 0),        # 20 rows: a partial second block
+    (16, W.F16, 4, [2100, 9, 700], 0),          # 64 rows: four row blocks
+    (8, W.BF16, 8, [1800, 30], 5),              # 64 rows, bf16, fixed splits
+    (12, W.BF16, 2, [64, 2000], 0),             # 24 rows
+    (16, W.F16, 8, [1200, 20], 0),              # 128 rows: causal views
 ])
 def test_attend_multi_small(T, dtype, G, lens, pps):
     rng = np.random.default_rng(T * 10 + G)
