@@ -151,7 +151,13 @@ def time_oracle(x: W.DecodeInputs, steps: int, warmup: int):
         O.decode(y, nthreads=cores)
         t.append(time.perf_counter() - t0)
     sec = statistics.median(t)
+    # the same sample on one host thread, once
+    t0 = time.perf_counter()
+    O.decode(y, nthreads=1)
+    sec1 = time.perf_counter() - t0
     return {"value": y.algorithmic_bytes() / sec / 1e9, "unit": "GB/s", "cores": cores,
+            "single_thread": {"value": y.algorithmic_bytes() / sec1 / 1e9, "unit": "GB/s",
+                              "ms_per_step": sec1 * 1e3, "cores": 1},
             "kind": "oracle", "ms_per_step": sec * 1e3,
             "tokens_per_s": x.B / sec * (y.Hkv / x.Hkv),
             "sample": f"all {x.B} sequences, KV heads 0..{y.Hkv - 1} of {x.Hkv} "
