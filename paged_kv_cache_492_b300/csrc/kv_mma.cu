@@ -1,5 +1,5 @@
-// Attention of up to 16 query rows per KV head over the paged cache on the
-// tensor cores: T query tokens x G grouped heads (T * G <= 16), so one page
+// Attention of up to 64 query rows per KV head over the paged cache on the
+// tensor cores: T query tokens x G grouped heads (T * G <= 64), so one page
 // tile read from HBM serves every row.  Used for several query tokens per
 // sequence (the step before decode: a prefill chunk or drafted tokens being
 // verified; the T queries are the sequence's last T tokens, causal) and for
@@ -19,8 +19,10 @@
 //    64 channels, channel half, slot, head, page) with the 128-byte swizzle
 //    into a ring of stages (full/empty mbarriers).  One stage is one page of
 //    every head of the block.
-//  * One consumer warp per KV head: S = Q K^T and O += P V are mma.sync
-//    m16n8k16 (fp32 accumulation) with the 16 query rows as M, K/V fragments
+//  * One consumer warp per KV head and block of 16 query rows (at most 8
+//    per CTA; a ring deep enough for ~192 KB in flight whatever the head
+//    block): S = Q K^T and O += P V are mma.sync m16n8k16 (fp32
+//    accumulation) with the warp's 16 query rows as M, K/V fragments
 //    from ldmatrix on the swizzled tiles (conflict-free), P taken from the
 //    score fragments straight into the A fragments of P V.  bf16
 //    probabilities are split into a high and a low bf16 part (two MMAs) so
