@@ -33,6 +33,10 @@ SMALL = [
     (51, 1, 32, 8, 128, [20000], W.F16),                       # one sequence over every chunk
     (60, 3, 64, 2, 128, [900, 0, 2500], W.BF16),               # G = 32: two row blocks
     (61, 2, 128, 2, 128, [3000, 77], W.F16),                   # G = 64: four row blocks
+    (65, 3, 12, 3, 128, [500, 1700, 16], W.BF16),              # head block 3, 8-stage ring
+    (66, 2, 20, 5, 128, [2300, 64], W.F16),                    # head block 5, 4-stage ring
+    (67, 2, 56, 7, 128, [1000, 999], W.BF16),                  # head block 7, 3-stage ring
+    (68, 2, 48, 1, 128, [1800, 33], W.F16),                    # Hkv = 1, G = 48: three row blocks
 ]
 
 

@@ -57,6 +57,7 @@ def _check(x, T, out, lse, ref_out, ref_lse):
     (16, W.F16, 4, [2100, 9, 700], 0),          # 64 rows: four row blocks
     (8, W.BF16, 8, [1800, 30], 5),              # 64 rows, bf16, fixed splits
     (12, W.BF16, 2, [64, 2000], 0),             # 24 rows
+    (12, W.F16, 4, [900, 11, 2600], 0),         # 48 rows: three row blocks
     (16, W.F16, 8, [1200, 20], 0),              # 128 rows: causal views
 ])
 def test_attend_multi_small(T, dtype, G, lens, pps):
