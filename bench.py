@@ -327,7 +327,8 @@ def run_ours(args, x, name, rank, world):
     d2h = x.B * x.Hq * x.d * 4 + x.B * x.Hq * 4
     line = {
         "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": n,
-        "warmup": args.warmup, "ms_per_step": t_step * 1e3, "higher_is_better": True,
+        "warmup": args.warmup, "ms_per_step": t_step * 1e3,
+        "ms_per_step_median": statistics.median(step_ms), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": W.DTYPE_NAMES[x.dtype],
         "data": "synthetic", "config": workload_config(x, name),
         "tokens_per_s": world * x.B / t_step, "kv_tokens_per_s": world * float(x.seq_lens.sum()) / t_step,
