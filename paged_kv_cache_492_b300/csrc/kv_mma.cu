@@ -443,11 +443,13 @@ __global__ void __launch_bounds__(32 * (1 + kMaxHeadBlock), 1)
 // lse = ln sum_s e^{lse_s}, out = sum_s e^{lse_s - lse} out_s (parts with
 // lse_s = -inf add nothing; all of them -inf gives out = 0, lse = -inf).
 // Split s of a sequence whose pages start in chunk c_0 is in slot 2 c_0 + 1
-// (s = 0) or 2 (c_0 + s).  One CTA per (sequence, KV head, row); its four
-// warps take a quarter of the splits each and merge them online, 32 at a
-// time (lane i holds split i's lse; the 16-partial batches are loaded before
-// they are needed, so a batch costs one memory round trip), then combine
-// through shared memory.  Single-split sequences were written by the
+// (s = 0) or 2 (c_0 + s).  One CTA per (sequence, KV head, row); its warps
+// take an equal share of the splits each and merge them online, 32 at a time
+// (lane i holds split i's lse; the 16-partial batches are loaded before they
+// are needed, so a batch costs one memory round trip), then combine through
+// shared memory.  16 warps when the grid fits the SMs once (few sequences,
+// each split over many chunks: one batch per warp), else 4 (many small CTAs
+// that schedule quickly and can wait beside the attention kernel's CTAs).  Single-split sequences were written by the
 // attention kernel; sequences without pages get out = 0, lse = -inf here.
 struct MmaMergeParams {
   const int32_t* page_off;  // [B + 1]
@@ -459,8 +461,7 @@ struct MmaMergeParams {
   int B, Hq, Hkv, G, Tq, rows, rows_pad;
 };
 
-constexpr int kMergeWarps = 4;
-
+template <int kMergeWarps>
 __global__ void __launch_bounds__(kMergeWarps * 32) mma_merge_kernel(const MmaMergeParams p) {
   __shared__ float sm_m[kMergeWarps], sm_l[kMergeWarps];
   __shared__ float4 sm_acc[kMergeWarps][32];
@@ -473,7 +474,7 @@ __global__ void __launch_bounds__(kMergeWarps * 32) mma_merge_kernel(const MmaMe
   const int i = r / p.G, g = r - (r / p.G) * p.G;
   const size_t row = ((size_t)b * p.Tq + i) * p.Hq + (size_t)h * p.G + g;
   if (ns == 0) {
-    p.out[row * kMmaD + threadIdx.x] = 0.f;
+    if (threadIdx.x < kMmaD) p.out[row * kMmaD + threadIdx.x] = 0.f;
     if (threadIdx.x == 0) p.lse[row] = -INFINITY;
     return;
   }
@@ -802,8 +803,14 @@ int mma_attend_launch(const void* q, const void* k_pool, const void* v_pool, int
   gp.Tq = Tq;
   gp.rows = mp.rows;
   gp.rows_pad = mp.rows_pad;
-  KV_CUDA_CHECK(launch(mma_merge_kernel, dim3((unsigned)((long long)B * Hkv), (unsigned)mp.rows),
-                       dim3(kMergeWarps * 32), 0, stream, true, gp));
+  const dim3 mgrid((unsigned)((long long)B * Hkv), (unsigned)mp.rows);
+  int dev = 0, sms = 0;
+  KV_CUDA_CHECK(cudaGetDevice(&dev));
+  KV_CUDA_CHECK(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev));
+  if ((long long)B * Hkv * mp.rows <= sms)
+    KV_CUDA_CHECK(launch(mma_merge_kernel<16>, mgrid, dim3(16 * 32), 0, stream, true, gp));
+  else
+    KV_CUDA_CHECK(launch(mma_merge_kernel<4>, mgrid, dim3(4 * 32), 0, stream, true, gp));
   return KV_OK;
 }
 
