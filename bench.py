@@ -208,11 +208,13 @@ def run_ours(args, x, name, rank, world):
     # calibrated once for the workload before any timing, as a server would
     # on first sight of a batch shape.
     policy = kv.DecodePolicy()
-    cands = list(policy.candidates)
+    cands = policy.usable(x.B, x.Hq, x.Hkv, x.d, x.max_pages)
     ws_t = kv.alloc_workspace(policy.workspace_size(x.B, x.Hq, x.Hkv, x.d, x.max_pages), device=dev)
     best, us = kv.kv_decode_tune(q, k, v, table, lens, x.scale, out, lse, ws_t, cands, reps=7)
     del ws_t
     pps = {"policy": best, "fused": 0, "tensor-core": kv.KV_DECODE_TENSOR_CORE}[args.engine]
+    if pps not in cands:
+        raise SystemExit(f"--engine {args.engine}: not available for this shape")
     tensor_core = pps == kv.KV_DECODE_TENSOR_CORE
     ws = kv.alloc_workspace(kv.kv_decode_hostio_workspace_size(x.B, x.Hq, x.Hkv, x.d, x.max_pages,
                                                                16, pps), device=dev)

@@ -306,11 +306,17 @@ class DecodePolicy:
         self.reps = reps
         self.table = {}
 
+    def usable(self, B, Hq, Hkv, d, max_pages, page_size=16):
+        """The candidates this shape supports (the tensor-core engine needs
+        d = 128 and G <= 64; an unsupported variant has workspace size 0)."""
+        return [c for c in self.candidates
+                if kv_decode_workspace_size(B, Hq, Hkv, d, max_pages, page_size, c) > 0]
+
     def workspace_size(self, B, Hq, Hkv, d, max_pages, page_size=16):
-        """Bytes a workspace needs to run every candidate (0 when none fits)."""
+        """Bytes a workspace needs to run every usable candidate (0 when none is)."""
         sizes = [kv_decode_workspace_size(B, Hq, Hkv, d, max_pages, page_size, c)
-                 for c in self.candidates]
-        return 0 if not sizes or min(sizes) == 0 else max(sizes)
+                 for c in self.usable(B, Hq, Hkv, d, max_pages, page_size)]
+        return max(sizes) if sizes else 0
 
     @staticmethod
     def signature(seq_lens_host, page_size=16):
@@ -326,9 +332,14 @@ class DecodePolicy:
                         lse, ws, stream=None):
         sig = self.signature(seq_lens_host, k_pool.shape[2])
         if sig not in self.table:
+            B, Hq, d = q.shape
+            _, Hkv, ps, _ = k_pool.shape
+            cands = self.usable(B, Hq, Hkv, d, block_table.shape[1], ps)
+            if not cands:
+                raise KVError(KV_EINVAL, "DecodePolicy: no candidate supports this shape")
             best, us = kv_decode_tune(q, k_pool, v_pool, block_table, seq_lens, scale, out, lse, ws,
-                                      self.candidates, self.reps, stream)
-            self.table[sig] = (best, dict(zip(self.candidates, us)))
+                                      cands, self.reps, stream)
+            self.table[sig] = (best, dict(zip(cands, us)))
         return self.table[sig][0]
 
 

@@ -61,23 +61,44 @@ def test_policy_calibrates_once_per_signature(monkeypatch):
         return candidates[-1], us
 
     monkeypatch.setattr(kv, "kv_decode_tune", fake_tune)
+    # every variant supported except the tensor-core engine at d = 64
+    monkeypatch.setattr(kv, "kv_decode_workspace_size",
+                        lambda B, Hq, Hkv, d, maxp, ps=16, pps=0: 0 if (pps < 0 and d != 128) else 1)
     pol = kv.DecodePolicy()
     assert pol.candidates[-1] == kv.KV_DECODE_TENSOR_CORE and 0 in pol.candidates
 
-    class Pool:  # only .shape is read: [P, Hkv, page_size, d]
+    class Shaped:  # only .shape is read
+        def __init__(self, *shape):
+            self.shape = shape
+
+    q = Shaped(3, 32, 128)
+    table = Shaped(3, 2000)
+
+    class Pool:  # [P, Hkv, page_size, d]
         shape = (10, 8, 16, 128)
 
     lens_a = [3000, 20, 500]
     lens_b = [3000, 20, 501]     # same pages, same signature
     lens_c = [30000, 20, 500]    # different page count
     for lens in (lens_a, lens_b, lens_a):
-        assert pol.pages_per_split(lens, None, Pool(), None, None, None, 1.0, None, None,
+        assert pol.pages_per_split(lens, q, Pool(), None, table, None, 1.0, None, None,
                                    None) == kv.KV_DECODE_TENSOR_CORE
     assert len(calls) == 1 and len(pol.table) == 1
-    pol.pages_per_split(lens_c, None, Pool(), None, None, None, 1.0, None, None, None)
+    pol.pages_per_split(lens_c, q, Pool(), None, table, None, 1.0, None, None, None)
     assert len(calls) == 2 and len(pol.table) == 2
     best, by_cand = pol.table[kv.DecodePolicy.signature(lens_c)]
     assert best == kv.KV_DECODE_TENSOR_CORE and by_cand[kv.KV_DECODE_TENSOR_CORE] == 5.0
+    assert calls[0] == tuple(pol.candidates)
+    # d = 64: the tensor-core engine is left out of the calibration
+    assert pol.usable(3, 32, 8, 64, 2000) == [c for c in pol.candidates if c >= 0]
+    assert pol.workspace_size(3, 32, 8, 64, 2000) == 1
+
+    class Pool64:
+        shape = (10, 8, 16, 64)
+
+    pol.pages_per_split([7, 7, 7], Shaped(3, 32, 64), Pool64(), None, table, None, 1.0, None,
+                        None, None)
+    assert calls[-1] == tuple(c for c in pol.candidates if c >= 0)
 
 
 def test_bench_launch_accounting():
