@@ -50,6 +50,42 @@ def test_decode_two_pages():
     assert math.isclose(_one(g, "lse0")[0], math.log(32), abs_tol=1e-15)
 
 
+def test_attend_multi_causal():
+    g = _read("attend_multi_causal.txt")
+    ps, P, d, T = 16, 6, 2, 3
+    kp = np.full((P, 1, ps, d), 7.0, np.float32)
+    vp = np.full((P, 1, ps, d), 7.0, np.float32)
+    lens = [int(t) for t in _one(g, "seq_lens")]
+    tables = [[int(t) for t in _one(g, f"table{b}")] for b in range(2)]
+
+    def put(b, t, k, v):
+        page = tables[b][t // ps]
+        kp[page, 0, t % ps], vp[page, 0, t % ps] = k, v
+
+    for t in range(16):
+        put(0, t, [0, 0], [1, 0])
+    put(0, 16, [1, 0], [0, 1])
+    put(0, 17, [1, 0], [0, 2])
+    put(1, 0, [0, 0], [1, 0])
+    put(1, 1, [1, 0], [0, 1])
+    x = W.DecodeInputs(name="golden_multi", B=2, Hq=1, Hkv=1, d=d, page_size=ps, dtype=W.F16,
+                       scale=_one(g, "scale")[0],
+                       q=W.to_bits(np.zeros((2, 1, d), np.float32), W.F16),
+                       k_pool=W.to_bits(kp, W.F16), v_pool=W.to_bits(vp, W.F16),
+                       block_table=np.array(tables, np.int32), seq_lens=np.array(lens, np.int32))
+    qm = W.to_bits(np.tile(np.array([1, 0], np.float32), (2, T, 1, 1)), W.F16)
+    out, lse = O.attend_multi(x, qm)
+    for b in range(2):
+        for i in range(T):
+            assert np.allclose(out[b, i, 0], g[f"out{b}"][i], rtol=0, atol=1e-12), (b, i)
+            want = g[f"lse{b}"][0][i]
+            if math.isinf(want):
+                assert math.isinf(lse[b, i, 0]) and lse[b, i, 0] < 0, (b, i)
+            else:
+                assert abs(lse[b, i, 0] - want) < 1e-12, (b, i)
+    assert math.isclose(g["lse0"][0][1], math.log(24), abs_tol=1e-15)
+
+
 def test_workqueue_small():
     g = _read("workqueue_small.txt")
     lens = [int(t) for t in _one(g, "seq_lens")]
