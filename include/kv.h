@@ -184,12 +184,17 @@ int kv_attend_multi(const void *q, const void *k_pool, const void *v_pool, int n
  * *best (host).  Synchronises `stream`; out/lse hold the last call's result.
  * `ws` must be sized for every candidate (kv_decode_workspace_size with the
  * smallest positive candidate covers all positive ones, and the size for
- * KV_DECODE_TENSOR_CORE covers it and the automatic one: pass the larger). */
+ * KV_DECODE_TENSOR_CORE covers it and the automatic one: pass the larger).
+ * `flush` (device, flush_bytes; NULL for none): a buffer larger than the L2
+ * cache, overwritten before every timed call (outside the events), so the
+ * candidates are timed with the inputs in HBM as a step that follows other
+ * work finds them; without it they are timed back to back, warm in L2. */
 int kv_decode_tune(const void *q, const void *k_pool, const void *v_pool, int num_pages,
                    const int32_t *block_table, int max_pages, const int32_t *seq_lens, int B,
                    int page_size, int Hq, int Hkv, int d, int dtype, float scale,
                    const int32_t *candidates, int n_candidates, int reps, float *out, float *lse,
-                   float *us, int32_t *best, void *ws, size_t ws_bytes, void *stream);
+                   float *us, int32_t *best, void *ws, size_t ws_bytes, void *flush,
+                   size_t flush_bytes, void *stream);
 
 /* Profiling aid: the next kv_decode (or kv_decode_hostio) issued from the
  * calling host thread records `event_before` (a cudaEvent_t) on its stream
@@ -198,6 +203,19 @@ int kv_decode_tune(const void *q, const void *k_pool, const void *v_pool, int nu
  * events disarm it. */
 int kv_profile_next_decode(void *event_before, void *event_after);
 
+/* Testing aid for the failure path (no counterpart on the pages): while `ns`
+ * is non-zero, every decode launched afterwards from this process (kv_decode
+ * with either engine, kv_attend_multi, kv_decode_hostio, kv_decode_noalloc)
+ * makes each consumer warp first wait `ns` nanoseconds on a barrier that
+ * nothing completes.  The wait runs out, and the kernel takes the way out
+ * every bounded wait takes: KV_ETIMEOUT in the status word, the producer
+ * stops issuing copies and waits for those in flight, and the outputs of
+ * non-empty sequences are left unwritten.  No GPU fault is involved.  0 (the
+ * default) turns it off.  A workspace used
+ * in this mode may hold partial merge state: reset it (kv_workspace_reset)
+ * before the next call. */
+int kv_test_consumer_timeout(unsigned long long ns);
+
 /* Workspace bytes for kv_decode_hostio: kv_decode's plus staging for q, the
  * block table, seq_lens, out and lse. */
 size_t kv_decode_hostio_workspace_size(int B, int Hq, int Hkv, int d, int max_pages,
@@ -205,11 +223,14 @@ size_t kv_decode_hostio_workspace_size(int B, int Hq, int Hkv, int d, int max_pa
 
 /* kv_decode with the per-step inputs and outputs in host memory: copies
  * h_q, h_block_table, h_seq_lens (host) into the workspace, runs kv_decode
- * against the device-resident pools, and copies out/lse back into h_out and
+ * against the device-resident pools, and delivers out/lse into h_out and
  * h_lse (host), all enqueued on `stream`.  Page-locked host buffers (which
- * the device can address) are read and written in place by one copy kernel
- * on each side; pageable ones take one cudaMemcpyAsync per buffer.  The
- * host buffers must stay valid until the stream reaches that point. */
+ * the device can address) are used in place: one copy kernel reads the three
+ * inputs, and the decode kernels write out/lse straight into h_out/h_lse
+ * (h_out 16-byte aligned; otherwise they are staged and copied back).
+ * Pageable buffers take one cudaMemcpyAsync each.  The host buffers must
+ * stay valid, and h_out/h_lse unread, until the stream reaches the end of
+ * the call. */
 int kv_decode_hostio(const void *h_q, const void *k_pool, const void *v_pool, int num_pages,
                      const int32_t *h_block_table, int max_pages, const int32_t *h_seq_lens,
                      int B, int page_size, int Hq, int Hkv, int d, int dtype, float scale,
@@ -228,14 +249,19 @@ int kv_decode_hostio(const void *h_q, const void *k_pool, const void *v_pool, in
  * cudaFree or allocating library routine.
  * Its scratch is one 16 MiB array in the library's device memory, present on
  * every device that loads the library until the process exits.  The first
- * call on a device looks up the array's device address (once per device);
+ * call on a device looks up the array's device address (once per device and
+ * CUDA context: after a cudaDeviceReset the next call looks it up again);
  * make that first call before any stream capture.  A batch whose scratch
  * (the size kv_decode_workspace_size reports) exceeds 16 MiB is rejected
  * with KV_EWORKSPACE and nothing is enqueued; with the automatic split this
  * holds every supported shape up to tens of thousands of sequences.  Every
- * call zeroes the part of the array it relies on, but all calls share the
- * array: calls whose work overlaps on the GPU (other streams, other host
- * threads) race and must be serialised by the caller. */
+ * call zeroes the part of the array it relies on (its merge tickets
+ * included), so a call that stopped early -- KV_ETIMEOUT -- leaves nothing
+ * that disturbs the next one, and unlike kv_decode this entry point never
+ * reports KV_EWORKSPACE for leftover tickets.  All calls share the array:
+ * calls whose work overlaps on the GPU (other streams, other host threads)
+ * race and must be serialised by the caller.  B = 0 enqueues only the
+ * zeroing of *status. */
 int kv_decode_noalloc(const void *q, const void *k_pool, const void *v_pool, int num_pages,
                       const int32_t *block_table, int max_pages, const int32_t *seq_lens, int B,
                       int page_size, int Hq, int Hkv, int d, int dtype, float scale,
@@ -368,6 +394,44 @@ int kv_append(const void *k_new, const void *v_new, void *k_pool, void *v_pool, 
               int32_t *block_table, int max_pages, int32_t *seq_lens, int32_t *free_list,
               int32_t *free_top, int32_t *refcnt, int B, int Hkv, int d, int page_size, int dtype,
               void *ws, size_t ws_bytes, void *stream);
+
+/* The budgeting part of one steady-state step [GP] in a single launch, for a
+ * batch without shared pages: the same results, bit for bit, as the calls
+ *   kv_update_query_summaries (first = 0; skipped when update_ema = 0),
+ *   kv_mark_active (mode 1), kv_summarize_last_pages, kv_score_pages,
+ *   kv_select_pages (KV_SELECT_BOUNDARY), kv_compact (page masks),
+ *   kv_append
+ * issued in that order on a valid state (every table entry in use is a pool
+ * page, lengths within the rows).  Each sequence's block computes its EMAs,
+ * its boundary mark, the summary of its page that just filled, its page
+ * scores, ranking and drift, and compacts its row unless it wants to grow;
+ * the last block to finish grants the grows in ascending b, compacts the
+ * rows that got no page, pushes the freed pages in (b, j) order and appends
+ * the token (k_new, v_new [B][Hkv][d]).  Arguments as in those calls;
+ * d in {64, 128}; `ws` of kv_budget_step_workspace_size bytes, zeroed before
+ * its first use (it keeps a counter in its header that each call leaves at
+ * zero; reset it after a call that failed).  Device errors as those calls
+ * report them. */
+size_t kv_budget_step_workspace_size(int B, int max_pages);
+int kv_budget_step(const void *q, const void *k_new, const void *v_new, void *k_pool,
+                   void *v_pool, int num_pages, int32_t *block_table, int max_pages,
+                   int32_t *seq_lens, int32_t *budget, int B, int Hq, int Hkv, int d,
+                   int page_size, int dtype, float a_fast, float a_slow, int update_ema,
+                   int n_first, int n_last, float delta, float ws_frac, float *ema, float *summ,
+                   float *scores, uint8_t *active, uint8_t *keep_mask, uint8_t *grow,
+                   int32_t *drift, int32_t *free_list, int32_t *free_top, void *ws,
+                   size_t ws_bytes, void *stream);
+
+/* Hand pool pages [first_page, first_page + n) to the free list (the
+ * integer free list of [EKV] section 2): pushed highest id first, so the
+ * following pops (kv_append, kv_compact) take them in ascending order.  This
+ * is how the pages of an elastic pool's growth (kv_vmm_pool_resize) become
+ * available to a budgeted sequence that grows.  free_list has `capacity`
+ * entries and *free_top (device) is its height; if the pages do not fit,
+ * KV_ENOSPACE goes to the status word of `ws` (kv_status_workspace_size
+ * bytes) and nothing changes. */
+int kv_free_list_push(int first_page, int n, int32_t *free_list, int capacity, int32_t *free_top,
+                      void *ws, void *stream);
 
 /* ------------------------------------------------------------------------ */
 /* Elastic page pool [EKV, section 3]: one reserved virtual address range     */

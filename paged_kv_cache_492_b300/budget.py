@@ -44,10 +44,16 @@ class BudgetedDecoder:
     seq_lens [B] int32, free_list [P] int32 + free_top [1] int32 (stack),
     budget [B] int32, refcnt [P] int32 (block-table references per pool page,
     for batches whose sequences share prefix pages; None = no sharing).  All
-    tensors live on one device and are updated in place by the kernels."""
+    tensors live on one device and are updated in place by the kernels.
+    pages_per_split picks the decode engine as kv_decode's argument does
+    (0: the fused kernel with the automatic split; KV_DECODE_TENSOR_CORE:
+    the tensor-core engine).  fused_step: issue the steady-state step's
+    budgeting part as the single kv_budget_step launch (batches without
+    shared pages) instead of its seven calls; the results are the same."""
 
     def __init__(self, k_pool, v_pool, block_table, seq_lens, free_list, free_top, budget,
-                 Hq: int, cfg: BudgetConfig, stream=None, refcnt=None):
+                 Hq: int, cfg: BudgetConfig, stream=None, refcnt=None, pages_per_split: int = 0,
+                 fused_step: bool = True):
         self.k_pool, self.v_pool = k_pool, v_pool
         self.table, self.lens = block_table, seq_lens
         self.free_list, self.free_top = free_list, free_top
@@ -68,12 +74,18 @@ class BudgetedDecoder:
         self.drift = torch.zeros(B, dtype=torch.int32, device=dev)
         self.out = torch.empty((B, Hq, d), dtype=torch.float32, device=dev)
         self.lse = torch.empty((B, Hq), dtype=torch.float32, device=dev)
+        self.fused_step = bool(fused_step) and refcnt is None
         ws = max(kv.kv_select_workspace_size(B, maxp),
                  kv.kv_compact_workspace_size(B, maxp, P if refcnt is not None else 0),
-                 kv.kv_append_workspace_size(B))
+                 kv.kv_append_workspace_size(B),
+                 kv.kv_budget_step_workspace_size(B, maxp) if self.fused_step else 0)
         self.ws = kv.alloc_workspace(ws, dev)
-        # kv_decode keeps merge tickets in its workspace between calls
-        self.decode_ws = kv.alloc_workspace(kv.kv_decode_workspace_size(B, Hq, Hkv, d, maxp), dev)
+        # kv_decode keeps merge tickets in its workspace between calls; sized
+        # for both engines so calibrate() can switch between them
+        self.pages_per_split = pages_per_split
+        self.decode_ws = kv.alloc_workspace(
+            max(kv.kv_decode_workspace_size(B, Hq, Hkv, d, maxp, ps, c)
+                for c in (0, pages_per_split, kv.KV_DECODE_TENSOR_CORE)), dev)
         self.scale = 1.0 / (d ** 0.5)
 
     # -- pieces ---------------------------------------------------------
@@ -120,6 +132,14 @@ class BudgetedDecoder:
         self._decode_part(q)
 
     def _budget_part(self, q, k_new, v_new, update_ema: bool):
+        if self.fused_step:
+            c = self.cfg
+            kv.kv_budget_step(q, k_new, v_new, self.k_pool, self.v_pool, self.table, self.lens,
+                              self.budget, c.a_fast, c.a_slow, update_ema, c.n_first, c.n_last,
+                              c.delta, c.ws_frac, self.ema, self.summ, self.scores, self.active,
+                              self.keep, self.grow, self.drift, self.free_list, self.free_top,
+                              self.ws, stream=self.stream)
+            return
         if update_ema:
             self.update_summaries(q, False)
         self.boundary()
@@ -129,14 +149,29 @@ class BudgetedDecoder:
 
     def _decode_part(self, q):
         kv.kv_decode(q, self.k_pool, self.v_pool, self.table, self.lens, self.scale, self.out,
-                     self.lse, self.decode_ws, stream=self.stream)
+                     self.lse, self.decode_ws, pages_per_split=self.pages_per_split,
+                     stream=self.stream)
+
+    def calibrate(self, q, candidates=(0, kv.KV_DECODE_TENSOR_CORE), reps=5, flush=None):
+        """Pick the decode engine for this batch by timing each candidate on
+        the current state (kv_decode_tune; `flush`, a device buffer larger
+        than L2, is overwritten before every timed call).  Call before
+        capture().  Returns (chosen pages_per_split, {candidate: us})."""
+        B, Hq, d = self.B, self.Hq, self.d
+        cands = [c for c in candidates
+                 if kv.kv_decode_workspace_size(B, Hq, self.Hkv, d, self.maxp, self.ps, c) > 0]
+        best, us = kv.kv_decode_tune(q, self.k_pool, self.v_pool, self.table, self.lens,
+                                     self.scale, self.out, self.lse, self.decode_ws, cands, reps,
+                                     self.stream, flush=flush)
+        self.pages_per_split = best
+        return best, dict(zip(cands, us))
 
     # -- the step as CUDA graphs ----------------------------------------
     def capture(self):
         """Record the steady-state step (t > 0) as two CUDA graphs -- the
         budgeting part (EMA, boundary compress-or-grow, append) and the
         decode -- over static input buffers, so a step costs two graph
-        launches instead of a dozen host calls.  Every kernel reads its
+        launches instead of a sequence of host calls.  Every kernel reads its
         state from device memory, so replays follow the batch as it evolves.
         Capture issues no work; call after at least one eager step (the
         library sets up its kernels on first use)."""

@@ -251,7 +251,8 @@ int kv_decode_hostio(const void* h_q, const void* k_pool, const void* v_pool, in
   void* m_s = mapped_host(h_lse);
   const bool in_mapped = m_q && m_t && m_l && !((uintptr_t)m_q & 3) && !((uintptr_t)m_t & 3) &&
                          !((uintptr_t)m_l & 3);
-  const bool out_mapped = m_o && m_s && !((uintptr_t)m_o & 3) && !((uintptr_t)m_s & 3);
+  // the kernels store out with 16-byte writes
+  const bool out_direct = m_o && m_s && !((uintptr_t)m_o & 15) && !((uintptr_t)m_s & 3);
   if (in_mapped) {
     CopySegs c{};
     c.src[0] = m_q; c.dst[0] = w + L.q; c.bytes[0] = qb;
@@ -264,19 +265,17 @@ int kv_decode_hostio(const void* h_q, const void* k_pool, const void* v_pool, in
     KV_CUDA_CHECK(cudaMemcpyAsync(w + L.table, h_block_table, tb, cudaMemcpyHostToDevice, s));
     KV_CUDA_CHECK(cudaMemcpyAsync(w + L.seq_lens, h_seq_lens, sb, cudaMemcpyHostToDevice, s));
   }
+  // Page-locked outputs are written in place by the decode kernels (the
+  // device addresses host memory directly; the writes are visible to the
+  // host once the stream has reached them); others are staged.
+  float* dev_out = out_direct ? static_cast<float*>(m_o) : reinterpret_cast<float*>(w + L.out);
+  float* dev_lse = out_direct ? static_cast<float*>(m_s) : reinterpret_cast<float*>(w + L.lse);
   int rc = engine_launch(w + L.q, k_pool, v_pool, num_pages,
                          reinterpret_cast<const int32_t*>(w + L.table), max_pages,
                          reinterpret_cast<const int32_t*>(w + L.seq_lens), B, page_size, Hq, Hkv, d,
-                         dtype, scale, pages_per_split, reinterpret_cast<float*>(w + L.out),
-                         reinterpret_cast<float*>(w + L.lse), ws, base, s);
+                         dtype, scale, pages_per_split, dev_out, dev_lse, ws, base, s);
   if (rc) return rc;
-  if (out_mapped) {
-    CopySegs c{};
-    c.src[0] = w + L.out; c.dst[0] = m_o; c.bytes[0] = ob;
-    c.src[1] = w + L.lse; c.dst[1] = m_s; c.bytes[1] = lb;
-    c.n = 2;
-    KV_CUDA_CHECK(launch_segs_copy(c, s));
-  } else {
+  if (!out_direct) {
     KV_CUDA_CHECK(cudaMemcpyAsync(h_out, w + L.out, ob, cudaMemcpyDeviceToHost, s));
     KV_CUDA_CHECK(cudaMemcpyAsync(h_lse, w + L.lse, lb, cudaMemcpyDeviceToHost, s));
   }
@@ -323,8 +322,10 @@ int kv_decode_tune(const void* q, const void* k_pool, const void* v_pool, int nu
                    const int32_t* block_table, int max_pages, const int32_t* seq_lens, int B,
                    int page_size, int Hq, int Hkv, int d, int dtype, float scale,
                    const int32_t* candidates, int n_candidates, int reps, float* out, float* lse,
-                   float* us, int32_t* best, void* ws, size_t ws_bytes, void* stream) {
+                   float* us, int32_t* best, void* ws, size_t ws_bytes, void* flush,
+                   size_t flush_bytes, void* stream) {
   if (!candidates || n_candidates < 1 || reps < 1 || !us || !best) return KV_EINVAL;
+  if (!flush) flush_bytes = 0;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   cudaEvent_t e0 = nullptr, e1 = nullptr;
   KV_CUDA_CHECK(cudaEventCreate(&e0));
@@ -342,6 +343,11 @@ int kv_decode_tune(const void* q, const void* k_pool, const void* v_pool, int nu
                        page_size, Hq, Hkv, d, dtype, scale, candidates[c], out, lse, ws, ws_bytes,
                        s);
     for (int r = 0; r < n && rc == KV_OK; ++r) {
+      // the L2 flush (when asked for) stays outside the timed events
+      if (flush_bytes && cudaMemsetAsync(flush, r & 0xff, flush_bytes, s) != cudaSuccess) {
+        rc = cuda_failed(cudaErrorUnknown, "cudaMemsetAsync (L2 flush)");
+        break;
+      }
       if (cudaEventRecord(e0, s) != cudaSuccess) { rc = cuda_failed(cudaErrorUnknown, "cudaEventRecord"); break; }
       rc = engine_launch(q, k_pool, v_pool, num_pages, block_table, max_pages, seq_lens, B,
                          page_size, Hq, Hkv, d, dtype, scale, candidates[c], out, lse, ws,
@@ -362,6 +368,11 @@ int kv_decode_tune(const void* q, const void* k_pool, const void* v_pool, int nu
   cudaEventDestroy(e1);
   if (rc == KV_OK) *best = candidates[best_i];
   return rc;
+}
+
+int kv_test_consumer_timeout(unsigned long long ns) {
+  set_test_consumer_wait_ns(ns);
+  return KV_OK;
 }
 
 int kv_profile_next_decode(void* event_before, void* event_after) {

@@ -11,6 +11,8 @@
 // stated in include/kv.h, so selections are reproducible bit for bit.
 #include <math.h>
 
+#include <algorithm>
+
 #include "kv_internal.h"
 
 namespace kvb {
@@ -263,23 +265,21 @@ struct SelectArgs {
   int* status;
 };
 
-// Phase 1: one block per sequence: ranks, drift, the compaction keep set.
-__global__ void __launch_bounds__(kSelThreads) select_rank_kernel(const SelectArgs a) {
-  extern __shared__ float sel_sm[];
-  __shared__ int red[32];
-  const int b = blockIdx.x;
+// One row (one block): ranks, drift and the compaction keep set of sequence
+// b; writes keep[b], drift[b], grow[b] = 0, and returns (on every thread)
+// whether the row wants to grow.  Inactive rows keep every page.
+__device__ int select_row(const SelectArgs& a, int b, float* sel_sm, int* red) {
   const int n = (int)ceil_div_ll(a.seq_lens[b], a.ps);
   uint8_t* keep = a.keep + (size_t)b * a.max_pages;
   const bool act = a.active ? a.active[b] != 0 : true;
   if (threadIdx.x == 0) {
-    a.wants[b] = 0;
     a.grow[b] = 0;
     if (a.drift) a.drift[b] = 0;
   }
   if (!act || n > a.max_pages) {
     if (n > a.max_pages && threadIdx.x == 0) set_status(a.status, KV_EINVAL);
     for (int j = threadIdx.x; j < a.max_pages; j += blockDim.x) keep[j] = j < n;
-    return;
+    return 0;
   }
   float* sf = sel_sm;
   float* ss = sf + n;
@@ -336,6 +336,15 @@ __global__ void __launch_bounds__(kSelThreads) select_rank_kernel(const SelectAr
     if (j < n) kp = cand[j] ? (rank[j] < k) : 1;
     keep[j] = kp;
   }
+  return wants;
+}
+
+// Phase 1: one block per sequence: ranks, drift, the compaction keep set.
+__global__ void __launch_bounds__(kSelThreads) select_rank_kernel(const SelectArgs a) {
+  extern __shared__ float sel_sm[];
+  __shared__ int red[32];
+  const int b = blockIdx.x;
+  const int wants = select_row(a, b, sel_sm, red);
   if (threadIdx.x == 0) a.wants[b] = wants;
 }
 
@@ -926,6 +935,436 @@ __global__ void append_copy_kernel(const AppendArgs a) {
   }
 }
 
+// ------------------------------------------------------------------ fused steady-state step
+// The budgeting part of one steady-state step in one launch, equal bit for
+// bit to kv_update_query_summaries (first = 0), kv_mark_active (mode 1),
+// kv_summarize_last_pages, kv_score_pages, kv_select_pages (boundary),
+// kv_compact (page masks) and kv_append issued in that order, for a batch
+// without shared pages.  Block b takes sequence b through the EMA update,
+// the boundary mark, the summary of the page that just filled, the scores,
+// the ranking and, unless it wants to grow, its compaction -- every value by
+// the same rounded operations in the same order as the separate kernels.
+// The last block to finish (a ticket taken after a fence; no block waits on
+// another) grants the grows in ascending b, compacts the rows that wanted to
+// grow but got no page, pushes the freed pages in (b, j) order and appends
+// the step's token.
+struct StepArgs {
+  const uint16_t* q;
+  const uint8_t* k_new;
+  const uint8_t* v_new;
+  uint8_t* k_pool;
+  uint8_t* v_pool;
+  int num_pages;
+  int32_t* table;
+  int max_pages;
+  int32_t* seq_lens;
+  int32_t* budget;
+  int B, Hq, Hkv, d, ps;
+  float a_fast, a_slow;
+  int n_first, n_last;
+  float delta, ws_frac;
+  int update_ema;     // 0: the EMAs are used as they are (the first step after the fit)
+  float* ema;
+  float* summ;
+  float* scores;
+  uint8_t* active;
+  uint8_t* keep;
+  uint8_t* grow;
+  int32_t* drift;
+  int32_t* free_list;
+  int32_t* free_top;
+  // workspace
+  int32_t* wants;     // [B]
+  int32_t* new_len;   // [B] length after compaction (before the append)
+  int32_t* drop_cnt;  // [B] pages freed by the compaction
+  int32_t* drop_ids;  // [B][max_pages] their ids, in j order
+  unsigned* ticket;   // in the status header; zero between calls
+  int* status;
+};
+
+constexpr int kStepThreads = 1024;
+constexpr size_t kStepTicketOffset = 64;  // bytes into the status header
+
+// Page-granular compaction of one row (whole block): the kept pages move to
+// the front in order (each reused where it is; no K/V moves), the row is -1
+// padded, the dropped page ids are listed in j order.  Returns the kept
+// token count K and sets *n_drops (both on every thread).  `row` is read
+// through L2 (it may have been written by another block).
+__device__ int compact_row_pages(int32_t* row, const uint8_t* keep_row, int n, int L, int ps,
+                                 int max_pages, int32_t* drops, int* n_drops, int* sm, int* carry) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
+  if (threadIdx.x == 0) carry[0] = carry[1] = 0;
+  __syncthreads();
+  int K_mine = 0;
+  for (int base = 0; base < n; base += blockDim.x) {
+    const int j = base + threadIdx.x;
+    const bool in = j < n;
+    const bool kept = in && __ldcg(keep_row + j) != 0;
+    const int old = in ? __ldcg(row + j) : -1;
+    const unsigned bk = __ballot_sync(FULL, kept), bd = __ballot_sync(FULL, in && !kept);
+    const unsigned lt = (1u << lane) - 1u;
+    if (lane == 0) {
+      sm[warp] = __popc(bk);
+      sm[32 + warp] = __popc(bd);
+    }
+    __syncthreads();
+    int bkb = 0, bdb = 0, tk = 0, td = 0;
+    for (int w = 0; w < nw; ++w) {
+      if (w < warp) {
+        bkb += sm[w];
+        bdb += sm[32 + w];
+      }
+      tk += sm[w];
+      td += sm[32 + w];
+    }
+    const int ck = carry[0], cd = carry[1];
+    // every old entry of this chunk has been read; a kept page moves to
+    // m <= j, so nothing not yet read is overwritten
+    __syncthreads();
+    if (kept) {
+      row[ck + bkb + __popc(bk & lt)] = old;
+      K_mine += min(L, (j + 1) * ps) - j * ps;
+    } else if (in) {
+      drops[cd + bdb + __popc(bd & lt)] = old;
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      carry[0] = ck + tk;
+      carry[1] = cd + td;
+    }
+    __syncthreads();
+  }
+  const int kept_total = carry[0];
+  *n_drops = carry[1];
+  for (int m = kept_total + threadIdx.x; m < max_pages; m += blockDim.x) row[m] = -1;
+  return block_sum_int(K_mine, sm);
+}
+
+template <class T, int CPL>
+__global__ void __launch_bounds__(kStepThreads) budget_step_kernel(const StepArgs a) {
+  extern __shared__ float step_sm[];
+  __shared__ int red[64];
+  __shared__ int s_carry[4];
+  __shared__ int s_last;
+  constexpr int D = 32 * CPL;
+  const int b = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int nw = blockDim.x >> 5;
+  const int G = a.Hq / a.Hkv;
+  float* ema_s = step_sm;                        // [2][Hkv][D], the updated EMAs of b
+  float* sel_sm = step_sm + 2 * a.Hkv * D;       // select_row's arrays
+  const uint16_t* k16 = reinterpret_cast<const uint16_t*>(a.k_pool);
+
+  // ---- query EMAs of b (as ema_kernel, first = 0)
+  for (int i = tid; i < a.Hkv * D; i += blockDim.x) {
+    const int h = i / D, c = i - h * D;
+    float gm = 0.0f;
+    if (a.update_ema) {
+      float acc = 0.0f;
+      for (int g = 0; g < G; ++g)
+        acc = __fadd_rn(acc, ld16<T>(a.q, ((size_t)b * a.Hq + (size_t)h * G + g) * D + c));
+      gm = __fdiv_rn(acc, (float)G);
+    }
+    for (int u = 0; u < 2; ++u) {
+      float* e = a.ema + (((size_t)b * 2 + u) * a.Hkv + h) * D + c;
+      const float al = u == 0 ? a.a_fast : a.a_slow;
+      float v = *e;
+      if (a.update_ema) {
+        v = __fadd_rn(__fmul_rn(al, v), __fmul_rn(__fsub_rn(1.0f, al), gm));
+        *e = v;
+      }
+      ema_s[(u * a.Hkv + h) * D + c] = v;
+    }
+  }
+  // ---- capacity boundary (as mark_kernel, mode 1)
+  const int L = a.seq_lens[b];
+  const bool act = L > 0 && L % a.ps == 0 && L / a.ps >= a.budget[b];
+  const int n = (int)ceil_div_ll(L, a.ps);
+  if (tid == 0) a.active[b] = act;
+  if (act && n <= a.max_pages) {
+    // ---- summary of the page that just filled (as summary_kernel)
+    const int page = a.table[(size_t)b * a.max_pages + (L / a.ps - 1)];
+    if (page < 0 || page >= a.num_pages) {
+      if (tid == 0) set_status(a.status, KV_EBADPAGE);
+    } else {
+      for (int i = tid; i < a.Hkv * D; i += blockDim.x) {
+        const int h = i / D, c = i - h * D;
+        float acc = 0.0f, mn = INFINITY, mx = -INFINITY;
+        for (int t = 0; t < a.ps; ++t) {
+          const float x = ld16<T>(k16, (((size_t)page * a.Hkv + h) * a.ps + t) * D + c);
+          acc = __fadd_rn(acc, x);
+          mn = x < mn ? x : mn;
+          mx = x > mx ? x : mx;
+        }
+        float* sp = a.summ + ((size_t)page * a.Hkv + h) * 3 * D;
+        sp[c] = __fdiv_rn(acc, (float)a.ps);
+        sp[D + c] = mn;
+        sp[2 * D + c] = mx;
+      }
+    }
+    __syncthreads();
+    // ---- scores of the resident pages (as score_kernel: one warp per page)
+    for (int j = warp; j < a.max_pages; j += nw) {
+      float2* out = reinterpret_cast<float2*>(a.scores + ((size_t)b * a.max_pages + j) * 2);
+      if (j >= n) {
+        if (lane == 0) *out = make_float2(-INFINITY, -INFINITY);
+        continue;
+      }
+      const int page = a.table[(size_t)b * a.max_pages + j];
+      if (page < 0 || page >= a.num_pages) {
+        if (lane == 0) set_status(a.status, KV_EBADPAGE);
+        continue;
+      }
+      float af = 0.0f, as = 0.0f;
+      for (int h = 0; h < a.Hkv; ++h) {
+        const float* uf = ema_s + (0 * a.Hkv + h) * D + lane * CPL;
+        const float* us = ema_s + (1 * a.Hkv + h) * D + lane * CPL;
+        const float* sm = a.summ + ((size_t)page * a.Hkv + h) * 3 * D + lane * CPL;
+#pragma unroll
+        for (int i = 0; i < CPL; ++i) {
+          const float mu = sm[i], mn = sm[D + i], mx = sm[2 * D + i];
+          {
+            const float u = uf[i];
+            const float ta = __fmul_rn(u, mn), tb = __fmul_rn(u, mx);
+            af = __fadd_rn(af, __fadd_rn(__fmul_rn(u, mu), ta > tb ? ta : tb));
+          }
+          {
+            const float u = us[i];
+            const float ta = __fmul_rn(u, mn), tb = __fmul_rn(u, mx);
+            as = __fadd_rn(as, __fadd_rn(__fmul_rn(u, mu), ta > tb ? ta : tb));
+          }
+        }
+      }
+#pragma unroll
+      for (int o = 16; o >= 1; o >>= 1) {
+        af = __fadd_rn(af, __shfl_xor_sync(FULL, af, o));
+        as = __fadd_rn(as, __shfl_xor_sync(FULL, as, o));
+      }
+      if (lane == 0) *out = make_float2(af, as);
+    }
+    __syncthreads();
+  }
+  // ---- selection (as select_rank_kernel, boundary mode)
+  SelectArgs sa{};
+  sa.scores = a.scores;
+  sa.seq_lens = a.seq_lens;
+  sa.active = a.active;
+  sa.budget = a.budget;
+  sa.B = a.B;
+  sa.max_pages = a.max_pages;
+  sa.ps = a.ps;
+  sa.n_first = a.n_first;
+  sa.n_last = a.n_last;
+  sa.mode = KV_SELECT_BOUNDARY;
+  sa.delta = a.delta;
+  sa.ws_frac = a.ws_frac;
+  sa.keep = a.keep;
+  sa.grow = a.grow;
+  sa.drift = a.drift;
+  sa.status = a.status;
+  __syncthreads();  // active[b] and the scores are visible to the block
+  const int wants = select_row(sa, b, sel_sm, red);
+  __threadfence();
+  __syncthreads();  // keep[b] is visible to the block
+  // ---- this row's compaction, unless it waits for the grant
+  int new_len = L, drops = 0;
+  if (act && !wants && n <= a.max_pages) {
+    new_len = compact_row_pages(a.table + (size_t)b * a.max_pages, a.keep + (size_t)b * a.max_pages,
+                                n, L, a.ps, a.max_pages, a.drop_ids + (size_t)b * a.max_pages,
+                                &drops, red, s_carry);
+  }
+  if (tid == 0) {
+    a.wants[b] = act ? wants : 0;
+    a.new_len[b] = new_len;
+    a.drop_cnt[b] = drops;
+  }
+  // ---- ticket: the last block to arrive finishes the step
+  __threadfence();
+  __syncthreads();
+  if (tid == 0) s_last = atomicAdd(a.ticket, 1u) == (unsigned)(a.B - 1);
+  __syncthreads();
+  if (!s_last) return;
+  __threadfence();
+  const int free_count = __ldcg(a.free_top);
+  // grants in ascending b while free pages last (as select_grant_kernel);
+  // rows that wanted a page and got none are compacted here
+  if (tid == 0) s_carry[2] = 0;  // rows left to compact
+  __syncthreads();
+  int* pend = reinterpret_cast<int*>(sel_sm);  // [B] rows to compact here
+  {
+    if (tid == 0) s_carry[3] = 0;
+    __syncthreads();
+    for (int base = 0; base < a.B; base += blockDim.x) {
+      const int bb = base + tid;
+      const int w = bb < a.B ? __ldcg(a.wants + bb) : 0;
+      int x = w;
+      for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(FULL, x, o);
+        if (lane >= o) x += y;
+      }
+      if (lane == 31) red[warp] = x;
+      __syncthreads();
+      int before = 0;
+      for (int i = 0; i < warp; ++i) before += red[i];
+      const int carry = s_carry[3];
+      const int excl = carry + before + x - w;
+      if (bb < a.B && w) {
+        if (excl < free_count) {
+          a.grow[bb] = 1;
+          a.budget[bb] += 1;
+          const int nb = (int)ceil_div_ll(__ldcg(a.seq_lens + bb), a.ps);
+          uint8_t* keep = a.keep + (size_t)bb * a.max_pages;
+          for (int j = 0; j < nb && j < a.max_pages; ++j) keep[j] = 1;
+        } else {
+          pend[atomicAdd(&s_carry[2], 1)] = bb;
+        }
+      }
+      __syncthreads();
+      if (tid == blockDim.x - 1) s_carry[3] = carry + before + x;
+      __syncthreads();
+    }
+  }
+  const int npend = s_carry[2];
+  for (int i = 0; i < npend; ++i) {
+    const int bb = pend[i];
+    const int Lb = __ldcg(a.seq_lens + bb);
+    int dr = 0;
+    const int K = compact_row_pages(a.table + (size_t)bb * a.max_pages,
+                                    a.keep + (size_t)bb * a.max_pages,
+                                    (int)ceil_div_ll(Lb, a.ps), Lb, a.ps, a.max_pages,
+                                    a.drop_ids + (size_t)bb * a.max_pages, &dr, red, s_carry);
+    if (tid == 0) {
+      a.new_len[bb] = K;
+      a.drop_cnt[bb] = dr;
+    }
+    __threadfence();
+    __syncthreads();
+  }
+  // freed pages onto the free list in (b, j) order (no page is popped by a
+  // page-granular compaction)
+  int top = free_count;
+  {
+    int* cnt_s = pend + a.B;  // [B] pages freed per row
+    if (tid == 0) s_carry[3] = 0;
+    __syncthreads();
+    for (int base = 0; base < a.B; base += blockDim.x) {
+      const int bb = base + tid;
+      const int c = bb < a.B ? __ldcg(a.drop_cnt + bb) : 0;
+      if (bb < a.B) cnt_s[bb] = c;
+      int x = c;
+      for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(FULL, x, o);
+        if (lane >= o) x += y;
+      }
+      if (lane == 31) red[warp] = x;
+      __syncthreads();
+      int before = 0;
+      for (int i = 0; i < warp; ++i) before += red[i];
+      const int carry = s_carry[3];
+      if (bb < a.B) pend[bb] = carry + before + x - c;  // exclusive offset of b's pushes
+      __syncthreads();
+      if (tid == blockDim.x - 1) s_carry[3] = carry + before + x;
+      __syncthreads();
+    }
+    const int pushes = s_carry[3];
+    for (int bb = 0; bb < a.B; ++bb) {
+      const int c = cnt_s[bb];
+      for (int r = tid; r < c; r += blockDim.x)
+        a.free_list[top + pend[bb] + r] = __ldcg(a.drop_ids + (size_t)bb * a.max_pages + r);
+    }
+    top += pushes;
+  }
+  __threadfence();
+  __syncthreads();
+  // ---- append (as append_plan_kernel + append_copy_kernel, no shared pages)
+  {
+    if (tid == 0) {
+      s_carry[0] = s_carry[1] = 0;
+      s_carry[3] = 0;
+    }
+    __syncthreads();
+    int my_need = 0;
+    for (int bb = tid; bb < a.B; bb += blockDim.x) {
+      const int Lb = __ldcg(a.new_len + bb);
+      if (Lb < 0) {
+        s_carry[1] = 1;
+      } else if (Lb % a.ps == 0) {
+        if (Lb / a.ps >= a.max_pages) s_carry[0] = 1;
+        ++my_need;
+      } else {
+        const int p = __ldcg(a.table + (size_t)bb * a.max_pages + Lb / a.ps);
+        if (p < 0 || p >= a.num_pages) s_carry[1] = 1;
+      }
+    }
+    const int total = block_sum_int(my_need, red);
+    if (total <= top)
+      for (int i = tid; i < total; i += blockDim.x) {
+        const int p = a.free_list[top - 1 - i];
+        if (p < 0 || p >= a.num_pages) s_carry[1] = 1;
+      }
+    __syncthreads();
+    const int err = s_carry[0] ? KV_EFULL : (s_carry[1] ? KV_EBADPAGE : (total > top ? KV_ENOSPACE : 0));
+    if (err) {
+      // the compaction stands; the append changes nothing
+      for (int bb = tid; bb < a.B; bb += blockDim.x) a.seq_lens[bb] = __ldcg(a.new_len + bb);
+      if (tid == 0) {
+        set_status(a.status, err);
+        *a.free_top = top;
+        *a.ticket = 0;
+      }
+      return;
+    }
+    int2* dest = reinterpret_cast<int2*>(pend);  // [B] (page, slot)
+    for (int base = 0; base < a.B; base += blockDim.x) {
+      const int bb = base + tid;
+      const int Lb = bb < a.B ? __ldcg(a.new_len + bb) : 1;
+      const bool nd = bb < a.B && Lb % a.ps == 0;
+      const unsigned bal = __ballot_sync(FULL, nd);
+      const int x = __popc(bal & ((1u << lane) - 1u));
+      __syncthreads();
+      if (lane == 0) red[warp] = __popc(bal);
+      __syncthreads();
+      int before = 0;
+      for (int i = 0; i < warp; ++i) before += red[i];
+      const int carry = s_carry[3];
+      if (bb < a.B) {
+        int32_t* slot = a.table + (size_t)bb * a.max_pages + Lb / a.ps;
+        int pg = __ldcg(slot);
+        if (nd) {
+          pg = a.free_list[top - 1 - (carry + before + x)];
+          *slot = pg;
+        }
+        dest[bb] = make_int2(pg, Lb % a.ps);
+        a.seq_lens[bb] = Lb + 1;
+      }
+      __syncthreads();
+      if (tid == 0) {
+        int tot = 0;
+        for (int i = 0; i < nw; ++i) tot += red[i];
+        s_carry[3] = carry + tot;
+      }
+      __syncthreads();
+    }
+    // the token's K and V rows (all heads) into place, 16 bytes per thread
+    const size_t row_bytes = (size_t)D * 2;
+    const int vec = (int)(row_bytes / 16);
+    const long long pieces = (long long)a.B * a.Hkv * vec;
+    for (long long i = tid; i < pieces; i += blockDim.x) {
+      const int bb = (int)(i / ((long long)a.Hkv * vec));
+      const int r = (int)(i - (long long)bb * a.Hkv * vec);
+      const int h = r / vec, v = r - h * vec;
+      const int2 dst = dest[bb];
+      const size_t so = ((size_t)bb * a.Hkv + h) * row_bytes + (size_t)v * 16;
+      const size_t dof = (((size_t)dst.x * a.Hkv + h) * a.ps + dst.y) * row_bytes + (size_t)v * 16;
+      *reinterpret_cast<uint4*>(a.k_pool + dof) = *reinterpret_cast<const uint4*>(a.k_new + so);
+      *reinterpret_cast<uint4*>(a.v_pool + dof) = *reinterpret_cast<const uint4*>(a.v_new + so);
+    }
+    if (tid == 0) {
+      *a.free_top = top - total;
+      *a.ticket = 0;  // ready for the next call
+    }
+  }
+}
+
 bool dtype_ok(int dtype) { return dtype == KV_F16 || dtype == KV_BF16; }
 
 constexpr int kCompactMaxSmem = 200 * 1024;  // shared memory of compact_apply_kernel, at most
@@ -940,6 +1379,34 @@ size_t ws_take(size_t* off, size_t bytes) {
 }  // namespace kvb
 
 using namespace kvb;
+
+namespace kvb {
+namespace {
+
+// Push pool pages [first, first + n) onto the free-list stack, highest id
+// first, so the next pops hand them out in ascending order.  One CTA; the
+// stack's capacity is checked before anything is written.
+__global__ void __launch_bounds__(256) free_push_kernel(int32_t* free_list, int32_t* free_top,
+                                                        int capacity, int first, int n,
+                                                        int* status) {
+  pdl_wait();
+  pdl_launch_dependents();
+  __shared__ int s_top;
+  if (threadIdx.x == 0) {
+    const int top = *free_top;
+    s_top = (top < 0 || (long long)top + n > capacity) ? -1 : top;
+    if (s_top < 0) set_status(status, KV_ENOSPACE);
+  }
+  __syncthreads();
+  const int top = s_top;
+  if (top < 0) return;
+  for (int i = threadIdx.x; i < n; i += blockDim.x) free_list[top + i] = first + n - 1 - i;
+  __syncthreads();
+  if (threadIdx.x == 0) *free_top = top + n;
+}
+
+}  // namespace
+}  // namespace kvb
 
 extern "C" {
 
@@ -1164,6 +1631,112 @@ int kv_compact(int32_t* block_table, int max_pages, int32_t* seq_lens, const uin
     KV_CUDA_CHECK(cudaFuncSetAttribute(compact_apply_kernel,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, kCompactMaxSmem));
   KV_CUDA_CHECK(launch(compact_apply_kernel, dim3(B), dim3(kApplyThreads), smem, s, false, a));
+  return KV_OK;
+}
+
+struct StepLayout {
+  size_t wants, new_len, drop_cnt, drop_ids, total;
+};
+static StepLayout step_layout(int B, int max_pages) {
+  StepLayout L{};
+  size_t off = kHeaderBytes;
+  const size_t nb = (size_t)(B > 0 ? B : 1);
+  L.wants = ws_take(&off, nb * 4);
+  L.new_len = ws_take(&off, nb * 4);
+  L.drop_cnt = ws_take(&off, nb * 4);
+  L.drop_ids = ws_take(&off, nb * (size_t)(max_pages > 0 ? max_pages : 1) * 4);
+  L.total = off;
+  return L;
+}
+
+// Dynamic shared memory of budget_step_kernel: the row's EMAs, then the
+// larger of select_row's arrays and the last block's per-row scratch.
+static size_t step_smem(int B, int Hkv, int d, int max_pages) {
+  return (size_t)2 * Hkv * d * 4 + std::max(select_smem(max_pages), (size_t)B * 8);
+}
+
+size_t kv_budget_step_workspace_size(int B, int max_pages) { return step_layout(B, max_pages).total; }
+
+int kv_budget_step(const void* q, const void* k_new, const void* v_new, void* k_pool, void* v_pool,
+                   int num_pages, int32_t* block_table, int max_pages, int32_t* seq_lens,
+                   int32_t* budget, int B, int Hq, int Hkv, int d, int page_size, int dtype,
+                   float a_fast, float a_slow, int update_ema, int n_first, int n_last, float delta,
+                   float ws_frac, float* ema, float* summ, float* scores, uint8_t* active,
+                   uint8_t* keep_mask, uint8_t* grow, int32_t* drift, int32_t* free_list,
+                   int32_t* free_top, void* ws, size_t ws_bytes, void* stream) {
+  if (B < 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv || (d != 64 && d != 128) || page_size <= 0 ||
+      max_pages < 1 || max_pages > kMaxSelectPages || n_first < 0 || n_last < 0 || num_pages < 1 ||
+      !dtype_ok(dtype))
+    return KV_EINVAL;
+  if (B == 0) return KV_OK;
+  if (!q || !k_new || !v_new || !k_pool || !v_pool || !block_table || !seq_lens || !budget ||
+      !ema || !summ || !scores || !active || !keep_mask || !grow || !free_list || !free_top || !ws)
+    return KV_EINVAL;
+  if (((uintptr_t)k_new | (uintptr_t)v_new | (uintptr_t)k_pool | (uintptr_t)v_pool) & 15)
+    return KV_EINVAL;
+  const StepLayout L = step_layout(B, max_pages);
+  if (ws_bytes < L.total) return KV_EWORKSPACE;
+  const size_t smem = step_smem(B, Hkv, d, max_pages);
+  int dev = 0, optin = 0;
+  KV_CUDA_CHECK(cudaGetDevice(&dev));
+  KV_CUDA_CHECK(cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev));
+  if (smem + 1024 > (size_t)optin) return KV_EINVAL;
+  uint8_t* w = static_cast<uint8_t*>(ws);
+  StepArgs a{};
+  a.q = static_cast<const uint16_t*>(q);
+  a.k_new = static_cast<const uint8_t*>(k_new);
+  a.v_new = static_cast<const uint8_t*>(v_new);
+  a.k_pool = static_cast<uint8_t*>(k_pool);
+  a.v_pool = static_cast<uint8_t*>(v_pool);
+  a.num_pages = num_pages;
+  a.table = block_table;
+  a.max_pages = max_pages;
+  a.seq_lens = seq_lens;
+  a.budget = budget;
+  a.B = B;
+  a.Hq = Hq;
+  a.Hkv = Hkv;
+  a.d = d;
+  a.ps = page_size;
+  a.a_fast = a_fast;
+  a.a_slow = a_slow;
+  a.n_first = n_first;
+  a.n_last = n_last;
+  a.delta = delta;
+  a.ws_frac = ws_frac;
+  a.update_ema = update_ema ? 1 : 0;
+  a.ema = ema;
+  a.summ = summ;
+  a.scores = scores;
+  a.active = active;
+  a.keep = keep_mask;
+  a.grow = grow;
+  a.drift = drift;
+  a.free_list = free_list;
+  a.free_top = free_top;
+  a.wants = reinterpret_cast<int32_t*>(w + L.wants);
+  a.new_len = reinterpret_cast<int32_t*>(w + L.new_len);
+  a.drop_cnt = reinterpret_cast<int32_t*>(w + L.drop_cnt);
+  a.drop_ids = reinterpret_cast<int32_t*>(w + L.drop_ids);
+  a.ticket = reinterpret_cast<unsigned*>(w + kStepTicketOffset);
+  a.status = reinterpret_cast<int*>(w);
+  using StepFn = void (*)(const StepArgs);
+  StepFn fn = dtype == KV_BF16 ? (d == 128 ? budget_step_kernel<BF16, 4> : budget_step_kernel<BF16, 2>)
+                               : (d == 128 ? budget_step_kernel<F16, 4> : budget_step_kernel<F16, 2>);
+  KV_CUDA_CHECK(cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem));
+  KV_CUDA_CHECK(launch(fn, dim3(B), dim3(kStepThreads), smem, static_cast<cudaStream_t>(stream),
+                       false, a));
+  return KV_OK;
+}
+
+int kv_free_list_push(int first_page, int n, int32_t* free_list, int capacity, int32_t* free_top,
+                      void* ws, void* stream) {
+  if (first_page < 0 || n < 0 || capacity < 0 || (long long)first_page + n > 0x7fffffffll)
+    return KV_EINVAL;
+  if (n == 0) return KV_OK;
+  if (!free_list || !free_top || !ws) return KV_EINVAL;
+  KV_CUDA_CHECK(launch(free_push_kernel, dim3(1), dim3(256), 0, static_cast<cudaStream_t>(stream),
+                       true, free_list, free_top, capacity, first_page, n, static_cast<int*>(ws)));
   return KV_OK;
 }
 

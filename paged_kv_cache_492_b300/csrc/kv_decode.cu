@@ -37,9 +37,11 @@
 //    a longer sequence's splits are merged in groups of about sqrt(splits)
 //    and then the groups, which spreads the merge traffic over the SMs that
 //    finish each group.  No CTA ever waits on another.
+#include <cuda.h>
 #include <math.h>
 
 #include <algorithm>
+#include <atomic>
 #include <mutex>
 #include <unordered_map>
 
@@ -59,8 +61,9 @@ constexpr int kDirectMerge = 8;  // splits merged in one pass; more go through g
 constexpr int kSmemAbort = 16 * kMaxStages;       // int
 constexpr int kSmemParams = kSmemAbort + 16;      // long long chunk, nchunks, W
 constexpr int kSmemScan = kSmemParams + 32;       // long long [32]
+constexpr int kSmemDead = kSmemScan + 32 * 8;     // mbarrier nothing completes (test mode)
 constexpr int kSmemHeader = 1024;
-static_assert(kSmemScan + 32 * 8 <= kSmemHeader, "shared header");
+static_assert(kSmemDead + 8 <= kSmemHeader, "shared header");
 
 struct DecodeParams {
   const uint8_t* q;
@@ -85,6 +88,7 @@ struct DecodeParams {
   uint32_t q_bytes;         // one sequence's q: Hq * d * 2
   uint32_t stage_bytes;     // K + V + q + header, 128-byte multiple
   uint32_t off_pbuf, off_offsets, off_stages;
+  unsigned long long test_wait_ns;  // > 0: failure-path test mode (see test_consumer_wait_ns)
 };
 
 __host__ __device__ constexpr uint32_t stage_header_offset(uint32_t kv_bytes, uint32_t q_bytes) {
@@ -114,6 +118,7 @@ __global__ void __launch_bounds__(kDecodeThreadsMax, 1) decode_kernel(const Deco
       mbar_init(smem_u32(&bars[s]), 1);
       mbar_init(smem_u32(&bars[kMaxStages + s]), p.Hkv);
     }
+    mbar_init(smem_u32(smem + kSmemDead), 1);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -222,9 +227,11 @@ __global__ void __launch_bounds__(kDecodeThreadsMax, 1) decode_kernel(const Deco
             const int pid = __shfl_sync(FULL, id, i);
             if (lane == 0) {
               bool ok = true;
-              if (round > 0) ok = mbar_wait(smem_u32(&bars[kMaxStages + slot]), (round - 1) & 1);
+              if (round > 0)
+                ok = mbar_wait(smem_u32(&bars[kMaxStages + slot]), (round - 1) & 1, kWaitLimitNs,
+                               abort_flag);
               if (!ok) {
-                set_status(p.status, KV_ETIMEOUT);
+                set_status(p.status, KV_ETIMEOUT);  // no-op when a consumer already set it
                 *abort_flag = 1;
                 aborted = true;
               } else {
@@ -255,7 +262,9 @@ __global__ void __launch_bounds__(kDecodeThreadsMax, 1) decode_kernel(const Deco
       if (!aborted) {
         // end-of-stream marker: a stage with no data
         bool ok = true;
-        if (round > 0) ok = mbar_wait(smem_u32(&bars[kMaxStages + slot]), (round - 1) & 1);
+        if (round > 0)
+          ok = mbar_wait(smem_u32(&bars[kMaxStages + slot]), (round - 1) & 1, kWaitLimitNs,
+                         abort_flag);
         if (ok) {
           uint8_t* st = stages + (size_t)slot * p.stage_bytes;
           *reinterpret_cast<int4*>(st + hdr_off) = make_int4(0, kDone, 0, -1);
@@ -420,6 +429,13 @@ __global__ void __launch_bounds__(kDecodeThreadsMax, 1) decode_kernel(const Deco
     }
   };
 
+  // test mode: a bounded wait on a barrier nothing completes runs out here,
+  // and the warp takes the same way out as any wait that runs out
+  if (p.test_wait_ns && !mbar_wait(smem_u32(smem + kSmemDead), 0, p.test_wait_ns)) {
+    set_status(p.status, KV_ETIMEOUT);
+    *abort_flag = 1;
+    return;
+  }
   int slot = 0, round = 0;
   for (;;) {  // one task (sequence, KV head h, split) per iteration
     if (!mbar_wait(smem_u32(&bars[slot]), round & 1)) {
@@ -782,7 +798,10 @@ bool shape_ok(int page_size, int Hq, int Hkv, int d, int dtype) {
 
 namespace {
 thread_local cudaEvent_t t_ev_before = nullptr, t_ev_after = nullptr;
+std::atomic<unsigned long long> g_test_wait_ns{0};
 }
+unsigned long long test_consumer_wait_ns() { return g_test_wait_ns.load(std::memory_order_relaxed); }
+void set_test_consumer_wait_ns(unsigned long long ns) { g_test_wait_ns.store(ns); }
 void set_profile_events(cudaEvent_t before, cudaEvent_t after) {
   t_ev_before = before;
   t_ev_after = after;
@@ -894,6 +913,7 @@ int decode_launch(const void* q, const void* k_pool, const void* v_pool, int num
   dp.off_pbuf = k.off_pbuf;
   dp.off_offsets = k.off_offsets;
   dp.off_stages = k.off_stages;
+  dp.test_wait_ns = test_consumer_wait_ns();
   KV_CUDA_CHECK(launch(k.fn, dim3((unsigned)n_workers), dim3((unsigned)k.threads), k.smem, stream,
                        true, dp));
   if (ev_after) KV_CUDA_CHECK(cudaEventRecord(ev_after, stream));
@@ -924,18 +944,57 @@ static __device__ __align__(256) uint8_t g_noalloc_scratch[kNoAllocScratchBytes]
 
 std::mutex g_noalloc_mu;
 void* g_noalloc_addr[kNoAllocMaxDevices] = {};
+unsigned long long g_noalloc_ctx[kNoAllocMaxDevices] = {};
 
-// Device address of the scratch array on the current device, looked up once
-// per device (the host-side name of the array is not a device address).
+// Unique id of the calling thread's current CUDA context (never reused, so
+// a context destroyed by cudaDeviceReset and created anew gets a new one);
+// 0 when no context is current yet.
+int current_context_id(unsigned long long* id) {
+  using CtxGetCurrent = CUresult (*)(CUcontext*);
+  using CtxGetId = CUresult (*)(CUcontext, unsigned long long*);
+  static CtxGetCurrent get_current = nullptr;
+  static CtxGetId get_id = nullptr;
+  if (!get_current || !get_id) {
+    void* f0 = nullptr;
+    void* f1 = nullptr;
+    cudaDriverEntryPointQueryResult q0, q1;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &f0, 12000, cudaEnableDefault, &q0) !=
+            cudaSuccess ||
+        q0 != cudaDriverEntryPointSuccess ||
+        cudaGetDriverEntryPointByVersion("cuCtxGetId", &f1, 12000, cudaEnableDefault, &q1) !=
+            cudaSuccess ||
+        q1 != cudaDriverEntryPointSuccess || !f0 || !f1)
+      return cuda_failed(cudaErrorNotSupported, "cuCtxGetCurrent / cuCtxGetId entry points");
+    get_current = reinterpret_cast<CtxGetCurrent>(f0);
+    get_id = reinterpret_cast<CtxGetId>(f1);
+  }
+  CUcontext ctx = nullptr;
+  *id = 0;
+  if (get_current(&ctx) != CUDA_SUCCESS)
+    return cuda_failed(cudaErrorUnknown, "cuCtxGetCurrent");
+  if (ctx && get_id(ctx, id) != CUDA_SUCCESS) return cuda_failed(cudaErrorUnknown, "cuCtxGetId");
+  return KV_OK;
+}
+
+// Device address of the scratch array on the current device (the host-side
+// name of the array is not a device address).  Looked up once per device and
+// context: a context reset (cudaDeviceReset) makes the next call look it up
+// again.  The lookup itself makes the device's primary context current.
 int noalloc_scratch(void** out) {
   int dev = 0;
   KV_CUDA_CHECK(cudaGetDevice(&dev));
   if (dev < 0 || dev >= kNoAllocMaxDevices) return KV_EINVAL;
+  unsigned long long ctx = 0;
+  int rc = current_context_id(&ctx);
+  if (rc) return rc;
   std::lock_guard<std::mutex> lk(g_noalloc_mu);
-  if (!g_noalloc_addr[dev]) {
+  if (!ctx || !g_noalloc_addr[dev] || g_noalloc_ctx[dev] != ctx) {
     void* ptr = nullptr;
     KV_CUDA_CHECK(cudaGetSymbolAddress(&ptr, g_noalloc_scratch));
+    rc = current_context_id(&ctx);
+    if (rc) return rc;
     g_noalloc_addr[dev] = ptr;
+    g_noalloc_ctx[dev] = ctx;
   }
   *out = g_noalloc_addr[dev];
   return KV_OK;
@@ -949,11 +1008,14 @@ int decode_noalloc(const void* q, const void* k_pool, const void* v_pool, int nu
   if (!shape_ok(page_size, Hq, Hkv, d, dtype)) return KV_EINVAL;
   if (B < 0 || num_pages < 0 || max_pages < 0 || pages_per_split < 0) return KV_EINVAL;
   if (!status) return KV_EINVAL;
-  if (B == 0) return KV_OK;
+  if ((uintptr_t)status & 3) return KV_EINVAL;
+  if (B == 0) {
+    KV_CUDA_CHECK(cudaMemsetAsync(status, 0, sizeof(int32_t), stream));
+    return KV_OK;
+  }
   if (num_pages < 1) return KV_EINVAL;
   if (!q || !k_pool || !v_pool || !block_table || !seq_lens || !out || !lse) return KV_EINVAL;
   if (((uintptr_t)q | (uintptr_t)k_pool | (uintptr_t)v_pool | (uintptr_t)out) & 15) return KV_EINVAL;
-  if ((uintptr_t)status & 3) return KV_EINVAL;
   KernelConfig k;
   int rc = kernel_config(Hq, Hkv, d, dtype, &k);
   if (rc) return rc;
@@ -1011,6 +1073,7 @@ int decode_noalloc(const void* q, const void* k_pool, const void* v_pool, int nu
   dp.off_pbuf = k.off_pbuf;
   dp.off_offsets = k.off_offsets;
   dp.off_stages = k.off_stages;
+  dp.test_wait_ns = test_consumer_wait_ns();
   KV_CUDA_CHECK(launch(k.fn, dim3((unsigned)n_workers), dim3((unsigned)k.threads), k.smem, stream,
                        true, dp));
   return KV_OK;

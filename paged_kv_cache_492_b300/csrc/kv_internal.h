@@ -117,4 +117,9 @@ int mma_attend_launch(const void* q, const void* k_pool, const void* v_pool, int
 void set_profile_events(cudaEvent_t before, cudaEvent_t after);
 void take_profile_events(cudaEvent_t* before, cudaEvent_t* after);
 
+// Failure-path test mode of the decode kernels (0 = off): every consumer
+// warp first waits this many nanoseconds on a barrier nothing completes.
+unsigned long long test_consumer_wait_ns();
+void set_test_consumer_wait_ns(unsigned long long ns);
+
 }  // namespace kvb

@@ -51,7 +51,10 @@ constexpr int kMaxStages = 12;          // pages in flight per CTA (3 at 8 heads
 constexpr int kRingBytes = 192 * 1024;  // shared memory for the ring
 constexpr int kMaxHeadBlock = 8;        // KV heads (consumer warps) per CTA
 constexpr int kHalfTile = 16 * 64 * 2;  // 16 tokens x 64 channels, bytes
-constexpr int kBarBytes = 256;          // full[kMaxStages], empty[kMaxStages]
+constexpr int kBarBytes = 256;          // full[kMaxStages], empty[kMaxStages], dead, abort
+constexpr int kDeadBar = 2 * kMaxStages;  // mbarrier nothing completes (test mode)
+constexpr int kAbortWord = 2 * kMaxStages + 1;  // 8-byte slot of the abort flag
+static_assert((kAbortWord + 1) * 8 <= kBarBytes, "barrier area");
 constexpr unsigned FULLM = 0xffffffffu;
 
 struct MmaParams {
@@ -69,6 +72,7 @@ struct MmaParams {
   int B, num_pages, max_pages, Hq, Hkv, G, Tq, rows, rows_pad, rb, hb, nhb, chunk_req, stages;
   long long n_chunks;         // chunks of the automatic split (CTAs per head block)
   float scale_log2;
+  unsigned long long test_wait_ns;  // > 0: failure-path test mode (see test_consumer_wait_ns)
 };
 
 __device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2,
@@ -154,15 +158,27 @@ __global__ void __launch_bounds__(32 * (1 + kMaxHeadBlock), 1)
 
   __shared__ int32_t s_off[kFusedMaxB + 1];
   __shared__ long long s_scan[32];
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(&bars[kAbortWord]);
   if (threadIdx.x == 0) {
     for (int s = 0; s < p.stages; ++s) {
       mbar_init(smem_u32(&bars[s]), 1);
       mbar_init(smem_u32(&bars[kMaxStages + s]), p.hb * p.rb);
     }
+    mbar_init(smem_u32(&bars[kDeadBar]), 1);
+    *abort_flag = 0;
     fence_mbar_init();
   }
   pdl_wait();  // lengths and page offsets may come from the previous kernel
   pdl_launch_dependents();
+  // Every producer reads block-table entries right after the offsets: have
+  // the table on its way to L2 meanwhile (spread over all CTAs).
+  {
+    const size_t lines = ((size_t)p.B * p.max_pages * 4 + 127) / 128;
+    const char* tb = reinterpret_cast<const char*>(p.table);
+    for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < lines && i < (1u << 20);
+         i += (size_t)gridDim.x * blockDim.x)
+      prefetch_l2(tb + i * 128);
+  }
   // page offsets O[b] of the batch (sum of ceil(L/16) before b)
   const int32_t* O = p.page_off_in;
   if (!O) {
@@ -227,9 +243,11 @@ __global__ void __launch_bounds__(32 * (1 + kMaxHeadBlock), 1)
           const int pid = __shfl_sync(FULLM, id, i);
           if (lane == 0) {
             bool ok = true;
-            if (round > 0) ok = mbar_wait(smem_u32(&bars[kMaxStages + slot]), (round - 1) & 1);
+            if (round > 0)
+              ok = mbar_wait(smem_u32(&bars[kMaxStages + slot]), (round - 1) & 1, kWaitLimitNs,
+                             abort_flag);
             if (!ok) {
-              set_status(p.status, KV_ETIMEOUT);
+              set_status(p.status, KV_ETIMEOUT);  // no-op when a consumer already set it
               aborted = true;
             } else {
               const uint32_t bar = smem_u32(&bars[slot]);
@@ -268,6 +286,13 @@ __global__ void __launch_bounds__(32 * (1 + kMaxHeadBlock), 1)
   const int h = hblk * p.hb + hw;
   const int qr0 = rbi * kMmaRows + (lane >> 2), qr1 = qr0 + 8, qc = (lane & 3) * 2;
   const int mi = lane >> 3, mr = lane & 7;  // ldmatrix: matrix mi, row mr
+  // test mode: a bounded wait on a barrier nothing completes runs out here,
+  // and the warp takes the same way out as any wait that runs out
+  if (p.test_wait_ns && !__all_sync(FULLM, mbar_wait(smem_u32(&bars[kDeadBar]), 0, p.test_wait_ns))) {
+    if (lane == 0) set_status(p.status, KV_ETIMEOUT);
+    *abort_flag = 1;
+    return;
+  }
   int slot = 0, round = 0;
   for (int b = b_first; b < p.B && O[b] < c1; ++b) {
     const long long Ob = O[b], np = O[b + 1] - Ob;
@@ -308,6 +333,7 @@ __global__ void __launch_bounds__(32 * (1 + kMaxHeadBlock), 1)
     for (int j = p0; j < p1; ++j) {
       if (!__all_sync(FULLM, mbar_wait(smem_u32(&bars[slot]), round & 1))) {
         if (lane == 0) set_status(p.status, KV_ETIMEOUT);
+        *abort_flag = 1;
         return;
       }
       const uint32_t kt = smem_u32(stages) + (uint32_t)slot * stage_bytes + hw * kHalfTile;
@@ -589,8 +615,44 @@ int encode_fn(EncodeTiledFn* out) {
 
 // Pool [P][Hkv][16][128] seen as 5-D (64 channels, channel half, slot, head,
 // page); one box is one channel half of `hb` heads of one page: hb x 16 rows
-// of 128 bytes, 128-byte swizzled.
+// of 128 bytes, 128-byte swizzled.  A map depends only on these arguments,
+// so the last few are kept and reused (encoding is host work on every call
+// otherwise).
+int encode_pool_map_uncached(CUtensorMap* m, const void* pool, int num_pages, int Hkv, int hb,
+                             int dtype);
 int encode_pool_map(CUtensorMap* m, const void* pool, int num_pages, int Hkv, int hb, int dtype) {
+  struct Entry {
+    const void* pool;
+    int num_pages, Hkv, hb, dtype;
+    CUtensorMap map;
+  };
+  constexpr int kEntries = 8;
+  static std::mutex mu;
+  static Entry cache[kEntries];
+  static int used = 0, next = 0;
+  {
+    std::lock_guard<std::mutex> lk(mu);
+    for (int i = 0; i < used; ++i) {
+      const Entry& e = cache[i];
+      if (e.pool == pool && e.num_pages == num_pages && e.Hkv == Hkv && e.hb == hb &&
+          e.dtype == dtype) {
+        *m = e.map;
+        return KV_OK;
+      }
+    }
+  }
+  const int rc = encode_pool_map_uncached(m, pool, num_pages, Hkv, hb, dtype);
+  if (rc) return rc;
+  std::lock_guard<std::mutex> lk(mu);
+  Entry& e = cache[next];
+  e = Entry{pool, num_pages, Hkv, hb, dtype, *m};
+  next = (next + 1) % kEntries;
+  if (used < kEntries) ++used;
+  return KV_OK;
+}
+
+int encode_pool_map_uncached(CUtensorMap* m, const void* pool, int num_pages, int Hkv, int hb,
+                             int dtype) {
   EncodeTiledFn fn;
   int rc = encode_fn(&fn);
   if (rc) return rc;
@@ -775,6 +837,7 @@ int mma_attend_launch(const void* q, const void* k_pool, const void* v_pool, int
   mp.chunk_req = pages_per_split;
   mp.n_chunks = chunks;
   mp.scale_log2 = scale * 1.4426950408889634f;
+  mp.test_wait_ns = test_consumer_wait_ns();
   // one CTA per (chunk, head block); chunks beyond the batch's count exit
   const long long grid = L.max_chunks * nhb;
   if (grid > 0x7fffffffll) return KV_EINVAL;

@@ -76,10 +76,11 @@ _SIGS = {
     "kv_decode_hostio": ([P, P, P, I, P, I, P, I, I, I, I, I, I, F, I, P, P, P, SZ, P], I),
     "kv_workqueue_workspace_size": ([I], SZ),
     "kv_profile_next_decode": ([P, P], I),
+    "kv_test_consumer_timeout": ([C.c_ulonglong], I),
     "kv_attend_multi_workspace_size": ([I, I, I, I, I, I, I, I], SZ),
     "kv_attend_multi": ([P, P, P, I, P, I, P, I, I, I, I, I, I, I, F, I, P, P, P, SZ, P], I),
-    "kv_decode_tune": ([P, P, P, I, P, I, P, I, I, I, I, I, I, F, P, I, I, P, P, P, P, P, SZ, P],
-                       I),
+    "kv_decode_tune": ([P, P, P, I, P, I, P, I, I, I, I, I, I, F, P, I, I, P, P, P, P, P, SZ, P,
+                        SZ, P], I),
     "kv_build_workqueue": ([P, I, I, I, I, I, I, P, I, P, I, P, P, P, P, P], I),
     "kv_update_query_summaries": ([P, I, I, I, I, I, F, F, I, P, P], I),
     "kv_mark_active": ([P, P, I, I, I, P, P], I),
@@ -91,6 +92,10 @@ _SIGS = {
     "kv_compact_workspace_size": ([I, I, I, I], SZ),
     "kv_compact": ([P, I, P, P, I, P, P, I, P, P, P, I, I, I, I, I, P, SZ, P], I),
     "kv_append_workspace_size": ([I], SZ),
+    "kv_free_list_push": ([I, I, P, I, P, P, P], I),
+    "kv_budget_step_workspace_size": ([I, I], SZ),
+    "kv_budget_step": ([P, P, P, P, P, I, P, I, P, P, I, I, I, I, I, I, F, F, I, I, I, F, F, P, P, P,
+                        P, P, P, P, P, P, P, SZ, P], I),
     "kv_vmm_pool_create": ([I, SZ, C.POINTER(C.c_void_p), C.POINTER(C.c_void_p),
                             C.POINTER(C.c_size_t)], I),
     "kv_vmm_pool_resize": ([P, SZ, C.POINTER(C.c_size_t)], I),
@@ -274,10 +279,11 @@ def kv_attend_multi(q, k_pool, v_pool, block_table, seq_lens, scale, out, lse, w
 
 
 def kv_decode_tune(q, k_pool, v_pool, block_table, seq_lens, scale, out, lse, ws, candidates,
-                   reps=5, stream=None):
+                   reps=5, stream=None, flush=None):
     """Time kv_decode for each candidate pages_per_split (0 = automatic,
     KV_DECODE_TENSOR_CORE = the tensor-core engine) on these inputs ->
-    (best candidate, [median us per candidate])."""
+    (best candidate, [median us per candidate]).  flush: a device buffer
+    larger than L2, overwritten before every timed call (None: timed warm)."""
     B, Hq, d = q.shape
     P_, Hkv, ps, _ = k_pool.shape
     cand = (C.c_int32 * len(candidates))(*[int(c) for c in candidates])
@@ -286,7 +292,10 @@ def kv_decode_tune(q, k_pool, v_pool, block_table, seq_lens, scale, out, lse, ws
     rc = lib().kv_decode_tune(_p(q), _p(k_pool), _p(v_pool), P_, _p(block_table),
                               block_table.shape[1], _p(seq_lens), B, ps, Hq, Hkv, d,
                               dtype_code(q), float(scale), cand, len(candidates), int(reps),
-                              _p(out), _p(lse), us, C.byref(best), _p(ws), ws.numel(), _s(stream))
+                              _p(out), _p(lse), us, C.byref(best), _p(ws), ws.numel(),
+                              _p(flush) if flush is not None else None,
+                              flush.numel() * flush.element_size() if flush is not None else 0,
+                              _s(stream))
     _check(rc, "kv_decode_tune")
     return int(best.value), [float(u) for u in us]
 
@@ -299,11 +308,15 @@ class DecodePolicy:
     size, log2 of its page count and its long-to-mean length ratio (rounded);
     the first batch with a new signature is timed with kv_decode_tune and the
     fastest variant is reused for every later batch with that signature.  The
-    workspace must be sized for every candidate (workspace_size)."""
+    workspace must be sized for every candidate (workspace_size).  With
+    `flush` (a device buffer larger than L2) the candidates are timed with L2
+    flushed before each call, as a step that follows other work runs."""
 
-    def __init__(self, candidates=(0, 8, 16, 32, 64, 128, KV_DECODE_TENSOR_CORE), reps=5):
+    def __init__(self, candidates=(0, 8, 16, 32, 64, 128, KV_DECODE_TENSOR_CORE), reps=5,
+                 flush=None):
         self.candidates = tuple(int(c) for c in candidates)
         self.reps = reps
+        self.flush = flush
         self.table = {}
 
     def usable(self, B, Hq, Hkv, d, max_pages, page_size=16):
@@ -338,7 +351,7 @@ class DecodePolicy:
             if not cands:
                 raise KVError(KV_EINVAL, "DecodePolicy: no candidate supports this shape")
             best, us = kv_decode_tune(q, k_pool, v_pool, block_table, seq_lens, scale, out, lse, ws,
-                                      cands, self.reps, stream)
+                                      cands, self.reps, stream, flush=self.flush)
             self.table[sig] = (best, dict(zip(cands, us)))
         return self.table[sig][0]
 
@@ -365,6 +378,13 @@ def kv_profile_next_decode(event_before, event_after):
     ev0 = event_before.cuda_event if event_before is not None else None
     ev1 = event_after.cuda_event if event_after is not None else None
     _check(lib().kv_profile_next_decode(ev0, ev1), "kv_profile_next_decode")
+
+
+def kv_test_consumer_timeout(ns: int):
+    """Failure-path test mode: while ns > 0, each decode consumer warp first
+    waits ns nanoseconds on a barrier nothing completes, so the kernel ends
+    with KV_ETIMEOUT (no GPU fault); 0 turns it off."""
+    _check(lib().kv_test_consumer_timeout(int(ns)), "kv_test_consumer_timeout")
 
 
 def kv_workqueue_workspace_size(B) -> int:
@@ -464,6 +484,34 @@ def kv_append(k_new, v_new, k_pool, v_pool, block_table, seq_lens, free_list, fr
                          _p(refcnt), B, Hkv, d, ps, dtype_code(k_pool), _p(ws), ws.numel(),
                          _s(stream))
     _check(rc, "kv_append")
+
+
+def kv_budget_step_workspace_size(B, max_pages) -> int:
+    return lib().kv_budget_step_workspace_size(B, max_pages)
+
+
+def kv_budget_step(q, k_new, v_new, k_pool, v_pool, block_table, seq_lens, budget, a_fast, a_slow,
+                   update_ema, n_first, n_last, delta, ws_frac, ema, summ, scores, active,
+                   keep_mask, grow, drift, free_list, free_top, ws, stream=None):
+    """The steady-state step's budgeting part in one launch (see kv.h)."""
+    B, Hq, d = q.shape
+    P_, Hkv, ps, _ = k_pool.shape
+    rc = lib().kv_budget_step(_p(q), _p(k_new), _p(v_new), _p(k_pool), _p(v_pool), P_,
+                              _p(block_table), block_table.shape[1], _p(seq_lens), _p(budget), B,
+                              Hq, Hkv, d, ps, dtype_code(k_pool), float(a_fast), float(a_slow),
+                              int(bool(update_ema)), int(n_first), int(n_last), float(delta),
+                              float(ws_frac), _p(ema), _p(summ), _p(scores), _p(active),
+                              _p(keep_mask), _p(grow), _p(drift), _p(free_list), _p(free_top),
+                              _p(ws), ws.numel(), _s(stream))
+    _check(rc, "kv_budget_step")
+
+
+def kv_free_list_push(first_page, n, free_list, free_top, ws, stream=None):
+    """Push pool pages [first_page, first_page + n) onto the free list
+    (highest id first, so they pop in ascending order)."""
+    rc = lib().kv_free_list_push(int(first_page), int(n), _p(free_list), free_list.numel(),
+                                 _p(free_top), _p(ws), _s(stream))
+    _check(rc, "kv_free_list_push")
 
 # ---------------------------------------------------------------- elastic pool
 class VmmPool:

@@ -91,18 +91,21 @@ class DecisionAnchor:
                                  self.summ64)
 
     # -- error bounds ------------------------------------------------------
-    def _score_error(self, b, pages, ema32, summ32, s64, s64b):
+    def _score_error(self, b, pages, ema32, summ32, s64):
         """Certified bound on |fp32 score - fp64 score| for row b's pages
         (n x 2): the stated order's arithmetic bound plus the exact effect of
-        the fp32 inputs."""
+        the fp32 inputs (their score evaluated in fp64 against the fp64
+        definition's)."""
         sm = summ32[pages].astype(np.float64)            # n, Hkv, 3, d
         err = np.zeros((len(pages), 2))
         for u in range(2):
             uu = ema32[b, u].astype(np.float64)          # Hkv, d
-            terms = (np.abs(uu * sm[:, :, 0]) +
-                     np.maximum(np.abs(uu * sm[:, :, 1]), np.abs(uu * sm[:, :, 2])))
+            ta, tb = uu * sm[:, :, 1], uu * sm[:, :, 2]
+            s64b = (uu * sm[:, :, 0] + np.maximum(ta, tb)).sum(axis=(1, 2))
+            terms = np.abs(uu * sm[:, :, 0]) + np.maximum(np.abs(ta), np.abs(tb))
             arith = (self.Hkv * self.d / 32 + 7) * U24 * terms.sum(axis=(1, 2))
-            err[:, u] = arith + np.abs(s64b[:, u] - s64[:, u]) + 1e-12 * np.abs(s64[:, u])
+            err[:, u] = (arith + np.abs(s64b - s64[:, u]) + 1e-12 * (np.abs(s64[:, u]) +
+                                                                      terms.sum(axis=(1, 2))))
         return err
 
     # -- one select_pages call -----------------------------------------------
@@ -116,9 +119,6 @@ class DecisionAnchor:
         s64 = np.zeros((B, maxp, 2))
         O.score_pages_f64(self.ema64, self.summ64, table, lens, act, self.Hkv, self.d, self.ps,
                           s64)
-        s64b = np.zeros((B, maxp, 2))
-        O.score_pages_f64(ema32.astype(np.float64), summ32.astype(np.float64), table, lens, act,
-                          self.Hkv, self.d, self.ps, s64b)
         st = self.stats
         wants64 = {}
         certain_wants = True
@@ -128,7 +128,7 @@ class DecisionAnchor:
                 continue
             n = -(-int(lens[b]) // self.ps)
             pages = table[b, :n]
-            err = self._score_error(b, pages, ema32, summ32, s64[b, :n], s64b[b, :n])
+            err = self._score_error(b, pages, ema32, summ32, s64[b, :n])
             # the fp32 scores really are within the bound of the fp64 ones
             d32 = np.abs(scores32[b, :n].astype(np.float64) - s64[b, :n])
             assert np.all(d32 <= err), (tag, b, float((d32 - err).max()))

@@ -3,7 +3,9 @@
 each; every step appends the new token's K/V (a page comes off the free list
 at each page boundary) and decodes over all tokens, with the split size
 chosen from the length.  Each step is checked against the oracle run on the
-same input state: the append bit for bit, the decode within tolerance."""
+same input state: the append bit for bit, the decode within tolerance, on
+both decode engines (the fused kernel and the tensor-core engine the bench's
+policy picks for these lengths)."""
 import os
 
 import numpy as np
@@ -23,14 +25,16 @@ def _pool_bits(t):
     return t.view(torch.int16).cpu().numpy().view(np.uint16)
 
 
+@pytest.mark.parametrize("engine", [kv.KV_DECODE_TENSOR_CORE, 0], ids=["tensor_core", "fused"])
 @pytest.mark.parametrize("L0", [32768, 65536, 131072])
-def test_bucketed_trace(L0):
+def test_bucketed_trace(L0, engine):
     steps = int(os.environ.get("KV_BUCKET_STEPS", "64"))
     seed = 3
     x = W.bucketed_long(L0, seed=seed, steps=steps)
     dd = DeviceDecode(x)
     fl, ft = i32(x.free_list), i32([x.free_top])
-    ws = kv.alloc_workspace(kv.kv_decode_workspace_size(x.B, x.Hq, x.Hkv, x.d, x.max_pages))
+    ws = kv.alloc_workspace(kv.kv_decode_workspace_size(x.B, x.Hq, x.Hkv, x.d, x.max_pages, 16,
+                                                        engine))
     ws_append = kv.alloc_workspace(kv.kv_append_workspace_size(x.B))
     # host state the oracle advances
     hk, hv = x.k_pool.copy(), x.v_pool.copy()
@@ -47,7 +51,8 @@ def test_bucketed_trace(L0):
         assert rc == 0
         dd.q.copy_(bits_to_dev(q, x.dtype))
         dd.out.fill_(float("nan"))
-        kv.kv_decode(dd.q, dd.k, dd.v, dd.table, dd.lens, x.scale, dd.out, dd.lse, ws)
+        kv.kv_decode(dd.q, dd.k, dd.v, dd.table, dd.lens, x.scale, dd.out, dd.lse, ws,
+                     pages_per_split=engine)
         assert kv.kv_get_status(ws) == 0, t
         # append: table, length, free list, and the written slot bit for bit
         assert np.array_equal(dd.table.cpu().numpy(), ht), t

@@ -11,6 +11,7 @@ from paged_kv_cache_492_b300 import budget as BG
 from paged_kv_cache_492_b300 import kv
 from paged_kv_cache_492_b300 import workloads as W
 from tests.budget_oracle import OracleBudget
+from tests.decision_check import DecisionAnchor
 from tests.gpu_util import DeviceDecode, assert_decode_close, bits_to_dev, i32
 
 pytestmark = pytest.mark.gpu
@@ -287,32 +288,42 @@ def test_tiny_selection_pipeline():
     keep, grow, bud, _ = _run_select(scr, x.seq_lens, None, [8], O.SELECT_TOPK, 0, 0, 0)
     kref, *_ = O.select_pages(scr, x.seq_lens, None, [8], 16, 0, 0, 0.5, O.SELECT_TOPK, 0)
     assert np.array_equal(keep, kref) and keep.sum() == 8
-    # fp64 definition: same selection (margin at the cut far above fp32 noise)
-    s64 = np.zeros((B, 16, 2))
-    summ64 = np.zeros((x.num_pages, Hkv, 3, d))
-    O.page_summaries_f64(x.k_pool, x.block_table[0], Hkv, 16, d, W.F16, summ64)
-    O.score_pages_f64(ref64, summ64, x.block_table, x.seq_lens, None, Hkv, d, 16, s64)
-    R = s64[0, :, 0] + s64[0, :, 1]
-    order = np.argsort(-R, kind="stable")
-    assert set(order[:8]) == set(np.nonzero(keep[0])[0])
-    margin = R[order[7]] - R[order[8]]
-    assert margin > 1e-3 * np.abs(R).max(), margin
+    # the fp64 definition keeps the same 8 pages, with the margin at the cut
+    # above the certified fp32 error bound
+    anchor = DecisionAnchor(B, Hq, Hkv, d, x.num_pages, W.F16, c["a_fast"], c["a_slow"])
+    for t in range(32):
+        anchor.update_ema(c["prior_q"][t], t == 0)
+    anchor.summarize(x.k_pool, x.block_table[0])
+    st = anchor.check(table=x.block_table, lens=x.seq_lens, active=None, budget=np.array([8]),
+                      free_count=0, mode=O.SELECT_TOPK, n_first=0, n_last=0, delta=0.5,
+                      ws_frac=0.5, ema32=ref, summ32=sref, scores32=scr, keep=keep, grow=grow,
+                      drift=np.zeros(B, np.int32), budget_after=bud, tag="tiny")
+    assert st.decisions == 1 and st.near_ties == 0, st.log
 
 
-def test_budgeted_serving_trajectory():
+@pytest.mark.parametrize("engine", [kv.KV_DECODE_TENSOR_CORE, 0], ids=["tensor_core", "fused"])
+def test_budgeted_serving_trajectory(engine):
     """Batch-64 budgeted decode: the fit, then every step's compress-or-grow,
-    append and block-table state bit-exact against the oracle's trajectory;
-    the decode output within tolerance on sampled steps."""
+    append and block-table state bit-exact against the oracle's trajectory.
+    Every step is also checked differentially: the oracle decodes the GPU's
+    input state for the sequences that compacted, grew or took a fresh page
+    that step plus 8 others drawn at random (the whole batch every 16 steps),
+    on the decode engine given.  With the tensor-core engine (the one the
+    bench picks) every budgeting decision is also checked against the fp64
+    definition: equal wherever its margin clears the fp32 error bound, and
+    near-ties reported."""
     steps = int(os.environ.get("KV_BUDGET_STEPS", "128"))
     c = W.budgeted_serving(steps=steps)
     x = c["decode"]
     cfg = BG.BudgetConfig(a_fast=c["a_fast"], a_slow=c["a_slow"], n_first=c["n_first"],
                           n_last=c["n_last"], delta=c["delta"])
-    orc = OracleBudget(x, c["budget"], cfg)
+    anchor = (DecisionAnchor(x.B, x.Hq, x.Hkv, x.d, x.num_pages, x.dtype, c["a_fast"],
+                             c["a_slow"]) if engine == kv.KV_DECODE_TENSOR_CORE else None)
+    orc = OracleBudget(x, c["budget"], cfg, anchor=anchor)
     orc.summarize_all()
     dd = DeviceDecode(x)
     dec = BG.BudgetedDecoder(dd.k, dd.v, dd.table, dd.lens, i32(x.free_list), i32([x.free_top]),
-                             i32(c["budget"]), x.Hq, cfg)
+                             i32(c["budget"]), x.Hq, cfg, pages_per_split=engine)
     dec.summarize_pages(i32(np.arange(x.num_pages)))
     q0, _, _ = W.step_tokens(c["seed"], 0, x.B, x.Hq, x.Hkv, x.d, x.dtype)
     dec.fit(bits_to_dev(q0, x.dtype))
@@ -329,8 +340,22 @@ def test_budgeted_serving_trajectory():
         assert np.array_equal(dec.free_list.cpu().numpy()[:top], orc.free_list[:top]), where
         assert np.array_equal(dec.ema.cpu().numpy(), orc.ema), where
 
+    def check_decisions(where):
+        if anchor is None:
+            return
+        pre = orc.pre
+        anchor.check(table=pre["table"], lens=pre["lens"], active=pre["active"],
+                     budget=pre["budget"], free_count=pre["free_count"], mode=pre["mode"],
+                     n_first=cfg.n_first, n_last=cfg.n_last, delta=cfg.delta,
+                     ws_frac=cfg.ws_frac, ema32=orc.ema, summ32=orc.summ,
+                     scores32=dec.scores.cpu().numpy(), keep=dec.keep.cpu().numpy(),
+                     grow=dec.grow.cpu().numpy(), drift=dec.drift.cpu().numpy(),
+                     budget_after=dec.budget.cpu().numpy(), tag=where)
+
     check_state("fit")
-    grows = compacts = 0
+    check_decisions("fit")
+    rng = np.random.default_rng(1234)
+    grows = compacts = checked_rows = 0
     for t in range(steps):
         q, kn, vn = W.step_tokens(c["seed"], t, x.B, x.Hq, x.Hkv, x.d, x.dtype)
         dec.step(bits_to_dev(q, x.dtype), bits_to_dev(kn, x.dtype), bits_to_dev(vn, x.dtype), t)
@@ -340,14 +365,31 @@ def test_budgeted_serving_trajectory():
         assert np.array_equal(dec.active.cpu().numpy(), orc.active)
         assert np.array_equal(dec.grow.cpu().numpy()[act], orc.grow[act])
         assert np.array_equal(dec.drift.cpu().numpy()[act], orc.drift[act])
+        check_decisions(f"step {t}")
         grows += int(orc.grow[act].sum())
         compacts += int(act.sum() - orc.grow[act].sum())
+        # decode on the GPU's input state, every step
+        y = orc.decode_inputs(q)
+        out = dec.out.cpu().numpy().astype(np.float64)
+        lse = dec.lse.cpu().numpy().astype(np.float64)
         if t % 16 == 15 or t == steps - 1:
-            y = orc.decode_inputs(q)
             ref_out, ref_lse = O.decode(y, nthreads=NCPU)
-            assert_decode_close(y, dec.out.cpu().numpy().astype(np.float64),
-                                dec.lse.cpu().numpy().astype(np.float64), ref_out, ref_lse)
-    print(f"budgeted serving: {steps} steps, {grows} grows, {compacts} compactions")
+            assert_decode_close(y, out, lse, ref_out, ref_lse)
+            checked_rows += x.B
+        else:
+            others = [b for b in range(x.B) if b not in orc.changed]
+            seqs = sorted(set(orc.changed) |
+                          set(rng.choice(others, size=min(8, len(others)), replace=False).tolist()))
+            rows = [(b, hq) for b in seqs for hq in range(x.Hq)]
+            ref_out, ref_lse = O.decode_rows(y, rows)
+            assert_decode_close(y, out, lse, ref_out, ref_lse, rows=rows)
+            checked_rows += len(seqs)
+    print(f"budgeted serving ({'tensor-core' if engine else 'fused'} decode): {steps} steps, "
+          f"{grows} grows, {compacts} compactions, {checked_rows} sequence decodes checked")
+    if anchor is not None:
+        print(f"fp64 anchor: {anchor.stats.summary()}")
+        for line in anchor.stats.log:
+            print("  " + line)
     assert grows > 0 and compacts > 0
 
 
@@ -493,3 +535,109 @@ def test_budgeted_step_graphed_matches_eager():
         assert torch.equal(eager.k_pool, graphed.k_pool) and torch.equal(eager.v_pool, graphed.v_pool), t
     for dec in decs:
         assert kv.kv_get_status(dec.ws) == 0 and kv.kv_get_status(dec.decode_ws) == 0
+
+
+# ------------------------------------------------------------- fused step
+_STATE = ("table", "lens", "budget", "free_top", "ema", "summ", "keep", "grow", "drift", "active",
+          "k_pool", "v_pool", "out", "lse")
+
+
+def _pair(x, budget, cfg, pages_per_split=0):
+    decs = []
+    for fused in (True, False):
+        dd = DeviceDecode(x)
+        dec = BG.BudgetedDecoder(dd.k, dd.v, dd.table, dd.lens, i32(x.free_list),
+                                 i32([x.free_top]), i32(budget), x.Hq, cfg,
+                                 pages_per_split=pages_per_split, fused_step=fused)
+        dec.summarize_pages(i32(np.arange(x.num_pages)))
+        decs.append(dec)
+    return decs
+
+
+def _same(a, b, where):
+    for name in _STATE:
+        assert torch.equal(getattr(a, name), getattr(b, name)), (where, name)
+    act = a.active.bool()
+    assert torch.equal(a.scores[act], b.scores[act]), (where, "scores")
+    top = int(a.free_top.item())
+    assert torch.equal(a.free_list[:top], b.free_list[:top]), (where, "free_list")
+    assert kv.kv_get_status(a.ws) == kv.kv_get_status(b.ws), where
+
+
+def test_fused_step_matches_the_calls():
+    """kv_budget_step (one launch) against the seven calls it replaces, on the
+    batch-64 budgeted workload: the whole state, bit for bit, every step."""
+    steps = 24
+    c = W.budgeted_serving(steps=steps)
+    x = c["decode"]
+    cfg = BG.BudgetConfig(a_fast=c["a_fast"], a_slow=c["a_slow"], n_first=c["n_first"],
+                          n_last=c["n_last"], delta=c["delta"])
+    fused, calls = _pair(x, c["budget"], cfg)
+    q0, _, _ = W.step_tokens(c["seed"], 0, x.B, x.Hq, x.Hkv, x.d, x.dtype)
+    for dec in (fused, calls):
+        dec.fit(bits_to_dev(q0, x.dtype))
+    _same(fused, calls, "fit")
+    grows = 0
+    for t in range(steps):
+        toks = [bits_to_dev(a, x.dtype)
+                for a in W.step_tokens(c["seed"], t, x.B, x.Hq, x.Hkv, x.d, x.dtype)]
+        for dec in (fused, calls):
+            dec.step(*toks, t)
+        torch.cuda.synchronize()
+        _same(fused, calls, f"step {t}")
+        grows += int(fused.grow[fused.active.bool()].sum())
+    assert grows > 0
+
+
+@pytest.mark.parametrize("dtype,d,free_top", [(W.F16, 64, 2), (W.BF16, 128, 0)])
+def test_fused_step_grants_run_out(dtype, d, free_top):
+    """Every row at a capacity boundary wants to grow (delta < 0); the free
+    list grants the first `free_top` rows and the rest are compacted by the
+    last block; the appends then take the freed pages.  Same state as the
+    separate calls."""
+    lens = [16 * 9, 16 * 12, 16 * 7, 16 * 30, 16 * 10, 16 * 8]
+    budget = np.array([9, 12, 7, 30, 10, 8], np.int32)
+    x = W.small_decode(91, len(lens), 8, 2, d, lens, dtype=dtype, pool_factor=1.3, pad_pages=3)
+    assert x.free_top >= free_top
+    x.free_top = free_top  # only the bottom `free_top` free pages are offered
+    cfg = BG.BudgetConfig(a_fast=0.9, a_slow=0.999, n_first=2, n_last=2, delta=-1.0)
+    fused, calls = _pair(x, budget, cfg)
+    rng = np.random.default_rng(5)
+    for t in range(3):
+        q = bits_to_dev(W.normal_bits(rng, (x.B, x.Hq, d), dtype), dtype)
+        kn = bits_to_dev(W.normal_bits(rng, (x.B, x.Hkv, d), dtype), dtype)
+        vn = bits_to_dev(W.normal_bits(rng, (x.B, x.Hkv, d), dtype), dtype)
+        for dec in (fused, calls):
+            if t == 0:
+                dec.update_summaries(q, True)
+            dec.step(q, kn, vn, t)
+        torch.cuda.synchronize()
+        _same(fused, calls, f"step {t}")
+        if t == 0:
+            act = fused.active.cpu().numpy().astype(bool)
+            assert act.all() and int(fused.grow.sum()) == free_top
+
+
+def test_fused_step_append_failure():
+    """A row whose last page is full but which is below its budget needs a
+    page the free list does not have: both paths report KV_ENOSPACE and
+    leave the same state (the compaction stands, the append changes
+    nothing)."""
+    lens = [16 * 5, 16 * 6, 40]
+    budget = np.array([5, 50, 9], np.int32)  # row 1 is below budget: no compaction, needs a page
+    x = W.small_decode(92, len(lens), 8, 2, 128, lens, dtype=W.BF16, pool_factor=1.0, pad_pages=2)
+    x.free_top = 0
+    cfg = BG.BudgetConfig(delta=0.5)
+    fused, calls = _pair(x, budget, cfg)
+    rng = np.random.default_rng(6)
+    q = bits_to_dev(W.normal_bits(rng, (x.B, x.Hq, 128), W.BF16), W.BF16)
+    kn = bits_to_dev(W.normal_bits(rng, (x.B, x.Hkv, 128), W.BF16), W.BF16)
+    vn = bits_to_dev(W.normal_bits(rng, (x.B, x.Hkv, 128), W.BF16), W.BF16)
+    for dec in (fused, calls):
+        dec.update_summaries(q, True)
+        dec._budget_part(q, kn, vn, False)
+    torch.cuda.synchronize()
+    for name in _STATE[:-2]:
+        assert torch.equal(getattr(fused, name), getattr(calls, name)), name
+    assert kv.kv_get_status(fused.ws) == kv.KV_ENOSPACE
+    assert kv.kv_get_status(calls.ws) == kv.KV_ENOSPACE

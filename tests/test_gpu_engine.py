@@ -182,6 +182,11 @@ def test_tune_and_policy_include_the_engine():
                                  cands, reps=3)
     assert best in cands and len(us) == 3 and all(u > 0 for u in us)
     assert us[cands.index(best)] == min(us)
+    # timed with L2 flushed before every call, as the bench times a step
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")
+    best_f, us_f = kv.kv_decode_tune(dd.q, dd.k, dd.v, dd.table, dd.lens, x.scale, dd.out, dd.lse,
+                                     ws, cands, reps=3, flush=flush)
+    assert best_f in cands and us_f[cands.index(best_f)] == min(us_f)
     out, lse, rc = dd.run(pages_per_split=best, ws=ws)
     assert rc == 0
     ref_out, ref_lse = O.decode(x, nthreads=NCPU)
@@ -213,6 +218,25 @@ def test_engine_device_errors():
     dd.lens.copy_(i32([16 * x.max_pages + 1, 40]))
     out, lse, rc = dd.run(pages_per_split=TC, ws=ws)
     assert rc == kv.KV_EINVAL and np.all(out[0] == 0)
+
+
+def test_engine_keeps_no_state_between_calls():
+    """The tensor-core engine rewrites all of its scratch (page offsets,
+    partials) on every call and keeps no counters between calls: a workspace
+    full of leftovers gives the same result as a clean one, call after call."""
+    x = W.small_decode(62, 3, 32, 8, 128, [20000, 900, 0])
+    dd = DeviceDecode(x)
+    ws = _ws(x)
+    ws[256:].fill_(1)
+    ref_out, ref_lse = O.decode(x, nthreads=NCPU)
+    first = None
+    for _ in range(3):
+        out, lse, rc = dd.run(pages_per_split=TC, ws=ws)
+        assert rc == 0
+        assert_decode_close(x, out, lse, ref_out, ref_lse)
+        if first is None:
+            first = (out, lse)
+        assert np.array_equal(out, first[0]) and np.array_equal(lse, first[1])
 
 
 def test_engine_argument_checks():

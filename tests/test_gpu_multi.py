@@ -59,6 +59,8 @@ def _check(x, T, out, lse, ref_out, ref_lse):
     (12, W.BF16, 2, [64, 2000], 0),             # 24 rows
     (12, W.F16, 4, [900, 11, 2600], 0),         # 48 rows: three row blocks
     (16, W.F16, 8, [1200, 20], 0),              # 128 rows: causal views
+    (1, W.F16, 4, [20000, 40, 0], 1),           # 1250 one-page splits: groups of 36
+    (4, W.BF16, 4, [17000, 3], 2),              # 532 splits x 16 rows: groups of 24
 ])
 def test_attend_multi_small(T, dtype, G, lens, pps):
     rng = np.random.default_rng(T * 10 + G)

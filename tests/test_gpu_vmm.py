@@ -120,3 +120,56 @@ def test_elastic_pool_resize_latency():
         assert small.mapped == 0
     finally:
         small.close()
+
+
+def test_grown_pages_reach_the_free_list():
+    """After the pool grows, kv_free_list_push hands the new pages to the free
+    list (highest id first), so the next appends pop them in ascending order
+    -- a budgeted grow can then draw on the pool's growth.  A push beyond the
+    list's capacity is refused and changes nothing."""
+    Hkv, d, ps = 2, 128, 16
+    page_bytes = Hkv * ps * d * 2
+    pk, pv = kv.VmmPool(1 << 28), kv.VmmPool(1 << 28)
+    try:
+        P0 = pk.granularity // page_bytes
+        pk.resize(P0 * page_bytes)
+        pv.resize(P0 * page_bytes)
+        x = W.small_decode(82, 3, 8, Hkv, d, [32, 20, 48], pool_factor=1.0, pad_pages=1)
+        assert x.num_pages <= P0
+        cap = 2 * P0
+        free_list = torch.full((cap,), -1, dtype=torch.int32, device="cuda")
+        free_top = i32([0])                       # every page of the first slice in use
+        ws = kv.alloc_workspace(kv.kv_status_workspace_size())
+        # grow by one slice and hand its pages to the free list
+        pk.resize(2 * P0 * page_bytes)
+        pv.resize(2 * P0 * page_bytes)
+        kv.kv_free_list_push(P0, P0, free_list, free_top, ws)
+        assert kv.kv_get_status(ws) == 0
+        assert int(free_top.item()) == P0
+        assert np.array_equal(free_list[:P0].cpu().numpy(), np.arange(2 * P0 - 1, P0 - 1, -1))
+        # appends to the sequences whose last page is full pop P0, P0 + 1, ...
+        k = pk.tensor((2 * P0, Hkv, ps, d), torch.float16)
+        v = pv.tensor((2 * P0, Hkv, ps, d), torch.float16)
+        k[:x.num_pages].copy_(torch.from_numpy(x.k_pool.view(np.int16)).view(torch.float16))
+        v[:x.num_pages].copy_(torch.from_numpy(x.v_pool.view(np.int16)).view(torch.float16))
+        table, lens = i32(x.block_table), i32(x.seq_lens)
+        rng = np.random.default_rng(3)
+        kn = torch.from_numpy(W.normal_bits(rng, (3, Hkv, d), W.F16).view(np.int16)).cuda().view(
+            torch.float16)
+        vn = torch.from_numpy(W.normal_bits(rng, (3, Hkv, d), W.F16).view(np.int16)).cuda().view(
+            torch.float16)
+        wa = kv.alloc_workspace(kv.kv_append_workspace_size(3))
+        kv.kv_append(kn, vn, k, v, table, lens, free_list, free_top, wa)
+        assert kv.kv_get_status(wa) == 0
+        t = table.cpu().numpy()
+        assert t[0, 2] == P0 and t[2, 3] == P0 + 1      # full pages at L = 32 and 48
+        assert np.array_equal(lens.cpu().numpy(), x.seq_lens + 1)
+        assert torch.equal(k[P0, :, 0], kn[0]) and torch.equal(v[P0 + 1, :, 0], vn[2])
+        # no room for more: refused, nothing changes
+        before = free_list.clone()
+        kv.kv_free_list_push(0, cap, free_list, free_top, ws)
+        assert kv.kv_get_status(ws) == kv.KV_ENOSPACE
+        assert torch.equal(free_list, before) and int(free_top.item()) == P0 - 2
+    finally:
+        pk.close()
+        pv.close()

@@ -54,7 +54,7 @@ def test_policy_calibrates_once_per_signature(monkeypatch):
     calls = []
 
     def fake_tune(q, k_pool, v_pool, table, lens, scale, out, lse, ws, candidates, reps,
-                  stream=None):
+                  stream=None, flush=None):
         calls.append(tuple(candidates))
         us = [10.0 + i for i in range(len(candidates))]
         us[-1] = 5.0  # the last candidate wins
