@@ -395,23 +395,28 @@ int kv_append(const void *k_new, const void *v_new, void *k_pool, void *v_pool, 
               int32_t *free_top, int32_t *refcnt, int B, int Hkv, int d, int page_size, int dtype,
               void *ws, size_t ws_bytes, void *stream);
 
-/* The budgeting part of one steady-state step [GP] in a single launch, for a
- * batch without shared pages: the same results, bit for bit, as the calls
+/* The budgeting part of one steady-state step [GP] in two launches (the step
+ * and a copy of the token's K/V rows), for a batch without shared pages: the
+ * same results, bit for bit, as the calls
  *   kv_update_query_summaries (first = 0; skipped when update_ema = 0),
  *   kv_mark_active (mode 1), kv_summarize_last_pages, kv_score_pages,
  *   kv_select_pages (KV_SELECT_BOUNDARY), kv_compact (page masks),
  *   kv_append
  * issued in that order on a valid state (every table entry in use is a pool
- * page, lengths within the rows).  Each sequence's block computes its EMAs,
- * its boundary mark, the summary of its page that just filled, its page
- * scores, ranking and drift, and compacts its row unless it wants to grow;
- * the last block to finish grants the grows in ascending b, compacts the
- * rows that got no page, pushes the freed pages in (b, j) order and appends
- * the token (k_new, v_new [B][Hkv][d]).  Arguments as in those calls;
+ * page, lengths within the rows, finite scores).  Sixteen work items per
+ * sequence at a capacity boundary (one for any other), taken in turn by a
+ * resident grid, form its updated EMAs and share its page scores (the item
+ * owning the last page summarises it first); the last of them to finish
+ * writes the EMAs, ranks the candidates under both summaries (working sets,
+ * drift) and compacts the row unless it wants to grow; the last sequence to
+ * finish grants the grows in ascending b, compacts the rows that got no
+ * page, pushes the freed pages in (b, j) order and plans the append, whose
+ * K/V rows (k_new, v_new [B][Hkv][d]) a second kernel copies.  No block
+ * waits on another.  Arguments as in those calls;
  * d in {64, 128}; `ws` of kv_budget_step_workspace_size bytes, zeroed before
- * its first use (it keeps a counter in its header that each call leaves at
- * zero; reset it after a call that failed).  Device errors as those calls
- * report them. */
+ * its first use and used by no other call: it keeps per-sequence counters
+ * that each call leaves at zero (reset it after a call that failed).  Device
+ * errors as those calls report them. */
 size_t kv_budget_step_workspace_size(int B, int max_pages);
 int kv_budget_step(const void *q, const void *k_new, const void *v_new, void *k_pool,
                    void *v_pool, int num_pages, int32_t *block_table, int max_pages,

@@ -77,9 +77,12 @@ class BudgetedDecoder:
         self.fused_step = bool(fused_step) and refcnt is None
         ws = max(kv.kv_select_workspace_size(B, maxp),
                  kv.kv_compact_workspace_size(B, maxp, P if refcnt is not None else 0),
-                 kv.kv_append_workspace_size(B),
-                 kv.kv_budget_step_workspace_size(B, maxp) if self.fused_step else 0)
+                 kv.kv_append_workspace_size(B))
         self.ws = kv.alloc_workspace(ws, dev)
+        # kv_budget_step keeps per-sequence tickets in its workspace between
+        # calls: it gets one of its own
+        self.step_ws = (kv.alloc_workspace(kv.kv_budget_step_workspace_size(B, maxp), dev)
+                        if self.fused_step else None)
         # kv_decode keeps merge tickets in its workspace between calls; sized
         # for both engines so calibrate() can switch between them
         self.pages_per_split = pages_per_split
@@ -138,7 +141,7 @@ class BudgetedDecoder:
                               self.budget, c.a_fast, c.a_slow, update_ema, c.n_first, c.n_last,
                               c.delta, c.ws_frac, self.ema, self.summ, self.scores, self.active,
                               self.keep, self.grow, self.drift, self.free_list, self.free_top,
-                              self.ws, stream=self.stream)
+                              self.step_ws, stream=self.stream)
             return
         if update_ema:
             self.update_summaries(q, False)
@@ -151,6 +154,60 @@ class BudgetedDecoder:
         kv.kv_decode(q, self.k_pool, self.v_pool, self.table, self.lens, self.scale, self.out,
                      self.lse, self.decode_ws, pages_per_split=self.pages_per_split,
                      stream=self.stream)
+
+    def status(self) -> int:
+        """First device-side error recorded by the budgeting calls or the
+        decode since the last check (0 = none); synchronises the stream."""
+        for ws in (self.ws, self.step_ws, self.decode_ws):
+            if ws is not None:
+                rc = kv.kv_get_status(ws, stream=self.stream)
+                if rc:
+                    return rc
+        return 0
+
+    # -- state dump for replaying a step ---------------------------------
+    STATE = ("table", "lens", "free_list", "free_top", "budget", "ema", "summ", "scores", "active",
+             "keep", "grow", "drift")
+
+    def dump(self, path, pools: bool = True):
+        """Write the batch's state to an .npz file (host copies): block
+        tables, lengths, free list, budgets, query EMAs, page summaries, the
+        last step's scores and decisions, reference counts and, with `pools`,
+        the K/V pools -- what a failed step needs to be replayed."""
+        import json
+
+        import numpy as np
+
+        arrays = {name: getattr(self, name).cpu().numpy() for name in self.STATE}
+        if self.refcnt is not None:
+            arrays["refcnt"] = self.refcnt.cpu().numpy()
+        if pools:
+            arrays["k_pool"] = self.k_pool.view(torch.int16).cpu().numpy()
+            arrays["v_pool"] = self.v_pool.view(torch.int16).cpu().numpy()
+        arrays["config"] = np.array(json.dumps(dataclasses.asdict(self.cfg)))
+        np.savez(path, **arrays)
+
+    def restore(self, path):
+        """Load a dump written by dump() into this decoder (same shapes and
+        configuration); the pools are restored when the dump holds them."""
+        import json
+
+        import numpy as np
+
+        with np.load(path) as z:
+            if json.loads(str(z["config"])) != dataclasses.asdict(self.cfg):
+                raise ValueError("dump was written with another budget configuration")
+            for name in self.STATE:
+                t = getattr(self, name)
+                a = z[name]
+                if tuple(a.shape) != tuple(t.shape):
+                    raise ValueError(f"dump has {name} of shape {a.shape}, decoder {tuple(t.shape)}")
+                t.copy_(torch.from_numpy(a))
+            if "refcnt" in z.files and self.refcnt is not None:
+                self.refcnt.copy_(torch.from_numpy(z["refcnt"]))
+            if "k_pool" in z.files:
+                self.k_pool.view(torch.int16).copy_(torch.from_numpy(z["k_pool"]))
+                self.v_pool.view(torch.int16).copy_(torch.from_numpy(z["v_pool"]))
 
     def calibrate(self, q, candidates=(0, kv.KV_DECODE_TENSOR_CORE), reps=5, flush=None):
         """Pick the decode engine for this batch by timing each candidate on
@@ -168,13 +225,14 @@ class BudgetedDecoder:
 
     # -- the step as CUDA graphs ----------------------------------------
     def capture(self):
-        """Record the steady-state step (t > 0) as two CUDA graphs -- the
-        budgeting part (EMA, boundary compress-or-grow, append) and the
-        decode -- over static input buffers, so a step costs two graph
-        launches instead of a sequence of host calls.  Every kernel reads its
-        state from device memory, so replays follow the batch as it evolves.
-        Capture issues no work; call after at least one eager step (the
-        library sets up its kernels on first use)."""
+        """Record the steady-state step (t > 0) as CUDA graphs over static
+        input buffers: the whole step as one graph, and its budgeting part
+        (EMA, boundary compress-or-grow, append) and decode as two more (to
+        time them apart), so a step costs one graph launch instead of a
+        sequence of host calls.  Every kernel reads its state from device
+        memory, so replays follow the batch as it evolves.  Capture issues no
+        work; call after at least one eager step (the library sets up its
+        kernels on first use)."""
         import torch
 
         B, Hq, Hkv, d = self.B, self.Hq, self.Hkv, self.d
@@ -186,25 +244,29 @@ class BudgetedDecoder:
         saved = self.stream
         side = torch.cuda.Stream(device=dev)
         self.g_budget, self.g_decode = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
+        self.g_step = torch.cuda.CUDAGraph()
         try:
             self.stream = None  # the capturing stream is the current one
             with torch.cuda.graph(self.g_budget, stream=side):
                 self._budget_part(self.q_in, self.k_in, self.v_in, True)
             with torch.cuda.graph(self.g_decode, stream=side):
                 self._decode_part(self.q_in)
+            with torch.cuda.graph(self.g_step, stream=side):
+                self._budget_part(self.q_in, self.k_in, self.v_in, True)
+                self._decode_part(self.q_in)
         finally:
             self.stream = saved
 
     def step_graphed(self, q, k_new, v_new, between=None):
         """One steady-state step (t > 0) by graph replay on the current
-        stream: copies the token's q/k/v into the static buffers, replays the
-        budgeting graph, calls `between()` if given (e.g. to record an
-        event), then replays the decode graph.  Same kernels, order and
-        results as step()."""
-        self.q_in.copy_(q)
-        self.k_in.copy_(k_new)
-        self.v_in.copy_(v_new)
+        stream: copies the token's q/k/v into the static buffers (one fused
+        copy) and replays the step's graph; with `between`, replays the
+        budgeting graph, calls `between()` (e.g. to record an event) and then
+        the decode graph.  Same kernels, order and results as step()."""
+        torch._foreach_copy_([self.q_in, self.k_in, self.v_in], [q, k_new, v_new])
+        if between is None:
+            self.g_step.replay()
+            return
         self.g_budget.replay()
-        if between is not None:
-            between()
+        between()
         self.g_decode.replay()

@@ -939,15 +939,22 @@ __global__ void append_copy_kernel(const AppendArgs a) {
 // The budgeting part of one steady-state step in one launch, equal bit for
 // bit to kv_update_query_summaries (first = 0), kv_mark_active (mode 1),
 // kv_summarize_last_pages, kv_score_pages, kv_select_pages (boundary),
-// kv_compact (page masks) and kv_append issued in that order, for a batch
-// without shared pages.  Block b takes sequence b through the EMA update,
-// the boundary mark, the summary of the page that just filled, the scores,
-// the ranking and, unless it wants to grow, its compaction -- every value by
-// the same rounded operations in the same order as the separate kernels.
-// The last block to finish (a ticket taken after a fence; no block waits on
-// another) grants the grows in ascending b, compacts the rows that wanted to
-// grow but got no page, pushes the freed pages in (b, j) order and appends
-// the step's token.
+// kv_compact (page masks) and kv_append issued in that order, for a valid
+// batch (finite scores) without shared pages.  Every value is computed by
+// the same rounded operations in the same order as in those kernels.
+//  * S blocks per sequence (one for a sequence not at a capacity boundary)
+//    each form the sequence's updated EMAs in shared memory and score a
+//    stride-S share of its pages, one warp per page; the block that owns the
+//    last page first summarises it (the page that just filled).
+//  * The last of those blocks to finish (a ticket; nobody waits) writes the
+//    EMAs, ranks the candidates under both summaries in one pass (working
+//    sets and drift), and -- unless the sequence wants to grow -- compacts
+//    it: a boundary compaction keeps all candidates but the last in
+//    retention order, the one with the smallest S_fast + S_slow (the higher
+//    logical index among equal keys).
+//  * The last sequence to finish (a second ticket) grants the grows in
+//    ascending b, compacts the sequences that wanted a page and got none,
+//    pushes the freed pages in (b, j) order and appends the step's token.
 struct StepArgs {
   const uint16_t* q;
   const uint8_t* k_new;
@@ -959,7 +966,7 @@ struct StepArgs {
   int max_pages;
   int32_t* seq_lens;
   int32_t* budget;
-  int B, Hq, Hkv, d, ps;
+  int B, Hq, Hkv, d, ps, S;
   float a_fast, a_slow;
   int n_first, n_last;
   float delta, ws_frac;
@@ -978,18 +985,27 @@ struct StepArgs {
   int32_t* new_len;   // [B] length after compaction (before the append)
   int32_t* drop_cnt;  // [B] pages freed by the compaction
   int32_t* drop_ids;  // [B][max_pages] their ids, in j order
-  unsigned* ticket;   // in the status header; zero between calls
+  int32_t* row_tk;    // [B] per-sequence tickets; zero between calls
+  int2* dest;         // [B] (page, slot) of each sequence's token, for step_copy_kernel
+  unsigned* ticket;   // in the status header: sequences finished; zero between calls
+  unsigned* grab;     // in the status header: items handed out; zero between calls
+  unsigned* exits;    // in the status header: blocks done taking items; zero between calls
+  int* ctl;           // in the status header: 1 when the append failed (nothing to copy)
   int* status;
 };
 
-constexpr int kStepThreads = 1024;
-constexpr size_t kStepTicketOffset = 64;  // bytes into the status header
+constexpr int kStepThreads = 512;
+constexpr int kStepSplit = 16;             // blocks per sequence at a boundary
+constexpr size_t kStepTicketOffset = 64;  // bytes into the status header: ticket,
+constexpr size_t kStepGrabOffset = 68;    // item counter,
+constexpr size_t kStepExitOffset = 72;    // exit counter,
+constexpr size_t kStepCtlOffset = 76;     // append-failed flag
 
 // Page-granular compaction of one row (whole block): the kept pages move to
 // the front in order (each reused where it is; no K/V moves), the row is -1
 // padded, the dropped page ids are listed in j order.  Returns the kept
-// token count K and sets *n_drops (both on every thread).  `row` is read
-// through L2 (it may have been written by another block).
+// token count K and sets *n_drops (both on every thread).  The row and its
+// keep mask are read through L2 (another block may have written them).
 __device__ int compact_row_pages(int32_t* row, const uint8_t* keep_row, int n, int L, int ps,
                                  int max_pages, int32_t* drops, int* n_drops, int* sm, int* carry) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
@@ -1040,21 +1056,173 @@ __device__ int compact_row_pages(int32_t* row, const uint8_t* keep_row, int n, i
   return block_sum_int(K_mine, sm);
 }
 
+// Ranks of the candidates j in [c0, c1) under two keys at once (the counting
+// definition of rank_of over that range: larger key first, equal keys by the
+// lower index); key2[j] = (key a, key b).  n <= 1024.
+__device__ void rank_two(const float2* key2, int c0, int c1, uint16_t* ra, uint16_t* rb) {
+  const int nc = c1 - c0;
+  int tpc = 1;  // lanes per candidate
+  while (tpc < 32 && tpc * 2 * nc <= (int)blockDim.x) tpc <<= 1;
+  const int per_pass = blockDim.x / tpc, sub = threadIdx.x & (tpc - 1);
+  for (int j0 = 0; j0 < nc; j0 += per_pass) {
+    const int j = c0 + j0 + (int)threadIdx.x / tpc;
+    const bool mine = j < c1;
+    int x = 0, y = 0;
+    if (mine) {
+      const float2 kj = key2[j];
+      for (int i = c0 + sub; i < c1; i += tpc) {
+        const float2 ki = key2[i];
+        x += ki.x > kj.x || (ki.x == kj.x && i < j);
+        y += ki.y > kj.y || (ki.y == kj.y && i < j);
+      }
+    }
+    for (int o = tpc >> 1; o; o >>= 1) {
+      x += __shfl_xor_sync(FULL, x, o);
+      y += __shfl_xor_sync(FULL, y, o);
+    }
+    if (mine && sub == 0) {
+      ra[j] = (uint16_t)x;
+      rb[j] = (uint16_t)y;
+    }
+  }
+  __syncthreads();
+}
+
+// Boundary selection of row b in one block (as select_row in boundary mode
+// for finite keys): writes keep[b], drift[b], grow[b] = 0; returns wants.
+// The candidates are the pages between the forced first and last ones.
+__device__ int select_boundary_row(const StepArgs& a, int b, int n, float* sm_f, int* red,
+                                   int* s_int) {
+  uint8_t* keep = a.keep + (size_t)b * a.max_pages;
+  if (threadIdx.x == 0) {
+    a.grow[b] = 0;
+    if (a.drift) a.drift[b] = 0;
+  }
+  const int c0 = min(a.n_first, n), c1 = max(c0, n - a.n_last);
+  const int nc = c1 - c0;
+  float2* key2 = reinterpret_cast<float2*>(sm_f);                  // [n] (S_fast, S_slow)
+  float* rr = reinterpret_cast<float*>(key2 + n);                  // [n] S_fast + S_slow
+  uint8_t* cand = reinterpret_cast<uint8_t*>(rr + n);              // [n] (rows above 1024)
+  uint16_t* idx = reinterpret_cast<uint16_t*>(cand + align_up(n, 4));  // [next_pow2(n)]
+  int P2 = 1;
+  while (P2 < n) P2 <<= 1;
+  uint16_t* rank_f = idx + P2;                                     // [n]
+  uint16_t* rank_s = rank_f + n;                                   // [n]
+  for (int j = threadIdx.x; j < n; j += blockDim.x) {
+    const float2 sc = __ldcg(reinterpret_cast<const float2*>(a.scores + (size_t)b * a.max_pages * 2) + j);
+    key2[j] = sc;
+    rr[j] = __fadd_rn(sc.x, sc.y);
+    cand[j] = j >= c0 && j < c1;
+  }
+  __syncthreads();
+  int wants = 0;
+  if (nc == 0) {
+    wants = 1;
+  } else {
+    int w = (int)ceilf(__fmul_rn(a.ws_frac, (float)nc));
+    w = max(1, min(w, nc));
+    if (n <= 1024) {
+      rank_two(key2, c0, c1, rank_f, rank_s);
+    } else {
+      float* sf = reinterpret_cast<float*>(rank_s + n);  // unpacked keys for the sort
+      float* ss = sf + n;
+      for (int j = threadIdx.x; j < n; j += blockDim.x) {
+        sf[j] = key2[j].x;
+        ss[j] = key2[j].y;
+      }
+      __syncthreads();
+      rank_candidates(sf, cand, n, idx, rank_f);
+      rank_candidates(ss, cand, n, idx, rank_s);
+    }
+    int my_d = 0;
+    for (int j = c0 + threadIdx.x; j < c1; j += blockDim.x) my_d += rank_f[j] < w && rank_s[j] >= w;
+    const int D = block_sum_int(my_d, red);
+    wants = (float)D > __fmul_rn(a.delta, (float)w);
+    if (threadIdx.x == 0 && a.drift) a.drift[b] = D;
+  }
+  // keep = forced + the best nc - 1 candidates by R: all candidates but the
+  // last in rank order -- the smallest R, the higher index among equal R
+  if (threadIdx.x == 0) s_int[0] = -1;
+  __syncthreads();
+  if (nc > 0) {
+    float best = INFINITY;
+    int bj = -1;
+    for (int j = c0 + threadIdx.x; j < c1; j += blockDim.x) {
+      if (bj < 0 || rr[j] < best || (rr[j] == best && j > bj)) {
+        best = rr[j];
+        bj = j;
+      }
+    }
+    for (int o = 16; o; o >>= 1) {
+      const float ob = __shfl_xor_sync(FULL, best, o);
+      const int oj = __shfl_xor_sync(FULL, bj, o);
+      if (oj >= 0 && (bj < 0 || ob < best || (ob == best && oj > bj))) {
+        best = ob;
+        bj = oj;
+      }
+    }
+    float* wb = reinterpret_cast<float*>(red);  // [32] values, [32..63] indices
+    if ((threadIdx.x & 31) == 0) {
+      wb[threadIdx.x >> 5] = best;
+      red[32 + (threadIdx.x >> 5)] = bj;
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      float bb = INFINITY;
+      int bjj = -1;
+      for (int w2 = 0; w2 < (int)(blockDim.x >> 5); ++w2) {
+        const float v = wb[w2];
+        const int jj = red[32 + w2];
+        if (jj >= 0 && (bjj < 0 || v < bb || (v == bb && jj > bjj))) {
+          bb = v;
+          bjj = jj;
+        }
+      }
+      s_int[0] = bjj;
+    }
+  }
+  __syncthreads();
+  const int drop = s_int[0];
+  for (int j = threadIdx.x; j < a.max_pages; j += blockDim.x) keep[j] = j < n && j != drop;
+  return wants;
+}
+
 template <class T, int CPL>
-__global__ void __launch_bounds__(kStepThreads) budget_step_kernel(const StepArgs a) {
+__global__ void __launch_bounds__(kStepThreads, 1) budget_step_kernel(const StepArgs a) {
   extern __shared__ float step_sm[];
   __shared__ int red[64];
   __shared__ int s_carry[4];
+  __shared__ int s_int[2];
   __shared__ int s_last;
   constexpr int D = 32 * CPL;
-  const int b = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int nw = blockDim.x >> 5;
   const int G = a.Hq / a.Hkv;
-  float* ema_s = step_sm;                        // [2][Hkv][D], the updated EMAs of b
-  float* sel_sm = step_sm + 2 * a.Hkv * D;       // select_row's arrays
+  float* ema_s = step_sm;                   // [2][Hkv][D], the updated EMAs of b
+  float* sel_sm = step_sm + 2 * a.Hkv * D;  // selection arrays / last block's scratch
   const uint16_t* k16 = reinterpret_cast<const uint16_t*>(a.k_pool);
+  bool finisher = false;  // this block finishes the step (the last sequence to arrive)
+  __shared__ unsigned s_item;
 
-  // ---- query EMAs of b (as ema_kernel, first = 0)
+  // items (sequence b, split s), split-major (every sequence's first item,
+  // then every second one, ...), taken one at a time by whichever block is
+  // free (a counter; blocks never wait on one another)
+  const unsigned n_items = (unsigned)a.B * (unsigned)a.S;
+  for (;;) {
+  __syncthreads();  // the previous item's use of shared memory is over
+  if (tid == 0) s_item = atomicAdd(a.grab, 1u);
+  __syncthreads();
+  const unsigned item = s_item;
+  if (item >= n_items) break;
+  const int s = (int)(item / a.B), b = (int)(item - (item / a.B) * a.B);
+  // ---- capacity boundary (as mark_kernel, mode 1)
+  const int L = a.seq_lens[b];
+  const bool act = L > 0 && L % a.ps == 0 && L / a.ps >= a.budget[b];
+  const int n = (int)ceil_div_ll(L, a.ps);
+  const bool scoring = act && n <= a.max_pages;
+  if (!scoring && s != 0) continue;  // one item for a sequence that is not scored
+  // ---- query EMAs of b (as ema_kernel, first = 0), into shared memory; the
+  // row's last block writes them out once every block has read the old ones
   for (int i = tid; i < a.Hkv * D; i += blockDim.x) {
     const int h = i / D, c = i - h * D;
     float gm = 0.0f;
@@ -1065,45 +1233,50 @@ __global__ void __launch_bounds__(kStepThreads) budget_step_kernel(const StepArg
       gm = __fdiv_rn(acc, (float)G);
     }
     for (int u = 0; u < 2; ++u) {
-      float* e = a.ema + (((size_t)b * 2 + u) * a.Hkv + h) * D + c;
       const float al = u == 0 ? a.a_fast : a.a_slow;
-      float v = *e;
-      if (a.update_ema) {
-        v = __fadd_rn(__fmul_rn(al, v), __fmul_rn(__fsub_rn(1.0f, al), gm));
-        *e = v;
-      }
+      float v = __ldcg(a.ema + (((size_t)b * 2 + u) * a.Hkv + h) * D + c);
+      if (a.update_ema) v = __fadd_rn(__fmul_rn(al, v), __fmul_rn(__fsub_rn(1.0f, al), gm));
       ema_s[(u * a.Hkv + h) * D + c] = v;
     }
   }
-  // ---- capacity boundary (as mark_kernel, mode 1)
-  const int L = a.seq_lens[b];
-  const bool act = L > 0 && L % a.ps == 0 && L / a.ps >= a.budget[b];
-  const int n = (int)ceil_div_ll(L, a.ps);
-  if (tid == 0) a.active[b] = act;
-  if (act && n <= a.max_pages) {
-    // ---- summary of the page that just filled (as summary_kernel)
-    const int page = a.table[(size_t)b * a.max_pages + (L / a.ps - 1)];
-    if (page < 0 || page >= a.num_pages) {
-      if (tid == 0) set_status(a.status, KV_EBADPAGE);
-    } else {
-      for (int i = tid; i < a.Hkv * D; i += blockDim.x) {
-        const int h = i / D, c = i - h * D;
-        float acc = 0.0f, mn = INFINITY, mx = -INFINITY;
-        for (int t = 0; t < a.ps; ++t) {
-          const float x = ld16<T>(k16, (((size_t)page * a.Hkv + h) * a.ps + t) * D + c);
-          acc = __fadd_rn(acc, x);
-          mn = x < mn ? x : mn;
-          mx = x > mx ? x : mx;
+  __syncthreads();
+  if (scoring) {
+    // ---- summary of the page that just filled (as summary_kernel), by the
+    // block that scores it
+    const int jl = n - 1;
+    if (jl % a.S == s) {
+      const int page = a.table[(size_t)b * a.max_pages + jl];
+      if (page < 0 || page >= a.num_pages) {
+        if (tid == 0) set_status(a.status, KV_EBADPAGE);
+      } else {
+        for (int i = tid; i < a.Hkv * D; i += blockDim.x) {
+          const int h = i / D, c = i - h * D;
+          const uint16_t* src = k16 + ((size_t)page * a.Hkv + h) * a.ps * D + c;
+          float acc = 0.0f, mn = INFINITY, mx = -INFINITY;
+          auto take = [&](float v) {
+            acc = __fadd_rn(acc, v);
+            mn = v < mn ? v : mn;
+            mx = v > mx ? v : mx;
+          };
+          if (a.ps == 16) {  // the 16 loads in flight together, then the running order
+            float x[16];
+#pragma unroll
+            for (int t = 0; t < 16; ++t) x[t] = ld16<T>(src, (size_t)t * D);
+#pragma unroll
+            for (int t = 0; t < 16; ++t) take(x[t]);
+          } else {
+            for (int t = 0; t < a.ps; ++t) take(ld16<T>(src, (size_t)t * D));
+          }
+          float* sp = a.summ + ((size_t)page * a.Hkv + h) * 3 * D;
+          sp[c] = __fdiv_rn(acc, (float)a.ps);
+          sp[D + c] = mn;
+          sp[2 * D + c] = mx;
         }
-        float* sp = a.summ + ((size_t)page * a.Hkv + h) * 3 * D;
-        sp[c] = __fdiv_rn(acc, (float)a.ps);
-        sp[D + c] = mn;
-        sp[2 * D + c] = mx;
       }
+      __syncthreads();
     }
-    __syncthreads();
-    // ---- scores of the resident pages (as score_kernel: one warp per page)
-    for (int j = warp; j < a.max_pages; j += nw) {
+    // ---- scores of this block's pages (as score_kernel: one warp per page)
+    for (int j = s + a.S * warp; j < a.max_pages; j += a.S * nw) {
       float2* out = reinterpret_cast<float2*>(a.scores + ((size_t)b * a.max_pages + j) * 2);
       if (j >= n) {
         if (lane == 0) *out = make_float2(-INFINITY, -INFINITY);
@@ -1115,22 +1288,30 @@ __global__ void __launch_bounds__(kStepThreads) budget_step_kernel(const StepArg
         continue;
       }
       float af = 0.0f, as = 0.0f;
+      const float* smp = a.summ + (size_t)page * a.Hkv * 3 * D + lane * CPL;
+#pragma unroll 4
       for (int h = 0; h < a.Hkv; ++h) {
         const float* uf = ema_s + (0 * a.Hkv + h) * D + lane * CPL;
         const float* us = ema_s + (1 * a.Hkv + h) * D + lane * CPL;
-        const float* sm = a.summ + ((size_t)page * a.Hkv + h) * 3 * D + lane * CPL;
+        const float* sm = smp + (size_t)h * 3 * D;
+        float mu[CPL], mnv[CPL], mxv[CPL];
 #pragma unroll
         for (int i = 0; i < CPL; ++i) {
-          const float mu = sm[i], mn = sm[D + i], mx = sm[2 * D + i];
+          mu[i] = sm[i];
+          mnv[i] = sm[D + i];
+          mxv[i] = sm[2 * D + i];
+        }
+#pragma unroll
+        for (int i = 0; i < CPL; ++i) {
           {
             const float u = uf[i];
-            const float ta = __fmul_rn(u, mn), tb = __fmul_rn(u, mx);
-            af = __fadd_rn(af, __fadd_rn(__fmul_rn(u, mu), ta > tb ? ta : tb));
+            const float ta = __fmul_rn(u, mnv[i]), tb = __fmul_rn(u, mxv[i]);
+            af = __fadd_rn(af, __fadd_rn(__fmul_rn(u, mu[i]), ta > tb ? ta : tb));
           }
           {
             const float u = us[i];
-            const float ta = __fmul_rn(u, mn), tb = __fmul_rn(u, mx);
-            as = __fadd_rn(as, __fadd_rn(__fmul_rn(u, mu), ta > tb ? ta : tb));
+            const float ta = __fmul_rn(u, mnv[i]), tb = __fmul_rn(u, mxv[i]);
+            as = __fadd_rn(as, __fadd_rn(__fmul_rn(u, mu[i]), ta > tb ? ta : tb));
           }
         }
       }
@@ -1141,93 +1322,108 @@ __global__ void __launch_bounds__(kStepThreads) budget_step_kernel(const StepArg
       }
       if (lane == 0) *out = make_float2(af, as);
     }
-    __syncthreads();
   }
-  // ---- selection (as select_rank_kernel, boundary mode)
-  SelectArgs sa{};
-  sa.scores = a.scores;
-  sa.seq_lens = a.seq_lens;
-  sa.active = a.active;
-  sa.budget = a.budget;
-  sa.B = a.B;
-  sa.max_pages = a.max_pages;
-  sa.ps = a.ps;
-  sa.n_first = a.n_first;
-  sa.n_last = a.n_last;
-  sa.mode = KV_SELECT_BOUNDARY;
-  sa.delta = a.delta;
-  sa.ws_frac = a.ws_frac;
-  sa.keep = a.keep;
-  sa.grow = a.grow;
-  sa.drift = a.drift;
-  sa.status = a.status;
-  __syncthreads();  // active[b] and the scores are visible to the block
-  const int wants = select_row(sa, b, sel_sm, red);
+  // ---- the row's last block: EMAs out, selection, compaction
   __threadfence();
-  __syncthreads();  // keep[b] is visible to the block
-  // ---- this row's compaction, unless it waits for the grant
-  int new_len = L, drops = 0;
-  if (act && !wants && n <= a.max_pages) {
-    new_len = compact_row_pages(a.table + (size_t)b * a.max_pages, a.keep + (size_t)b * a.max_pages,
-                                n, L, a.ps, a.max_pages, a.drop_ids + (size_t)b * a.max_pages,
-                                &drops, red, s_carry);
+  __syncthreads();
+  if (tid == 0)
+    s_last = atomicAdd(a.row_tk + b, 1) == (scoring ? a.S : 1) - 1;
+  __syncthreads();
+  if (!s_last) continue;
+  __threadfence();
+  for (int i = tid; i < 2 * a.Hkv * D; i += blockDim.x) {
+    const int u = i / (a.Hkv * D), r = i - u * (a.Hkv * D);
+    a.ema[((size_t)b * 2 + u) * a.Hkv * D + r] = ema_s[i];
+  }
+  int wants = 0, new_len = L, drops = 0;
+  uint8_t* keep = a.keep + (size_t)b * a.max_pages;
+  if (tid == 0) {
+    a.active[b] = act;
+    a.row_tk[b] = 0;  // ready for the next call
+  }
+  if (!act || n > a.max_pages) {
+    // as select_row for a row that is not selected: every page kept
+    if (n > a.max_pages && tid == 0) set_status(a.status, KV_EINVAL);
+    if (tid == 0) {
+      a.grow[b] = 0;
+      if (a.drift) a.drift[b] = 0;
+    }
+    for (int j = tid; j < a.max_pages; j += blockDim.x) keep[j] = j < n;
+  } else {
+    wants = select_boundary_row(a, b, n, sel_sm, red, s_int);
+    __threadfence();
+    __syncthreads();
+    if (!wants)
+      new_len = compact_row_pages(a.table + (size_t)b * a.max_pages, keep, n, L, a.ps,
+                                  a.max_pages, a.drop_ids + (size_t)b * a.max_pages, &drops, red,
+                                  s_carry);
   }
   if (tid == 0) {
     a.wants[b] = act ? wants : 0;
     a.new_len[b] = new_len;
     a.drop_cnt[b] = drops;
   }
-  // ---- ticket: the last block to arrive finishes the step
+  // ---- the last sequence to arrive finishes the step
   __threadfence();
   __syncthreads();
   if (tid == 0) s_last = atomicAdd(a.ticket, 1u) == (unsigned)(a.B - 1);
   __syncthreads();
-  if (!s_last) return;
+  if (s_last) finisher = true;
+  }  // items
+  // the last block to stop taking items puts the counters back to zero
+  if (tid == 0 && atomicAdd(a.exits, 1u) == gridDim.x - 1) {
+    *a.grab = 0;
+    *a.exits = 0;
+  }
+  if (!finisher) return;
+  __syncthreads();
   __threadfence();
   const int free_count = __ldcg(a.free_top);
+  int* pend = reinterpret_cast<int*>(sel_sm);  // [B] rows to compact here, then offsets
+  int* cnt_s = pend + a.B;                     // [B] pages freed per row
   // grants in ascending b while free pages last (as select_grant_kernel);
   // rows that wanted a page and got none are compacted here
-  if (tid == 0) s_carry[2] = 0;  // rows left to compact
+  if (tid == 0) {
+    s_carry[2] = 0;
+    s_carry[3] = 0;
+  }
   __syncthreads();
-  int* pend = reinterpret_cast<int*>(sel_sm);  // [B] rows to compact here
-  {
-    if (tid == 0) s_carry[3] = 0;
-    __syncthreads();
-    for (int base = 0; base < a.B; base += blockDim.x) {
-      const int bb = base + tid;
-      const int w = bb < a.B ? __ldcg(a.wants + bb) : 0;
-      int x = w;
-      for (int o = 1; o < 32; o <<= 1) {
-        const int y = __shfl_up_sync(FULL, x, o);
-        if (lane >= o) x += y;
-      }
-      if (lane == 31) red[warp] = x;
-      __syncthreads();
-      int before = 0;
-      for (int i = 0; i < warp; ++i) before += red[i];
-      const int carry = s_carry[3];
-      const int excl = carry + before + x - w;
-      if (bb < a.B && w) {
-        if (excl < free_count) {
-          a.grow[bb] = 1;
-          a.budget[bb] += 1;
-          const int nb = (int)ceil_div_ll(__ldcg(a.seq_lens + bb), a.ps);
-          uint8_t* keep = a.keep + (size_t)bb * a.max_pages;
-          for (int j = 0; j < nb && j < a.max_pages; ++j) keep[j] = 1;
-        } else {
-          pend[atomicAdd(&s_carry[2], 1)] = bb;
-        }
-      }
-      __syncthreads();
-      if (tid == blockDim.x - 1) s_carry[3] = carry + before + x;
-      __syncthreads();
+  for (int base = 0; base < a.B; base += blockDim.x) {
+    const int bb = base + tid;
+    const int w = bb < a.B ? __ldcg(a.wants + bb) : 0;
+    int x = w;
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(FULL, x, o);
+      if (lane >= o) x += y;
     }
+    if (lane == 31) red[warp] = x;
+    __syncthreads();
+    int before = 0;
+    for (int i = 0; i < warp; ++i) before += red[i];
+    const int carry = s_carry[3];
+    const int excl = carry + before + x - w;
+    if (bb < a.B && w) {
+      if (excl < free_count) {
+        a.grow[bb] = 1;
+        a.budget[bb] += 1;
+        const int nb = (int)ceil_div_ll(__ldcg(a.seq_lens + bb), a.ps);
+        uint8_t* kb = a.keep + (size_t)bb * a.max_pages;
+        for (int j = 0; j < nb && j < a.max_pages; ++j) kb[j] = 1;
+      } else {
+        pend[atomicAdd(&s_carry[2], 1)] = bb;
+      }
+    }
+    __syncthreads();
+    if (tid == blockDim.x - 1) s_carry[3] = carry + before + x;
+    __syncthreads();
   }
   const int npend = s_carry[2];
   for (int i = 0; i < npend; ++i) {
     const int bb = pend[i];
     const int Lb = __ldcg(a.seq_lens + bb);
     int dr = 0;
+    __threadfence();
+    __syncthreads();
     const int K = compact_row_pages(a.table + (size_t)bb * a.max_pages,
                                     a.keep + (size_t)bb * a.max_pages,
                                     (int)ceil_div_ll(Lb, a.ps), Lb, a.ps, a.max_pages,
@@ -1240,16 +1436,14 @@ __global__ void __launch_bounds__(kStepThreads) budget_step_kernel(const StepArg
     __syncthreads();
   }
   // freed pages onto the free list in (b, j) order (no page is popped by a
-  // page-granular compaction)
+  // page-granular compaction); one warp per sequence
   int top = free_count;
   {
-    int* cnt_s = pend + a.B;  // [B] pages freed per row
     if (tid == 0) s_carry[3] = 0;
     __syncthreads();
     for (int base = 0; base < a.B; base += blockDim.x) {
       const int bb = base + tid;
       const int c = bb < a.B ? __ldcg(a.drop_cnt + bb) : 0;
-      if (bb < a.B) cnt_s[bb] = c;
       int x = c;
       for (int o = 1; o < 32; o <<= 1) {
         const int y = __shfl_up_sync(FULL, x, o);
@@ -1260,108 +1454,120 @@ __global__ void __launch_bounds__(kStepThreads) budget_step_kernel(const StepArg
       int before = 0;
       for (int i = 0; i < warp; ++i) before += red[i];
       const int carry = s_carry[3];
-      if (bb < a.B) pend[bb] = carry + before + x - c;  // exclusive offset of b's pushes
+      if (bb < a.B) {
+        pend[bb] = carry + before + x - c;  // exclusive offset of b's pushes
+        cnt_s[bb] = c;
+      }
       __syncthreads();
       if (tid == blockDim.x - 1) s_carry[3] = carry + before + x;
       __syncthreads();
     }
     const int pushes = s_carry[3];
-    for (int bb = 0; bb < a.B; ++bb) {
+    for (int bb = warp; bb < a.B; bb += nw) {
       const int c = cnt_s[bb];
-      for (int r = tid; r < c; r += blockDim.x)
+      for (int r = lane; r < c; r += 32)
         a.free_list[top + pend[bb] + r] = __ldcg(a.drop_ids + (size_t)bb * a.max_pages + r);
     }
     top += pushes;
   }
   __threadfence();
   __syncthreads();
-  // ---- append (as append_plan_kernel + append_copy_kernel, no shared pages)
-  {
+  // ---- append (as append_plan_kernel + append_copy_kernel, no shared pages).
+  // Each sequence's length, its page for the token and the ids to be popped
+  // are read once; sequences are taken blockDim at a time.
+  int2* dest = reinterpret_cast<int2*>(pend);  // [B] (page, slot)
+  if (tid == 0) {
+    s_carry[0] = s_carry[1] = 0;
+    s_carry[3] = 0;
+  }
+  __syncthreads();
+  int my_need = 0;
+  for (int bb = tid; bb < a.B; bb += blockDim.x) {
+    const int Lb = __ldcg(a.new_len + bb);
+    int pg = -1;
+    if (Lb < 0) {
+      s_carry[1] = 1;
+    } else if (Lb % a.ps == 0) {
+      if (Lb / a.ps >= a.max_pages) s_carry[0] = 1;
+      ++my_need;
+    } else {
+      pg = __ldcg(a.table + (size_t)bb * a.max_pages + Lb / a.ps);
+      if (pg < 0 || pg >= a.num_pages) s_carry[1] = 1;
+    }
+    dest[bb] = make_int2(pg, Lb);  // (page or -1 for a pop, length) until the pops are known
+  }
+  const int total = block_sum_int(my_need, red);
+  if (total <= top)
+    for (int i = tid; i < total; i += blockDim.x) {
+      const int p = __ldcg(a.free_list + (top - 1 - i));
+      if (p < 0 || p >= a.num_pages) s_carry[1] = 1;
+    }
+  __syncthreads();
+  const int err = s_carry[0] ? KV_EFULL : (s_carry[1] ? KV_EBADPAGE : (total > top ? KV_ENOSPACE : 0));
+  if (err) {
+    // the compaction stands; the append changes nothing
+    for (int bb = tid; bb < a.B; bb += blockDim.x) a.seq_lens[bb] = dest[bb].y;
     if (tid == 0) {
-      s_carry[0] = s_carry[1] = 0;
-      s_carry[3] = 0;
+      set_status(a.status, err);
+      *a.free_top = top;
+      *a.ctl = 1;
+      *a.ticket = 0;
+    }
+    return;
+  }
+  for (int base = 0; base < a.B; base += blockDim.x) {
+    const int bb = base + tid;
+    const int2 dl = bb < a.B ? dest[bb] : make_int2(0, 1);
+    const int Lb = dl.y;
+    const bool nd = bb < a.B && Lb % a.ps == 0;
+    const unsigned bal = __ballot_sync(FULL, nd);
+    const int x = __popc(bal & ((1u << lane) - 1u));
+    __syncthreads();
+    if (lane == 0) red[warp] = __popc(bal);
+    __syncthreads();
+    int before = 0;
+    for (int i = 0; i < warp; ++i) before += red[i];
+    const int carry = s_carry[3];
+    if (bb < a.B) {
+      int pg = dl.x;
+      if (nd) {
+        pg = __ldcg(a.free_list + (top - 1 - (carry + before + x)));
+        a.table[(size_t)bb * a.max_pages + Lb / a.ps] = pg;
+      }
+      dest[bb] = make_int2(pg, Lb % a.ps);
+      a.seq_lens[bb] = Lb + 1;
     }
     __syncthreads();
-    int my_need = 0;
-    for (int bb = tid; bb < a.B; bb += blockDim.x) {
-      const int Lb = __ldcg(a.new_len + bb);
-      if (Lb < 0) {
-        s_carry[1] = 1;
-      } else if (Lb % a.ps == 0) {
-        if (Lb / a.ps >= a.max_pages) s_carry[0] = 1;
-        ++my_need;
-      } else {
-        const int p = __ldcg(a.table + (size_t)bb * a.max_pages + Lb / a.ps);
-        if (p < 0 || p >= a.num_pages) s_carry[1] = 1;
-      }
-    }
-    const int total = block_sum_int(my_need, red);
-    if (total <= top)
-      for (int i = tid; i < total; i += blockDim.x) {
-        const int p = a.free_list[top - 1 - i];
-        if (p < 0 || p >= a.num_pages) s_carry[1] = 1;
-      }
-    __syncthreads();
-    const int err = s_carry[0] ? KV_EFULL : (s_carry[1] ? KV_EBADPAGE : (total > top ? KV_ENOSPACE : 0));
-    if (err) {
-      // the compaction stands; the append changes nothing
-      for (int bb = tid; bb < a.B; bb += blockDim.x) a.seq_lens[bb] = __ldcg(a.new_len + bb);
-      if (tid == 0) {
-        set_status(a.status, err);
-        *a.free_top = top;
-        *a.ticket = 0;
-      }
-      return;
-    }
-    int2* dest = reinterpret_cast<int2*>(pend);  // [B] (page, slot)
-    for (int base = 0; base < a.B; base += blockDim.x) {
-      const int bb = base + tid;
-      const int Lb = bb < a.B ? __ldcg(a.new_len + bb) : 1;
-      const bool nd = bb < a.B && Lb % a.ps == 0;
-      const unsigned bal = __ballot_sync(FULL, nd);
-      const int x = __popc(bal & ((1u << lane) - 1u));
-      __syncthreads();
-      if (lane == 0) red[warp] = __popc(bal);
-      __syncthreads();
-      int before = 0;
-      for (int i = 0; i < warp; ++i) before += red[i];
-      const int carry = s_carry[3];
-      if (bb < a.B) {
-        int32_t* slot = a.table + (size_t)bb * a.max_pages + Lb / a.ps;
-        int pg = __ldcg(slot);
-        if (nd) {
-          pg = a.free_list[top - 1 - (carry + before + x)];
-          *slot = pg;
-        }
-        dest[bb] = make_int2(pg, Lb % a.ps);
-        a.seq_lens[bb] = Lb + 1;
-      }
-      __syncthreads();
-      if (tid == 0) {
-        int tot = 0;
-        for (int i = 0; i < nw; ++i) tot += red[i];
-        s_carry[3] = carry + tot;
-      }
-      __syncthreads();
-    }
-    // the token's K and V rows (all heads) into place, 16 bytes per thread
-    const size_t row_bytes = (size_t)D * 2;
-    const int vec = (int)(row_bytes / 16);
-    const long long pieces = (long long)a.B * a.Hkv * vec;
-    for (long long i = tid; i < pieces; i += blockDim.x) {
-      const int bb = (int)(i / ((long long)a.Hkv * vec));
-      const int r = (int)(i - (long long)bb * a.Hkv * vec);
-      const int h = r / vec, v = r - h * vec;
-      const int2 dst = dest[bb];
-      const size_t so = ((size_t)bb * a.Hkv + h) * row_bytes + (size_t)v * 16;
-      const size_t dof = (((size_t)dst.x * a.Hkv + h) * a.ps + dst.y) * row_bytes + (size_t)v * 16;
-      *reinterpret_cast<uint4*>(a.k_pool + dof) = *reinterpret_cast<const uint4*>(a.k_new + so);
-      *reinterpret_cast<uint4*>(a.v_pool + dof) = *reinterpret_cast<const uint4*>(a.v_new + so);
-    }
     if (tid == 0) {
-      *a.free_top = top - total;
-      *a.ticket = 0;  // ready for the next call
+      int tot = 0;
+      for (int i = 0; i < nw; ++i) tot += red[i];
+      s_carry[3] = carry + tot;
     }
+    __syncthreads();
+  }
+  // the copies of the token's K and V rows are step_copy_kernel's
+  for (int bb = tid; bb < a.B; bb += blockDim.x) a.dest[bb] = dest[bb];
+  if (tid == 0) {
+    *a.free_top = top - total;
+    *a.ctl = 0;
+    *a.ticket = 0;  // ready for the next call
+  }
+}
+
+// The step's token: K and V rows (all heads) of sequence blockIdx.x into the
+// (page, slot) the fused step planned; nothing when its append failed.
+__global__ void __launch_bounds__(128) step_copy_kernel(const StepArgs a) {
+  if (*a.ctl) return;
+  const int b = blockIdx.x;
+  const int2 dst = a.dest[b];
+  const size_t row_bytes = (size_t)a.d * 2;
+  const int vec = (int)(row_bytes / 16);
+  for (int i = threadIdx.x; i < a.Hkv * vec; i += blockDim.x) {
+    const int h = i / vec, v = i - h * vec;
+    const size_t so = ((size_t)b * a.Hkv + h) * row_bytes + (size_t)v * 16;
+    const size_t dof = (((size_t)dst.x * a.Hkv + h) * a.ps + dst.y) * row_bytes + (size_t)v * 16;
+    *reinterpret_cast<uint4*>(a.k_pool + dof) = *reinterpret_cast<const uint4*>(a.k_new + so);
+    *reinterpret_cast<uint4*>(a.v_pool + dof) = *reinterpret_cast<const uint4*>(a.v_new + so);
   }
 }
 
@@ -1635,7 +1841,7 @@ int kv_compact(int32_t* block_table, int max_pages, int32_t* seq_lens, const uin
 }
 
 struct StepLayout {
-  size_t wants, new_len, drop_cnt, drop_ids, total;
+  size_t wants, new_len, drop_cnt, row_tk, dest, drop_ids, total;
 };
 static StepLayout step_layout(int B, int max_pages) {
   StepLayout L{};
@@ -1644,15 +1850,23 @@ static StepLayout step_layout(int B, int max_pages) {
   L.wants = ws_take(&off, nb * 4);
   L.new_len = ws_take(&off, nb * 4);
   L.drop_cnt = ws_take(&off, nb * 4);
+  L.row_tk = ws_take(&off, nb * 4);
+  L.dest = ws_take(&off, nb * 8);
   L.drop_ids = ws_take(&off, nb * (size_t)(max_pages > 0 ? max_pages : 1) * 4);
   L.total = off;
   return L;
 }
 
 // Dynamic shared memory of budget_step_kernel: the row's EMAs, then the
-// larger of select_row's arrays and the last block's per-row scratch.
+// larger of the selection's arrays (three keys, the sort's index array above
+// 1024 pages, two ranks, the candidate flags) and the last block's per-row
+// scratch.
 static size_t step_smem(int B, int Hkv, int d, int max_pages) {
-  return (size_t)2 * Hkv * d * 4 + std::max(select_smem(max_pages), (size_t)B * 8);
+  size_t p2 = 1;
+  while (p2 < (size_t)max_pages) p2 <<= 1;
+  // packed keys, R, flags, ranks (two), unpacked keys above 1024 pages
+  const size_t sel = (size_t)max_pages * (8 + 4 + 1 + 2 + 2 + 8) + p2 * 2 + 32;
+  return (size_t)2 * Hkv * d * 4 + std::max(align_up(sel, 16), (size_t)B * 8);
 }
 
 size_t kv_budget_step_workspace_size(int B, int max_pages) { return step_layout(B, max_pages).total; }
@@ -1718,13 +1932,28 @@ int kv_budget_step(const void* q, const void* k_new, const void* v_new, void* k_
   a.new_len = reinterpret_cast<int32_t*>(w + L.new_len);
   a.drop_cnt = reinterpret_cast<int32_t*>(w + L.drop_cnt);
   a.drop_ids = reinterpret_cast<int32_t*>(w + L.drop_ids);
+  a.row_tk = reinterpret_cast<int32_t*>(w + L.row_tk);
+  a.dest = reinterpret_cast<int2*>(w + L.dest);
+  a.S = kStepSplit;
   a.ticket = reinterpret_cast<unsigned*>(w + kStepTicketOffset);
+  a.grab = reinterpret_cast<unsigned*>(w + kStepGrabOffset);
+  a.exits = reinterpret_cast<unsigned*>(w + kStepExitOffset);
+  a.ctl = reinterpret_cast<int*>(w + kStepCtlOffset);
   a.status = reinterpret_cast<int*>(w);
   using StepFn = void (*)(const StepArgs);
   StepFn fn = dtype == KV_BF16 ? (d == 128 ? budget_step_kernel<BF16, 4> : budget_step_kernel<BF16, 2>)
                                : (d == 128 ? budget_step_kernel<F16, 4> : budget_step_kernel<F16, 2>);
   KV_CUDA_CHECK(cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem));
-  KV_CUDA_CHECK(launch(fn, dim3(B), dim3(kStepThreads), smem, static_cast<cudaStream_t>(stream),
+  // a resident grid: every block is scheduled at once and takes items
+  // (sequence, split) in turn
+  int sms = 0, per_sm = 0;
+  KV_CUDA_CHECK(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev));
+  KV_CUDA_CHECK(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fn, kStepThreads, smem));
+  if (per_sm < 1) return cuda_failed(cudaErrorInvalidConfiguration, "budget step occupancy");
+  const long long grid = std::min<long long>((long long)B * kStepSplit, (long long)sms * per_sm);
+  KV_CUDA_CHECK(launch(fn, dim3((unsigned)grid), dim3(kStepThreads), smem,
+                       static_cast<cudaStream_t>(stream), false, a));
+  KV_CUDA_CHECK(launch(step_copy_kernel, dim3(B), dim3(128), 0, static_cast<cudaStream_t>(stream),
                        false, a));
   return KV_OK;
 }
