@@ -259,11 +259,13 @@ class BudgetedDecoder:
 
     def step_graphed(self, q, k_new, v_new, between=None):
         """One steady-state step (t > 0) by graph replay on the current
-        stream: copies the token's q/k/v into the static buffers (one fused
-        copy) and replays the step's graph; with `between`, replays the
-        budgeting graph, calls `between()` (e.g. to record an event) and then
-        the decode graph.  Same kernels, order and results as step()."""
-        torch._foreach_copy_([self.q_in, self.k_in, self.v_in], [q, k_new, v_new])
+        stream: copies the token's q/k/v into the static buffers and replays
+        the step's graph; with `between`, replays the budgeting graph, calls
+        `between()` (e.g. to record an event) and then the decode graph.
+        Same kernels, order and results as step()."""
+        self.q_in.copy_(q)
+        self.k_in.copy_(k_new)
+        self.v_in.copy_(v_new)
         if between is None:
             self.g_step.replay()
             return

@@ -7,6 +7,7 @@ same input state: the append bit for bit, the decode within tolerance, on
 both decode engines (the fused kernel and the tensor-core engine the bench's
 policy picks for these lengths)."""
 import os
+from concurrent.futures import ThreadPoolExecutor
 
 import numpy as np
 import pytest
@@ -19,6 +20,13 @@ from tests.gpu_util import DeviceDecode, assert_decode_close, bits_to_dev, i32
 
 pytestmark = pytest.mark.gpu
 NCPU = len(os.sched_getaffinity(0))
+# the oracle's per-row decodes run side by side (the C call releases the GIL)
+_ROWS = ThreadPoolExecutor(max_workers=max(1, min(8, NCPU)))
+
+
+def _decode_rows(y, rows):
+    parts = [f.result() for f in [_ROWS.submit(O.decode_rows, y, [r]) for r in rows]]
+    return np.concatenate([p[0] for p in parts]), np.concatenate([p[1] for p in parts])
 
 
 def _pool_bits(t):
@@ -62,13 +70,22 @@ def test_bucketed_trace(L0, engine):
         page = int(ht[0, L // 16])
         assert np.array_equal(_pool_bits(dd.k[page, :, L % 16]), hk[page, :, L % 16]), t
         assert np.array_equal(_pool_bits(dd.v[page, :, L % 16]), hv[page, :, L % 16]), t
-        # decode over L + 1 tokens
+        # decode over L + 1 tokens: four query heads every step, rotating so
+        # two steps cover all eight KV heads, and all of them every 16 steps
         y = W.DecodeInputs(name=x.name, B=1, Hq=x.Hq, Hkv=x.Hkv, d=x.d, page_size=16,
                            dtype=x.dtype, scale=x.scale, q=q, k_pool=hk, v_pool=hv,
                            block_table=ht, seq_lens=hl)
-        ref_out, ref_lse = O.decode(y, nthreads=NCPU)
-        assert_decode_close(y, dd.out.cpu().numpy().astype(np.float64),
-                            dd.lse.cpu().numpy().astype(np.float64), ref_out, ref_lse)
+        out = dd.out.cpu().numpy().astype(np.float64)
+        lse = dd.lse.cpu().numpy().astype(np.float64)
+        if t % 16 == 15 or t == steps - 1:
+            ref_out, ref_lse = O.decode(y, nthreads=NCPU)
+            assert_decode_close(y, out, lse, ref_out, ref_lse)
+        else:
+            G = x.Hq // x.Hkv
+            kv_heads = range(t % 2, x.Hkv, 2)           # even KV heads, then odd
+            rows = [(0, h * G + (t // 2) % G) for h in kv_heads]
+            ref_out, ref_lse = _decode_rows(y, rows)
+            assert_decode_close(y, out, lse, ref_out, ref_lse, rows=rows)
         page_counts.add(int(-(-(L + 1) // 16)))
     # the whole pools agree at the end (nothing else was written)
     assert np.array_equal(_pool_bits(dd.k), hk) and np.array_equal(_pool_bits(dd.v), hv)
