@@ -1,5 +1,5 @@
 """Benchmark: one paged GQA decode step (per-CTA workqueue + split-KV decode +
-LSE merge, one kernel launch) on the batch-8 bimodal fp16 workload (Hq=32,
+LSE merge, by the engine a calibrated policy picks) on the batch-8 bimodal fp16 workload (Hq=32,
 Hkv=8, d=128, page 16, lengths half U[512, 2048] and half U[16384, 32768],
 pages scattered in a pool of 1.25x the pages used), measured as KV HBM GB/s
 and tokens/s.  The `budget_step` object times the whole budgeted step (query
@@ -11,8 +11,8 @@ batch-64 bf16 workload with per-sequence page budgets.
 
 Prints one JSON line.  `value` is algorithmic bytes (valid K/V tokens + q +
 block-table entries) per step / device time per step, with inputs resident in
-HBM and L2 flushed between steps (a 512 MiB memset, outside the timed
-events).  `e2e` times the host-buffer entry point (q, block table and
+HBM and L2 flushed between steps (a 512 MiB memset, then its first 256 MiB
+read back so the lines left in L2 are clean; both outside the timed events).  `e2e` times the host-buffer entry point (q, block table and
 lengths copied in, out and lse copied back, per step).  `roofline` reports
 the attention kernel alone (events bracket it inside the call) against the
 measured HBM copy bandwidth.  `cpu_baseline` times the CPU oracle on a
@@ -69,8 +69,34 @@ def workload_config(x: W.DecodeInputs, name: str):
             "page_size": x.page_size, "dtype": W.DTYPE_NAMES[x.dtype],
             "seq_lens": [int(v) for v in x.seq_lens], "num_pages": x.num_pages,
             "kv_bytes_per_step": x.kv_bytes(), "algorithmic_bytes_per_step": x.algorithmic_bytes(),
-            "l2": "flushed between steps (512 MiB memset outside the timed events)",
+            "l2": L2_NOTE,
             "parallelism": "replicas (one independent decode per GPU)"}
+
+
+L2_NOTE = ("flushed between steps: a 512 MiB memset, then its first 256 MiB read back, so L2 "
+           "holds clean lines of the flush buffer (none of the inputs, no write-back pending); "
+           "both outside the timed events")
+
+
+class L2Flush:
+    """The L2 flush between timed steps.  A 512 MiB memset alone leaves L2
+    full of the memset's dirty lines, which the next kernel then writes back
+    to HBM while it streams its own inputs; reading back the first half of the
+    buffer (long since pushed out of L2 by the second half) replaces them with
+    clean lines, so the timed step starts as ncu's cache control starts a
+    kernel: no input in L2, no write-back pending.  `write_only` is the
+    memset alone, kept for comparison."""
+
+    def __init__(self, torch, dev, mib=512):
+        self.torch = torch
+        self.buf = torch.empty(mib << 20, dtype=torch.uint8, device=dev)
+        self.half = self.buf[: (mib // 2) << 20].view(torch.float32)
+        self.acc = torch.empty((), dtype=torch.float32, device=dev)
+
+    def __call__(self, write_only=False):
+        self.buf.zero_()
+        if not write_only:
+            self.torch.sum(self.half, dim=0, out=self.acc)
 
 
 class ClockSampler:
@@ -204,7 +230,7 @@ def run_ours(args, x, name, rank, world):
     lens = torch.from_numpy(x.seq_lens).to(dev)
     out = torch.empty((x.B, x.Hq, x.d), dtype=torch.float32, device=dev)
     lse = torch.empty((x.B, x.Hq), dtype=torch.float32, device=dev)
-    flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
+    flush = L2Flush(torch, dev)
 
     # The engine: PersistentKV's adaptive policy among this library's own
     # variants (the fused kernel's split sizes and the tensor-core engine),
@@ -214,7 +240,7 @@ def run_ours(args, x, name, rank, world):
     cands = policy.usable(x.B, x.Hq, x.Hkv, x.d, x.max_pages)
     ws_t = kv.alloc_workspace(policy.workspace_size(x.B, x.Hq, x.Hkv, x.d, x.max_pages), device=dev)
     best, us = kv.kv_decode_tune(q, k, v, table, lens, x.scale, out, lse, ws_t, cands, reps=7,
-                                 flush=flush)
+                                 flush=flush.buf)
     del ws_t
     pps = {"policy": best, "fused": 0, "tensor-core": kv.KV_DECODE_TENSOR_CORE}[args.engine]
     if pps not in cands:
@@ -264,7 +290,7 @@ def run_ours(args, x, name, rank, world):
     def e2e_loop(count):
         t = []
         for _ in range(count):
-            flush.zero_()
+            flush()
             torch.cuda.synchronize()
             t0 = time.perf_counter()
             if hostio():
@@ -280,22 +306,33 @@ def run_ours(args, x, name, rank, world):
     torch.cuda.synchronize()
     with ClockSampler(dev.index if dev.index is not None else 0) as clk:
         # the step as a user runs it: no profiling hooks inside the timed region
-        t_wall0 = time.perf_counter()
+        queue_ahead(torch, n)
         for i in range(n):
-            flush.zero_()
+            flush()
             ev[i][0].record(stream)
             step()
             ev[i][1].record(stream)
         torch.cuda.synchronize()
-        t_wall = time.perf_counter() - t_wall0
         if world > 1:
             dist.barrier()
         torch.cuda.synchronize()
         # the attention kernel alone (events recorded inside the call, around it)
+        queue_ahead(torch, n)
         for i in range(n):
-            flush.zero_()
+            flush()
             kv.kv_profile_next_decode(evk[i][0], evk[i][1])
             step()
+        torch.cuda.synchronize()
+        # the same steps after the memset alone (its dirty lines still in L2),
+        # for comparison with the flush used above
+        evd = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(n)]
+        queue_ahead(torch, n)
+        for i in range(n):
+            flush(write_only=True)
+            evd[i][0].record(stream)
+            step()
+            evd[i][1].record(stream)
         torch.cuda.synchronize()
         # the same end-to-end loop while the clocks are sampled, for reference
         e2e_t = e2e_loop(max(3, n // 2))
@@ -336,7 +373,9 @@ def run_ours(args, x, name, rank, world):
         "tokens_per_s": world * x.B / t_step, "kv_tokens_per_s": world * float(x.seq_lens.sum()) / t_step,
         "pct_of_peak": 100.0 * (nbytes / t_step / 1e9) / peak,
         "pct_of_nominal_peak": 100.0 * (nbytes / t_step / 1e9) / NOMINAL_HBM_GBS,
-        "wall_ms_per_step_incl_flush": t_wall / n * 1e3,
+        "device_ms_per_step_incl_flush": ev[0][0].elapsed_time(ev[-1][1]) / n,
+        "ms_per_step_after_memset_only_flush": statistics.mean(
+            a.elapsed_time(b) for a, b in evd),
         "e2e": {"value": world * nbytes / t_e2e_q / 1e9, "unit": "GB/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": t_e2e_q * 1e3,
                 "ms_per_step_during_clock_sampling": t_e2e * 1e3,
@@ -359,7 +398,7 @@ def run_ours(args, x, name, rank, world):
     }
     line["config"]["engine"] = ("tensor-core engine" if tensor_core else
                                 f"fused decode kernel, pages_per_split={pps} (0 = automatic)")
-    line["policy"] = {"candidates_pages_per_split": cands, "median_us": us, "best": best,
+    line["policy"] = {"candidates_pages_per_split": cands, "us": us, "best": best,
                       "chosen": pps,
                       "note": f"0 = automatic split rule, {kv.KV_DECODE_TENSOR_CORE} = tensor-core "
                               "engine; calibrated once before timing, L2 flushed before every "
@@ -390,6 +429,15 @@ def whole_job_gbs(bytes_per_replica, t_step_max, world):
     """Whole-job throughput: every replica moves bytes_per_replica per step,
     the job's step takes the slowest replica's time."""
     return world * bytes_per_replica / t_step_max / 1e9
+
+
+def queue_ahead(torch, steps, ms_per_step=0.5):
+    """Hold the GPU in a bounded sleep kernel while the host enqueues the
+    timed steps, so that each step's events bracket device work only: a host
+    call delayed past the queued flush would otherwise leave the GPU idle
+    between a step's start event and its first kernel.  The sleep runs before
+    the first start event and is outside every timed interval."""
+    torch.cuda._sleep(int(max(2.0, steps * ms_per_step) * 1e-3 * 2.1e9))
 
 
 def launches_per_step(B, tensor_core=False):
@@ -427,10 +475,10 @@ def measure_budget(dev, peak, peak_kind, steps, warmup):
             for t in range(warmup + steps)]
     q0 = dev_bits(W.step_tokens(c["seed"], 0, x.B, x.Hq, x.Hkv, x.d, x.dtype)[0])
     dec.fit(q0)
-    flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
+    flush = L2Flush(torch, dev)
     stream = torch.cuda.current_stream()
     # the decode engine for this batch, picked as for the decode-only leg
-    engine, engine_us = dec.calibrate(q0, flush=flush)
+    engine, engine_us = dec.calibrate(q0, flush=flush.buf)
     eager_steps = 24
     split_steps = 24  # further graph-replayed steps with the decode timed apart
     gw = 2            # untimed steps that replay each graph once (its first launch uploads it)
@@ -452,9 +500,10 @@ def measure_budget(dev, peak, peak_kind, steps, warmup):
            for _ in range(split_steps)]
     lens_after = []
     torch.cuda.synchronize()
+    queue_ahead(torch, steps)
     for i in range(steps):
         t = warmup + i
-        flush.zero_()
+        flush()
         ev[i][0].record(stream)
         dec.step_graphed(*toks[t])
         ev[i][1].record(stream)
@@ -462,27 +511,33 @@ def measure_budget(dev, peak, peak_kind, steps, warmup):
     torch.cuda.synchronize()
     # the decode part alone, on the following steps (budgeting and decode
     # replayed as two graphs with events between them)
-    split_bytes = []
+    split_lens = []
+    queue_ahead(torch, split_steps)
     for i in range(split_steps):
         t = warmup + steps + i
-        flush.zero_()
+        flush()
         dec.step_graphed(*toks[t], between=evk[i][0].record)
         evk[i][1].record(stream)
-        Lh = dec.lens.cpu().numpy().astype(np.int64)
+        split_lens.append(dec.lens.clone())
+    torch.cuda.synchronize()
+    split_bytes = []
+    for L in split_lens:
+        Lh = L.cpu().numpy().astype(np.int64)
         split_bytes.append(int(Lh.sum()) * 2 * x.Hkv * x.d * 2 + x.B * x.Hq * x.d * 2 +
                            4 * int((-(-Lh // x.page_size)).sum()))
-    torch.cuda.synchronize()
-    # the same step issued call by call (host-bound) on the next steps
-    eager_ms = []
+    # the same step issued call by call from Python on the next steps (the
+    # tokens passed straight to the calls: no copies into static buffers)
+    eva = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(eager_steps)]
+    queue_ahead(torch, eager_steps)
     for i in range(eager_steps):
         t = warmup + steps + split_steps + i
-        flush.zero_()
-        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        a.record(stream)
+        flush()
+        eva[i][0].record(stream)
         dec.step(*toks[t], t)
-        b.record(stream)
-        torch.cuda.synchronize()
-        eager_ms.append(a.elapsed_time(b))
+        eva[i][1].record(stream)
+    torch.cuda.synchronize()
+    eager_ms = [a.elapsed_time(b) for a, b in eva]
     st = [dec.status()]
     if any(st):
         raise SystemExit(f"device error in the budgeted step: {st}")
@@ -501,22 +556,24 @@ def measure_budget(dev, peak, peak_kind, steps, warmup):
         "workload": "budgeted_b64_bf16 (Hq=32, Hkv=8, d=128, L~U[2048,16384], budgets U[32,256])",
         "steps_timed": steps, "warmup_steps": warmup,
         "ms_per_step": t_step / steps * 1e3, "decode_ms_per_step": t_dec / steps * 1e3,
-        "issue": "the step replayed as one CUDA graph; inputs copied into static buffers "
-                 "(one fused copy) inside the timed region; the decode part timed apart on "
-                 f"{split_steps} further steps (two graphs, events between them)",
+        "issue": "the step replayed as one CUDA graph; the token's q, k and v copied into "
+                 "the graph's static buffers (three copies) inside the timed region; the "
+                 f"decode part timed apart on {split_steps} further steps (two graphs, events "
+                 "between them)",
         "budgeting": "one kv_budget_step launch (EMA, marks, summaries, scores, selection, "
                      "grant, compaction, append)" if dec.fused_step else "separate calls",
-        "decode_engine": {"chosen": engine, "median_us": {str(k): v for k, v in engine_us.items()},
+        "decode_engine": {"chosen": engine, "us": {str(k): v for k, v in engine_us.items()},
                           "note": f"{kv.KV_DECODE_TENSOR_CORE} = tensor-core engine, 0 = fused "
                                   "kernel; calibrated on the fitted batch, L2 flushed"},
-        "eager_ms_per_step": statistics.median(eager_ms),
-        "eager_note": f"median of {eager_steps} further steps issued call by call from Python",
+        "eager_ms_per_step": statistics.mean(eager_ms),
+        "eager_note": f"mean of {eager_steps} further steps issued call by call from Python "
+                      "with the tokens passed to the calls directly (no copies)",
         "step_gbs": tot_b / t_step / 1e9, "decode_gbs": dec_b / t_dec / 1e9,
         "decode_frac_of_peak": dec_b / t_dec / 1e9 / peak, "peak_gbs": peak,
         "peak_source": f"MEASURED_PEAKS.json hbm_gbs ({peak_kind})",
         "tokens_per_s": x.B * steps / t_step,
         "resident_kv_bytes_per_step": tot_b / steps,
-        "l2": "flushed between steps (512 MiB memset outside the timed events)",
+        "l2": L2_NOTE,
         "setup_s": setup_s,
     }
 
@@ -542,13 +599,13 @@ def measure_multi(x, dev, peak, T=4, steps=10):
     lse = torch.empty((x.B, T, x.Hq), dtype=torch.float32, device=dev)
     ws = kv.alloc_workspace(kv.kv_attend_multi_workspace_size(x.B, T, x.Hq, x.Hkv, x.d,
                                                               x.max_pages), device=dev)
-    flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
+    flush = L2Flush(torch, dev)
     stream = torch.cuda.current_stream()
     for _ in range(3):
         kv.kv_attend_multi(qm, k, v, table, lens, x.scale, out, lse, ws)
     ms = []
     for _ in range(steps):
-        flush.zero_()
+        flush()
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record(stream)
         kv.kv_attend_multi(qm, k, v, table, lens, x.scale, out, lse, ws)

@@ -179,16 +179,20 @@ int kv_attend_multi(const void *q, const void *k_pool, const void *v_pool, int n
  * variants are the fused kernel's split sizes and the tensor-core engine):
  * runs kv_decode on the given inputs once per candidate pages_per_split
  * (0 = automatic, KV_DECODE_TENSOR_CORE = tensor-core engine) untimed, then `reps` (<= 64)
- * times timed with CUDA events on `stream`, writes the median microseconds
- * per candidate to us[n_candidates] (host) and the fastest candidate to
+ * times timed with CUDA events on `stream`, writes the microseconds per
+ * candidate (mean of the middle half of its sorted times) to
+ * us[n_candidates] (host) and the fastest candidate to
  * *best (host).  Synchronises `stream`; out/lse hold the last call's result.
  * `ws` must be sized for every candidate (kv_decode_workspace_size with the
  * smallest positive candidate covers all positive ones, and the size for
  * KV_DECODE_TENSOR_CORE covers it and the automatic one: pass the larger).
- * `flush` (device, flush_bytes; NULL for none): a buffer larger than the L2
- * cache, overwritten before every timed call (outside the events), so the
- * candidates are timed with the inputs in HBM as a step that follows other
- * work finds them; without it they are timed back to back, warm in L2. */
+ * `flush` (device, flush_bytes; NULL for none): a buffer more than twice the
+ * size of the L2 cache, overwritten and then read back over its first half
+ * before every timed call (outside the events), so the candidates are timed
+ * with their inputs in HBM and with no dirty lines of the flush left in L2 to
+ * write back, as a step that follows ordinary work finds them; without it
+ * they are timed back to back, warm in L2.  The buffer's contents are
+ * scratch. */
 int kv_decode_tune(const void *q, const void *k_pool, const void *v_pool, int num_pages,
                    const int32_t *block_table, int max_pages, const int32_t *seq_lens, int B,
                    int page_size, int Hq, int Hkv, int d, int dtype, float scale,

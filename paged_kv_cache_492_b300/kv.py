@@ -282,8 +282,10 @@ def kv_decode_tune(q, k_pool, v_pool, block_table, seq_lens, scale, out, lse, ws
                    reps=5, stream=None, flush=None):
     """Time kv_decode for each candidate pages_per_split (0 = automatic,
     KV_DECODE_TENSOR_CORE = the tensor-core engine) on these inputs ->
-    (best candidate, [median us per candidate]).  flush: a device buffer
-    larger than L2, overwritten before every timed call (None: timed warm)."""
+    (best candidate, [us per candidate, the mean of the middle half of its
+    reps]).  flush: a device buffer more than twice the L2 size, overwritten
+    and half read back before every timed call so L2 holds none of the inputs
+    and no dirty lines (None: timed warm)."""
     B, Hq, d = q.shape
     P_, Hkv, ps, _ = k_pool.shape
     cand = (C.c_int32 * len(candidates))(*[int(c) for c in candidates])
@@ -309,8 +311,9 @@ class DecodePolicy:
     the first batch with a new signature is timed with kv_decode_tune and the
     fastest variant is reused for every later batch with that signature.  The
     workspace must be sized for every candidate (workspace_size).  With
-    `flush` (a device buffer larger than L2) the candidates are timed with L2
-    flushed before each call, as a step that follows other work runs."""
+    `flush` (a device buffer more than twice the L2 size) the candidates are
+    timed with L2 flushed before each call, as a step that follows other work
+    runs."""
 
     def __init__(self, candidates=(0, 8, 16, 32, 64, 128, KV_DECODE_TENSOR_CORE), reps=5,
                  flush=None):
