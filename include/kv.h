@@ -160,12 +160,14 @@ int kv_decode(const void *q, const void *k_pool, const void *v_pool, int num_pag
  * a query with no token to attend to gets out = 0 and lse = -inf.
  * q [B][T][Hq][d] 16-bit, out [B][T][Hq][d] fp32, lse [B][T][Hq] fp32
  * (device).  Other arguments and errors as kv_decode; the workspace is
- * kv_attend_multi_workspace_size bytes (give it its own).  Where T * G <= 64
- * (d = 128, page_size 16) the tensor-core engine streams each page once for
- * all T tokens (T = 1 is kv_decode's KV_DECODE_TENSOR_CORE engine);
- * otherwise the fused decode kernel runs on B*T causal views of the batch,
- * streaming each page once per query token, and the workspace keeps its
- * merge tickets between calls as kv_decode's does. */
+ * kv_attend_multi_workspace_size bytes (give it its own).  With d = 128 and
+ * page_size 16 (G <= 64) the tensor-core engine serves up to 64 / G tokens
+ * per pass over the pages (T * G <= 64: one pass for all T tokens; T = 1 is
+ * kv_decode's KV_DECODE_TENSOR_CORE engine); larger T runs as
+ * ceil(T * G / 64) consecutive passes over chunks of at most 64 / G tokens
+ * (as even as possible), so each page is streamed that many times.  With d = 64 the fused decode kernel runs on B*T
+ * causal views of the batch, streaming each page once per query token, and
+ * the workspace keeps its merge tickets between calls as kv_decode's does. */
 size_t kv_attend_multi_workspace_size(int B, int T, int Hq, int Hkv, int d, int max_pages,
                                       int page_size, int pages_per_split);
 int kv_attend_multi(const void *q, const void *k_pool, const void *v_pool, int num_pages,

@@ -174,7 +174,7 @@ int engine_launch(const void* q, const void* k_pool, const void* v_pool, int num
   const size_t region = tensor_core_region(B, Hq, Hkv, d, max_pages, page_size);
   if (!region) return KV_EINVAL;
   return mma_attend_launch(q, k_pool, v_pool, num_pages, block_table, max_pages, seq_lens, B, 1,
-                           Hq, Hkv, dtype, scale, 0, out, lse, ws, ws_bytes, region, s);
+                           1, 0, Hq, Hkv, dtype, scale, 0, out, lse, ws, ws_bytes, region, s);
 }
 
 }  // namespace

@@ -73,6 +73,7 @@ constexpr int kFusedMaxB = 1024;
 struct OffsetsArgs {
   const int32_t* seq_lens;
   int B, page_size, max_pages;
+  int len_shift;      // lengths are taken as max(0, L - len_shift) (0: as given)
   int32_t* page_off;  // [B + 1]
   int* status;
 };
@@ -104,14 +105,20 @@ int decode_num_workers(int Hq, int Hkv, int d, int page_size, int dtype);
 // kernel.  Its scratch starts `region` bytes into the workspace (the status
 // word stays at the workspace's start), so it can share a workspace with
 // the decode kernel's merge tickets.
+// Query tokens per pass of the tensor-core kernel (T * G <= 64 rows per KV
+// head); 0 where the kernel does not apply.
+int mma_attend_max_tokens(int Hq, int Hkv, int d);
 bool mma_attend_supported(int Hq, int Hkv, int d, int Tq);
 size_t mma_attend_workspace_size(int B, int Hkv, int rows, int max_pages, int pages_per_split,
                                  size_t region);
+// q, out and lse hold Tstride query tokens per sequence; this call serves Tq
+// of them (from row 0 of the pointers passed), which see max(0, L - len_shift)
+// cached tokens causally (decode: Tq = Tstride = 1, len_shift = 0).
 int mma_attend_launch(const void* q, const void* k_pool, const void* v_pool, int num_pages,
                       const int32_t* block_table, int max_pages, const int32_t* seq_lens, int B,
-                      int Tq, int Hq, int Hkv, int dtype, float scale, int pages_per_split,
-                      float* out, float* lse, void* ws, size_t ws_bytes, size_t region,
-                      cudaStream_t stream);
+                      int Tq, int Tstride, int len_shift, int Hq, int Hkv, int dtype,
+                      float scale, int pages_per_split, float* out, float* lse, void* ws,
+                      size_t ws_bytes, size_t region, cudaStream_t stream);
 
 // One-shot profiling events for the next decode on this host thread.
 void set_profile_events(cudaEvent_t before, cudaEvent_t after);

@@ -58,18 +58,20 @@ static_assert((kAbortWord + 1) * 8 <= kBarBytes, "barrier area");
 constexpr unsigned FULLM = 0xffffffffu;
 
 struct MmaParams {
-  const uint16_t* q;          // [B][Tq][Hq][128]
+  const uint16_t* q;          // [B][Tstride][Hq][128], this call's first token at row 0
   const int32_t* table;
   const int32_t* seq_lens;
   const int32_t* page_off_in; // [B + 1] page offsets (large batches), else null
   int32_t* page_off_out;      // [B + 1] written by CTA 0 for the merge (small batches)
   int32_t* chunk_out;         // [1] the chunk size, written by CTA 0
-  float* out;                 // [B][Tq][Hq][128]
-  float* lse;                 // [B][Tq][Hq]
+  float* out;                 // [B][Tstride][Hq][128], as q
+  float* lse;                 // [B][Tstride][Hq]
   float* part_o;              // [slot][Hkv][16][128]
   float* part_lse;            // [slot][Hkv][16]
   int* status;
   int B, num_pages, max_pages, Hq, Hkv, G, Tq, rows, rows_pad, rb, hb, nhb, chunk_req, stages;
+  int Tstride;                // query tokens per sequence in q/out/lse (>= Tq)
+  int len_shift;              // this call's tokens see max(0, L - len_shift) cached tokens
   long long n_chunks;         // chunks of the automatic split (CTAs per head block)
   float scale_log2;
   unsigned long long test_wait_ns;  // > 0: failure-path test mode (see test_consumer_wait_ns)
@@ -133,6 +135,12 @@ __device__ __forceinline__ void tma_load_5d(uint32_t dst, const void* tmap, int 
       : "memory");
 }
 
+// The cached tokens a call's queries see: max(0, L - shift); a negative
+// length stays negative, so it is still reported.
+__device__ __forceinline__ int shifted_len(int L, int shift) {
+  return L < 0 ? L : max(0, L - shift);
+}
+
 // Stage layout: K then V; each is [channel half][head of the block][token]
 // rows of 128 bytes (64 channels), i.e. a (half, head) sub-tile of 2 KiB.
 // The 128-byte swizzle stores logical 16-byte chunk c of a row at chunk
@@ -187,7 +195,7 @@ __global__ void __launch_bounds__(32 * (1 + kMaxHeadBlock), 1)
     long long mine = 0;
     bool bad = false;
     for (int b = b0; b < b1; ++b) {
-      const int L = __ldg(p.seq_lens + b);
+      const int L = shifted_len(__ldg(p.seq_lens + b), p.len_shift);
       const long long np = L > 0 ? ceil_div_ll(L, 16) : 0;
       if (L < 0 || np > p.max_pages) bad = true; else mine += np;
     }
@@ -196,7 +204,7 @@ __global__ void __launch_bounds__(32 * (1 + kMaxHeadBlock), 1)
     const long long W = block_exclusive_scan(mine, &off, s_scan);  // <= B * max_pages < 2^31
     for (int b = b0; b < b1; ++b) {
       s_off[b] = (int32_t)off;
-      const int L = __ldg(p.seq_lens + b);
+      const int L = shifted_len(__ldg(p.seq_lens + b), p.len_shift);
       const long long np = L > 0 ? ceil_div_ll(L, 16) : 0;
       if (L >= 0 && np <= p.max_pages) off += np;
     }
@@ -302,13 +310,13 @@ __global__ void __launch_bounds__(32 * (1 + kMaxHeadBlock), 1)
     const int p0 = (int)lo, p1 = (int)hi;
     const bool single = split_count(Ob, np, chunk) == 1;
     const long long slot_id = 2ll * c + (c == Ob / chunk ? 1 : 0);
-    const int L = __ldg(p.seq_lens + b);
+    const int L = shifted_len(__ldg(p.seq_lens + b), p.len_shift);
 
     // Q fragments; row r = i * G + g is query token i, head h * G + g
     auto qrow = [&](int r) -> const uint16_t* {
       if (r >= p.rows) return nullptr;
       const int i = r / p.G, g = r - (r / p.G) * p.G;
-      return p.q + (((size_t)b * p.Tq + i) * p.Hq + (size_t)h * p.G + g) * kMmaD;
+      return p.q + (((size_t)b * p.Tstride + i) * p.Hq + (size_t)h * p.G + g) * kMmaD;
     };
     const uint16_t* q0 = qrow(qr0);
     const uint16_t* q1 = qrow(qr1);
@@ -437,7 +445,7 @@ __global__ void __launch_bounds__(32 * (1 + kMaxHeadBlock), 1)
     auto dst_row = [&](int r, float** o_ptr, float** l_ptr) {
       if (single) {
         const int i = r / p.G, g = r - (r / p.G) * p.G;
-        const size_t row = ((size_t)b * p.Tq + i) * p.Hq + (size_t)h * p.G + g;
+        const size_t row = ((size_t)b * p.Tstride + i) * p.Hq + (size_t)h * p.G + g;
         *o_ptr = p.out + row * kMmaD;
         *l_ptr = p.lse + row;
       } else {
@@ -484,7 +492,7 @@ struct MmaMergeParams {
   const float* part_lse;
   float* out;
   float* lse;
-  int B, Hq, Hkv, G, Tq, rows, rows_pad;
+  int B, Hq, Hkv, G, Tstride, rows, rows_pad;
 };
 
 template <int kMergeWarps>
@@ -498,7 +506,7 @@ __global__ void __launch_bounds__(kMergeWarps * 32) mma_merge_kernel(const MmaMe
   const long long ns = split_count(Ob, np, chunk);
   if (ns == 1 || r >= p.rows) return;
   const int i = r / p.G, g = r - (r / p.G) * p.G;
-  const size_t row = ((size_t)b * p.Tq + i) * p.Hq + (size_t)h * p.G + g;
+  const size_t row = ((size_t)b * p.Tstride + i) * p.Hq + (size_t)h * p.G + g;
   if (ns == 0) {
     if (threadIdx.x < kMmaD) p.out[row * kMmaD + threadIdx.x] = 0.f;
     if (threadIdx.x == 0) p.lse[row] = -INFINITY;
@@ -751,6 +759,11 @@ int mma_chunks(int Hkv, int rows, long long* out) {
 
 }  // namespace
 
+int mma_attend_max_tokens(int Hq, int Hkv, int d) {
+  if (d != kMmaD || Hkv <= 0 || Hq <= 0 || Hq % Hkv) return 0;
+  return kMmaRows * kMaxRowBlocks / (Hq / Hkv);  // 0 when G > 64
+}
+
 bool mma_attend_supported(int Hq, int Hkv, int d, int Tq) {
   return d == kMmaD && Hkv > 0 && Hq % Hkv == 0 && Tq >= 1 &&
          (long long)(Hq / Hkv) * Tq <= (long long)kMmaRows * kMaxRowBlocks;
@@ -767,11 +780,12 @@ size_t mma_attend_workspace_size(int B, int Hkv, int rows, int max_pages, int pa
 
 int mma_attend_launch(const void* q, const void* k_pool, const void* v_pool, int num_pages,
                       const int32_t* block_table, int max_pages, const int32_t* seq_lens, int B,
-                      int Tq, int Hq, int Hkv, int dtype, float scale, int pages_per_split,
-                      float* out, float* lse, void* ws, size_t ws_bytes, size_t region,
-                      cudaStream_t stream) {
+                      int Tq, int Tstride, int len_shift, int Hq, int Hkv, int dtype,
+                      float scale, int pages_per_split, float* out, float* lse, void* ws,
+                      size_t ws_bytes, size_t region, cudaStream_t stream) {
   if (!mma_attend_supported(Hq, Hkv, kMmaD, Tq) || (dtype != KV_F16 && dtype != KV_BF16))
     return KV_EINVAL;
+  if (Tstride < Tq || len_shift < 0) return KV_EINVAL;
   if (B < 0 || num_pages < 1 || max_pages < 0 || pages_per_split < 0) return KV_EINVAL;
   if (B == 0) return KV_OK;
   if ((long long)B * max_pages > 0x7fffffffll) return KV_EINVAL;  // page offsets are int32
@@ -804,6 +818,7 @@ int mma_attend_launch(const void* q, const void* k_pool, const void* v_pool, int
     oa.B = B;
     oa.page_size = 16;
     oa.max_pages = max_pages;
+    oa.len_shift = len_shift;
     oa.page_off = page_off;
     oa.status = status;
     KV_CUDA_CHECK(launch_page_offsets(oa, stream));
@@ -828,6 +843,8 @@ int mma_attend_launch(const void* q, const void* k_pool, const void* v_pool, int
   mp.Hkv = Hkv;
   mp.G = Hq / Hkv;
   mp.Tq = Tq;
+  mp.Tstride = Tstride;
+  mp.len_shift = len_shift;
   mp.rows = rows;
   mp.rows_pad = rb * kMmaRows;
   mp.stages = ring_stages(hb);
@@ -863,7 +880,7 @@ int mma_attend_launch(const void* q, const void* k_pool, const void* v_pool, int
   gp.Hq = Hq;
   gp.Hkv = Hkv;
   gp.G = mp.G;
-  gp.Tq = Tq;
+  gp.Tstride = Tstride;
   gp.rows = mp.rows;
   gp.rows_pad = mp.rows_pad;
   const dim3 mgrid((unsigned)((long long)B * Hkv), (unsigned)mp.rows);

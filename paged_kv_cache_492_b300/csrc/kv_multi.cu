@@ -4,12 +4,17 @@
 // sequence b are its last T cached tokens (their K/V already appended), and
 // query i attends causally to tokens [0, L_b - T + 1 + i).
 //
-// Two forms.  Where T * G <= 64 rows per KV head (d = 128, page size 16),
-// the tensor-core kernel (kv_mma.cu) streams each page once for all T
-// tokens.  Otherwise the decode kernel runs unchanged on
-// B*T virtual sequences: virtual sequence b*T + i has length
-// max(0, L_b - T + 1 + i), reads block-table row b, query row q[b][i] and
-// output row out[b][i], so each page is streamed once per query token.
+// Two forms.  With d = 128 and page size 16 the tensor-core kernel
+// (kv_mma.cu) takes up to 64 rows per KV head (T * G) in one pass over the
+// pages; more query tokens are served in ceil(T * G / 64) passes over chunks
+// of at most 64 / G tokens, as even as possible (chunk [t0, t0 + Tc) sees
+// L_b - (T - t0 - Tc) cached tokens, and the usual causal rule within the
+// chunk then gives every token its own limit), so each page is streamed
+// ceil(T * G / 64) times.  Otherwise (d = 64) the
+// decode kernel runs unchanged on B*T virtual sequences: virtual sequence
+// b*T + i has length max(0, L_b - T + 1 + i), reads block-table row b, query
+// row q[b][i] and output row out[b][i], so each page is streamed once per
+// query token.
 #include "kv_internal.h"
 
 namespace kvb {
@@ -35,10 +40,12 @@ __global__ void multi_lens_kernel(const MultiLensArgs a) {
 
 size_t lens_offset(size_t decode_bytes) { return align_up(decode_bytes, 256); }
 
-// The tensor-core form wherever it applies: it streams each page once for
-// all T tokens, and at T = 1 it is the tensor-core decode engine.
-bool use_mma(int page_size, int Hq, int Hkv, int d, int T) {
-  return page_size == 16 && mma_attend_supported(Hq, Hkv, d, T);
+// The tensor-core form wherever it applies (at T = 1 it is the tensor-core
+// decode engine); tokens per pass: as many as fit in 64 rows per KV head.
+int mma_chunk_tokens(int page_size, int Hq, int Hkv, int d, int T) {
+  if (page_size != 16) return 0;
+  const int most = mma_attend_max_tokens(Hq, Hkv, d);
+  return most < T ? most : T;
 }
 
 }  // namespace
@@ -51,8 +58,8 @@ extern "C" {
 size_t kv_attend_multi_workspace_size(int B, int T, int Hq, int Hkv, int d, int max_pages,
                                       int page_size, int pages_per_split) {
   if (B < 0 || T < 1) return 0;
-  if (use_mma(page_size, Hq, Hkv, d, T))
-    return mma_attend_workspace_size(B, Hkv, (Hq / Hkv) * T, max_pages, pages_per_split,
+  if (const int tc = mma_chunk_tokens(page_size, Hq, Hkv, d, T))
+    return mma_attend_workspace_size(B, Hkv, (Hq / Hkv) * tc, max_pages, pages_per_split,
                                      kHeaderBytes);
   const size_t base = kv_decode_workspace_size(B * T, Hq, Hkv, d, max_pages, page_size,
                                                pages_per_split);
@@ -69,10 +76,21 @@ int kv_attend_multi(const void* q, const void* k_pool, const void* v_pool, int n
   if (B == 0) return KV_OK;
   if (!seq_lens || !ws) return KV_EINVAL;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  if (use_mma(page_size, Hq, Hkv, d, T)) {
-    return mma_attend_launch(q, k_pool, v_pool, num_pages, block_table, max_pages, seq_lens, B, T,
-                             Hq, Hkv, dtype, scale, pages_per_split, out, lse, ws, ws_bytes,
-                             kHeaderBytes, s);
+  if (const int tc = mma_chunk_tokens(page_size, Hq, Hkv, d, T)) {
+    // the fewest passes of at most tc tokens, as even as possible (a pass's
+    // time grows with its rows), in order on the stream (one workspace)
+    const int passes = (T + tc - 1) / tc, per = (T + passes - 1) / passes;
+    const size_t qrow = (size_t)Hq * d * 2;  // bytes of one query token's heads
+    for (int t0 = 0; t0 < T; t0 += per) {
+      const int n = T - t0 < per ? T - t0 : per;
+      const int rc = mma_attend_launch(
+          q ? static_cast<const uint8_t*>(q) + (size_t)t0 * qrow : nullptr, k_pool, v_pool,
+          num_pages, block_table, max_pages, seq_lens, B, n, T, T - t0 - n, Hq, Hkv, dtype, scale,
+          pages_per_split, out ? out + (size_t)t0 * Hq * d : nullptr, lse ? lse + (size_t)t0 * Hq : nullptr,
+          ws, ws_bytes, kHeaderBytes, s);
+      if (rc) return rc;
+    }
+    return KV_OK;
   }
   const size_t base = kv_decode_workspace_size(B * T, Hq, Hkv, d, max_pages, page_size,
                                                pages_per_split);

@@ -156,8 +156,9 @@ __global__ void __launch_bounds__(kWqThreads, 1) build_workqueue_kernel(Workqueu
 
 // Page offsets of the batch for decode calls too large to compute them in
 // every decode CTA: page_off[b] = sum of ceil(L_b' / page_size) over b' < b,
-// page_off[B] = total.  Invalid lengths count as 0 pages and set KV_EINVAL;
-// a total beyond int32 sets KV_EINVAL and yields an empty batch.
+// page_off[B] = total, with L = max(0, seq_lens[b] - len_shift).  Invalid
+// lengths count as 0 pages and set KV_EINVAL; a total beyond int32 sets
+// KV_EINVAL and yields an empty batch.
 __global__ void __launch_bounds__(kWqThreads, 1) page_offsets_kernel(const OffsetsArgs a) {
   __shared__ long long sm[32];
   pdl_wait();  // seq_lens may come from the previous kernel on the stream
@@ -167,8 +168,12 @@ __global__ void __launch_bounds__(kWqThreads, 1) page_offsets_kernel(const Offse
   const int b0 = min(a.B, tid * per), b1 = min(a.B, b0 + per);
   long long mine = 0;
   bool bad = false;
-  for (int b = b0; b < b1; ++b) {
+  auto len = [&](int b) {
     const int L = a.seq_lens[b];
+    return L < 0 ? L : max(0, L - a.len_shift);  // a negative length stays negative
+  };
+  for (int b = b0; b < b1; ++b) {
+    const int L = len(b);
     long long np = L > 0 ? ceil_div_ll(L, a.page_size) : 0;
     if (L < 0 || np > a.max_pages) {
       bad = true;
@@ -183,7 +188,7 @@ __global__ void __launch_bounds__(kWqThreads, 1) page_offsets_kernel(const Offse
   if (overflow && tid == 0) set_status(a.status, KV_EINVAL);
   for (int b = b0; b < b1; ++b) {
     a.page_off[b] = overflow ? 0 : (int32_t)off;
-    const int L = a.seq_lens[b];
+    const int L = len(b);
     const long long np = L > 0 ? ceil_div_ll(L, a.page_size) : 0;
     if (L >= 0 && np <= a.max_pages) off += np;
   }

@@ -40,8 +40,8 @@ def _check(x, T, out, lse, ref_out, ref_lse):
             assert np.abs(lse[b, i] - ref_lse[b, i]).max() <= 1e-3, (b, i)
 
 
-# T * G <= 64 (d = 128) runs on the tensor-core kernel (one consumer warp per
-# 16 rows); the rest on the decode kernel over causal views.
+# d = 128 runs on the tensor-core kernel (one consumer warp per 16 rows), in
+# the fewest even passes of at most 64 / G tokens where T * G > 64.
 @pytest.mark.parametrize("T,dtype,G,lens,pps", [
     (4, W.F16, 4, [3000, 17, 0, 2, 900], 0),
     (4, W.BF16, 4, [2500, 3, 0, 16, 48, 4100], 0),
@@ -58,7 +58,12 @@ def _check(x, T, out, lse, ref_out, ref_lse):
     (8, W.BF16, 8, [1800, 30], 5),              # 64 rows, bf16, fixed splits
     (12, W.BF16, 2, [64, 2000], 0),             # 24 rows
     (12, W.F16, 4, [900, 11, 2600], 0),         # 48 rows: three row blocks
-    (16, W.F16, 8, [1200, 20], 0),              # 128 rows: causal views
+    (16, W.F16, 8, [1200, 20], 0),              # 128 rows: two passes of 8 tokens
+    (20, W.F16, 4, [1500, 7, 0, 300], 0),       # 80 rows: passes of 10 + 10 tokens
+    (33, W.BF16, 2, [900, 40, 2, 33], 0),       # 66 rows: 17 + 16 tokens; L < T rows
+    (70, W.F16, 1, [500, 69, 71, 64], 0),       # G = 1: 35 + 35 tokens
+    (24, W.BF16, 8, [2000, 10, 25], 3),         # 192 rows: three passes, fixed splits
+    (40, W.F16, 4, [4000, 1, 39, 41], 1),       # 160 rows, one-page splits
     (1, W.F16, 4, [20000, 40, 0], 1),           # 1250 one-page splits: groups of 36
     (4, W.BF16, 4, [17000, 3], 2),              # 532 splits x 16 rows: groups of 24
 ])
@@ -95,3 +100,40 @@ def test_attend_multi_t1_matches_decode():
         assert np.abs(lse[b, 0] - l[b]).max() <= 1e-3
     ref_out, ref_lse = O.attend_multi(x, x.q[:, None], nthreads=NCPU)
     _check(x, 1, out, lse, ref_out, ref_lse)
+
+
+def _rows_of(x, rows):
+    """The batch restricted to `rows` (same pools), for oracle samples."""
+    rows = np.asarray(rows)
+    return W.DecodeInputs(**{**x.__dict__, "B": len(rows), "q": x.q[rows],
+                             "block_table": np.ascontiguousarray(x.block_table[rows]),
+                             "seq_lens": np.ascontiguousarray(x.seq_lens[rows])})
+
+
+def test_attend_multi_large_batch_passes():
+    """Above 1024 sequences the page offsets come from a separate pass, which
+    takes each pass's shortened lengths: 1100 sequences, T = 20 (80 rows per
+    KV head: two passes of 10 tokens), lengths from 0 to 60 (many below T)."""
+    rng = np.random.default_rng(61)
+    lens = rng.integers(0, 61, size=1100).astype(np.int32)
+    x = W.small_decode(61, 1100, 32, 8, 128, lens.tolist(), dtype=W.F16)
+    T = 20
+    qm = W.normal_bits(rng, (x.B, T, x.Hq, x.d), x.dtype)
+    out, lse = _run(x, qm, T)
+    ref_out, ref_lse = O.attend_multi(x, qm, nthreads=NCPU)
+    _check(x, T, out, lse, ref_out, ref_lse)
+
+
+def test_attend_multi_bimodal_t32_sampled():
+    """32 query tokens per sequence on the batch-8 bimodal fp16 workload (128
+    rows per KV head: two passes of 16 tokens), checked against the oracle on
+    three of the sequences (a long one, a short one, and the longest)."""
+    x = W.bimodal()
+    T = 32
+    rng = np.random.default_rng(32)
+    qm = W.normal_bits(rng, (x.B, T, x.Hq, x.d), x.dtype)
+    out, lse = _run(x, qm, T)
+    rows = [int(np.argmax(x.seq_lens)), int(np.argmin(x.seq_lens)), 1]
+    y = _rows_of(x, rows)
+    ref_out, ref_lse = O.attend_multi(y, qm[rows], nthreads=NCPU)
+    _check(y, T, out[rows], lse[rows], ref_out, ref_lse)
