@@ -982,7 +982,8 @@ struct StepArgs {
   int32_t* free_top;
   // workspace
   int32_t* wants;     // [B]
-  int32_t* new_len;   // [B] length after compaction (before the append)
+  int32_t* new_len;   // [B] length after compaction, then the final length (step_copy_kernel
+                      // stores it in seq_lens, which stays as the step found it until then)
   int32_t* drop_cnt;  // [B] pages freed by the compaction
   int32_t* drop_ids;  // [B][max_pages] their ids, in j order
   int32_t* row_tk;    // [B] per-sequence tickets; zero between calls
@@ -996,6 +997,7 @@ struct StepArgs {
 
 constexpr int kStepThreads = 512;
 constexpr int kStepSplit = 16;             // blocks per sequence at a boundary
+constexpr int kStepListMax = 2048;         // sequences the step lists in shared memory
 constexpr size_t kStepTicketOffset = 64;  // bytes into the status header: ticket,
 constexpr size_t kStepGrabOffset = 68;    // item counter,
 constexpr size_t kStepExitOffset = 72;    // exit counter,
@@ -1203,24 +1205,67 @@ __global__ void __launch_bounds__(kStepThreads, 1) budget_step_kernel(const Step
   const uint16_t* k16 = reinterpret_cast<const uint16_t*>(a.k_pool);
   bool finisher = false;  // this block finishes the step (the last sequence to arrive)
   __shared__ unsigned s_item;
+  __shared__ int s_rows[kStepListMax];  // the sequences at a boundary, ascending
+  __shared__ int s_nsc;
 
-  // items (sequence b, split s), split-major (every sequence's first item,
-  // then every second one, ...), taken one at a time by whichever block is
-  // free (a counter; blocks never wait on one another)
-  const unsigned n_items = (unsigned)a.B * (unsigned)a.S;
+  // Work items: (sequence b, split s).  A sequence at a capacity boundary
+  // (scored) has S items, any other one item.  Every block lists the scored
+  // sequences from the lengths (which no block changes during this kernel:
+  // the final lengths go to new_len), so the items can be numbered densely:
+  // first the scored sequences' S splits, split-major, then one item per
+  // sequence in b order (scored ones skip it).  Above kStepListMax sequences
+  // the items are all B x S pairs, split-major, the unscored ones skipped.
+  // Blocks take items one at a time from a counter and never wait on one
+  // another.
+  auto is_scored = [&](int b) {  // as mark_kernel, mode 1, within the table
+    const int L = a.seq_lens[b];
+    return L > 0 && L % a.ps == 0 && L / a.ps >= a.budget[b] &&
+           ceil_div_ll(L, a.ps) <= a.max_pages;
+  };
+  const bool listed = a.B <= kStepListMax;
+  if (tid == 0) s_nsc = 0;
+  __syncthreads();
+  if (listed)
+    for (int base = 0; base < a.B; base += blockDim.x) {
+      const int bb = base + tid;
+      const bool sc = bb < a.B && is_scored(bb);
+      const unsigned bal = __ballot_sync(FULL, sc);
+      if (lane == 0) red[warp] = __popc(bal);
+      __syncthreads();
+      int before = s_nsc;
+      for (int i = 0; i < warp; ++i) before += red[i];
+      if (sc) s_rows[before + __popc(bal & ((1u << lane) - 1u))] = bb;
+      __syncthreads();
+      if (tid == 0)
+        for (int i = 0; i < nw; ++i) s_nsc += red[i];
+      __syncthreads();
+    }
+  const int nsc = s_nsc;
+  const unsigned n_items = listed ? (unsigned)(nsc * a.S + a.B) : (unsigned)a.B * (unsigned)a.S;
   for (;;) {
   __syncthreads();  // the previous item's use of shared memory is over
   if (tid == 0) s_item = atomicAdd(a.grab, 1u);
   __syncthreads();
   const unsigned item = s_item;
   if (item >= n_items) break;
-  const int s = (int)(item / a.B), b = (int)(item - (item / a.B) * a.B);
+  int s, b;
+  if (!listed) {
+    s = (int)(item / a.B);
+    b = (int)(item - (item / a.B) * a.B);
+  } else if (item < (unsigned)(nsc * a.S)) {
+    s = (int)(item / nsc);
+    b = s_rows[item - (unsigned)s * nsc];
+  } else {
+    s = 0;
+    b = (int)(item - (unsigned)(nsc * a.S));
+  }
   // ---- capacity boundary (as mark_kernel, mode 1)
   const int L = a.seq_lens[b];
   const bool act = L > 0 && L % a.ps == 0 && L / a.ps >= a.budget[b];
   const int n = (int)ceil_div_ll(L, a.ps);
   const bool scoring = act && n <= a.max_pages;
   if (!scoring && s != 0) continue;  // one item for a sequence that is not scored
+  if (listed && scoring && item >= (unsigned)(nsc * a.S)) continue;  // its items came first
   // ---- query EMAs of b (as ema_kernel, first = 0), into shared memory; the
   // row's last block writes them out once every block has read the old ones
   for (int i = tid; i < a.Hkv * D; i += blockDim.x) {
@@ -1505,8 +1550,8 @@ __global__ void __launch_bounds__(kStepThreads, 1) budget_step_kernel(const Step
   __syncthreads();
   const int err = s_carry[0] ? KV_EFULL : (s_carry[1] ? KV_EBADPAGE : (total > top ? KV_ENOSPACE : 0));
   if (err) {
-    // the compaction stands; the append changes nothing
-    for (int bb = tid; bb < a.B; bb += blockDim.x) a.seq_lens[bb] = dest[bb].y;
+    // the compaction stands (new_len holds its lengths); the append changes
+    // nothing
     if (tid == 0) {
       set_status(a.status, err);
       *a.free_top = top;
@@ -1535,7 +1580,7 @@ __global__ void __launch_bounds__(kStepThreads, 1) budget_step_kernel(const Step
         a.table[(size_t)bb * a.max_pages + Lb / a.ps] = pg;
       }
       dest[bb] = make_int2(pg, Lb % a.ps);
-      a.seq_lens[bb] = Lb + 1;
+      a.new_len[bb] = Lb + 1;  // the final length (all of new_len was read above)
     }
     __syncthreads();
     if (tid == 0) {
@@ -1555,10 +1600,12 @@ __global__ void __launch_bounds__(kStepThreads, 1) budget_step_kernel(const Step
 }
 
 // The step's token: K and V rows (all heads) of sequence blockIdx.x into the
-// (page, slot) the fused step planned; nothing when its append failed.
+// (page, slot) the fused step planned (nothing when its append failed), and
+// the sequence's final length into seq_lens.
 __global__ void __launch_bounds__(128) step_copy_kernel(const StepArgs a) {
-  if (*a.ctl) return;
   const int b = blockIdx.x;
+  if (threadIdx.x == 0) a.seq_lens[b] = a.new_len[b];
+  if (*a.ctl) return;
   const int2 dst = a.dest[b];
   const size_t row_bytes = (size_t)a.d * 2;
   const int vec = (int)(row_bytes / 16);
@@ -1894,7 +1941,6 @@ int kv_budget_step(const void* q, const void* k_new, const void* v_new, void* k_
   int dev = 0, optin = 0;
   KV_CUDA_CHECK(cudaGetDevice(&dev));
   KV_CUDA_CHECK(cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev));
-  if (smem + 1024 > (size_t)optin) return KV_EINVAL;
   uint8_t* w = static_cast<uint8_t*>(ws);
   StepArgs a{};
   a.q = static_cast<const uint16_t*>(q);
@@ -1943,6 +1989,9 @@ int kv_budget_step(const void* q, const void* k_new, const void* v_new, void* k_
   using StepFn = void (*)(const StepArgs);
   StepFn fn = dtype == KV_BF16 ? (d == 128 ? budget_step_kernel<BF16, 4> : budget_step_kernel<BF16, 2>)
                                : (d == 128 ? budget_step_kernel<F16, 4> : budget_step_kernel<F16, 2>);
+  cudaFuncAttributes fa{};
+  KV_CUDA_CHECK(cudaFuncGetAttributes(&fa, fn));
+  if (smem + fa.sharedSizeBytes > (size_t)optin) return KV_EINVAL;  // rows too wide for one block
   KV_CUDA_CHECK(cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem));
   // a resident grid: every block is scheduled at once and takes items
   // (sequence, split) in turn
