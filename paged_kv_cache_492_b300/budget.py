@@ -238,9 +238,13 @@ class BudgetedDecoder:
         B, Hq, Hkv, d = self.B, self.Hq, self.Hkv, self.d
         dt = self.k_pool.dtype
         dev = self.k_pool.device
-        self.q_in = torch.zeros((B, Hq, d), dtype=dt, device=dev)
-        self.k_in = torch.zeros((B, Hkv, d), dtype=dt, device=dev)
-        self.v_in = torch.zeros((B, Hkv, d), dtype=dt, device=dev)
+        # q, k and v of the step's token: views of one buffer, so a token packed
+        # the same way (pack_token) arrives in one copy
+        nq, nk = B * Hq * d, B * Hkv * d
+        self.tok_in = torch.zeros(nq + 2 * nk, dtype=dt, device=dev)
+        self.q_in = self.tok_in[:nq].view(B, Hq, d)
+        self.k_in = self.tok_in[nq:nq + nk].view(B, Hkv, d)
+        self.v_in = self.tok_in[nq + nk:].view(B, Hkv, d)
         saved = self.stream
         side = torch.cuda.Stream(device=dev)
         self.g_budget, self.g_decode = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
@@ -266,6 +270,22 @@ class BudgetedDecoder:
         self.q_in.copy_(q)
         self.k_in.copy_(k_new)
         self.v_in.copy_(v_new)
+        self._replay(between)
+
+    @staticmethod
+    def pack_token(q, k_new, v_new):
+        """The step's q, k and v in the layout of the graphs' input buffer."""
+        import torch
+
+        return torch.cat([q.reshape(-1), k_new.reshape(-1), v_new.reshape(-1)])
+
+    def step_graphed_packed(self, tok, between=None):
+        """step_graphed with the token already packed (pack_token): one copy
+        into the static buffers instead of three."""
+        self.tok_in.copy_(tok)
+        self._replay(between)
+
+    def _replay(self, between):
         if between is None:
             self.g_step.replay()
             return

@@ -526,7 +526,10 @@ def test_budgeted_step_graphed_matches_eager():
     graphed.capture()
     for t in range(1, steps + 1):
         eager.step(*toks[t], t)
-        graphed.step_graphed(*toks[t])
+        if t % 2:
+            graphed.step_graphed(*toks[t])
+        else:  # the token packed into the graphs' input buffer in one copy
+            graphed.step_graphed_packed(graphed.pack_token(*toks[t]))
         torch.cuda.synchronize()
         for name in ("table", "lens", "free_top", "ema", "keep", "grow", "active", "out", "lse"):
             a, b = getattr(eager, name), getattr(graphed, name)
@@ -617,6 +620,35 @@ def test_fused_step_grants_run_out(dtype, d, free_top):
         if t == 0:
             act = fused.active.cpu().numpy().astype(bool)
             assert act.all() and int(fused.grow.sum()) == free_top
+
+
+@pytest.mark.parametrize("B", [2048, 2100])
+def test_fused_step_many_sequences(B):
+    """Up to 2048 sequences the fused step lists the rows at a capacity
+    boundary in shared memory and numbers its work items densely; above that
+    it numbers every (sequence, split) pair.  Both against the separate calls,
+    bit for bit, over three steps: short rows, two thirds of them at a page
+    boundary, budgets of 1 to 5 pages."""
+    rng = np.random.default_rng(B)
+    pages = rng.integers(1, 6, size=B)
+    lens = pages * 16
+    lens[::3] -= rng.integers(1, 15, size=len(lens[::3]))
+    budget = rng.integers(1, 6, size=B).astype(np.int32)
+    x = W.small_decode(93, B, 8, 2, 64, lens.tolist(), dtype=W.F16, pool_factor=1.5, pad_pages=2)
+    cfg = BG.BudgetConfig(a_fast=0.9, a_slow=0.999, n_first=1, n_last=1, delta=0.3)
+    fused, calls = _pair(x, budget, cfg)
+    for t in range(3):
+        q = bits_to_dev(W.normal_bits(rng, (x.B, x.Hq, 64), W.F16), W.F16)
+        kn = bits_to_dev(W.normal_bits(rng, (x.B, x.Hkv, 64), W.F16), W.F16)
+        vn = bits_to_dev(W.normal_bits(rng, (x.B, x.Hkv, 64), W.F16), W.F16)
+        for dec in (fused, calls):
+            if t == 0:
+                dec.update_summaries(q, True)
+            dec.step(q, kn, vn, t)
+        torch.cuda.synchronize()
+        _same(fused, calls, f"step {t}")
+        if t == 0:
+            assert int(fused.active.sum()) > B // 10  # many rows at a boundary
 
 
 def test_fused_step_append_failure():
