@@ -1191,6 +1191,9 @@ __device__ int select_boundary_row(const StepArgs& a, int b, int n, float* sm_f,
 
 template <class T, int CPL>
 __global__ void __launch_bounds__(kStepThreads, 1) budget_step_kernel(const StepArgs a) {
+  // the token copy that follows may be scheduled early; it waits for this
+  // grid to finish before it reads anything (griddepcontrol.wait)
+  pdl_launch_dependents();
   extern __shared__ float step_sm[];
   __shared__ int red[64];
   __shared__ int s_carry[4];
@@ -1603,6 +1606,8 @@ __global__ void __launch_bounds__(kStepThreads, 1) budget_step_kernel(const Step
 // (page, slot) the fused step planned (nothing when its append failed), and
 // the sequence's final length into seq_lens.
 __global__ void __launch_bounds__(128) step_copy_kernel(const StepArgs a) {
+  pdl_wait();  // launched early: the step kernel's plan must be complete
+  pdl_launch_dependents();
   const int b = blockIdx.x;
   if (threadIdx.x == 0) a.seq_lens[b] = a.new_len[b];
   if (*a.ctl) return;
@@ -2003,7 +2008,7 @@ int kv_budget_step(const void* q, const void* k_new, const void* v_new, void* k_
   KV_CUDA_CHECK(launch(fn, dim3((unsigned)grid), dim3(kStepThreads), smem,
                        static_cast<cudaStream_t>(stream), false, a));
   KV_CUDA_CHECK(launch(step_copy_kernel, dim3(B), dim3(128), 0, static_cast<cudaStream_t>(stream),
-                       false, a));
+                       true, a));
   return KV_OK;
 }
 
