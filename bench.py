@@ -361,7 +361,8 @@ def run_ours(args, x, name, rank, world):
         if tj.get("kernel_source_hash") == kernel_hash(engine):  # null once the kernel changed
             traffic = float(tj["dram_bytes_per_launch"])
     tname = W.DTYPE_NAMES[x.dtype].upper()
-    kernel = f"mma_attend_kernel<{tname}>" if tensor_core else f"decode_kernel<128,{x.Hq // x.Hkv},{tname}>"
+    kernel = (f"mma_attend_kernel<{tname},{x.d}>" if tensor_core
+              else f"decode_kernel<{x.d},{x.Hq // x.Hkv},{tname}>")
     h2d = x.q.nbytes + x.block_table.nbytes + x.seq_lens.nbytes
     d2h = x.B * x.Hq * x.d * 4 + x.B * x.Hq * 4
     line = {

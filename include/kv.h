@@ -42,8 +42,9 @@
  *                   page_size) are never read (-1 padding is customary)
  *      seq_lens     [B] int32, tokens held by each sequence (L_b >= 0)
  *    Query head hq attends with KV head hq / (Hq / Hkv) (contiguous groups).
- *  - Supported shapes: page_size 16; d in {64, 128}; Hq / Hkv in {1, 2, 4, 8};
- *    Hkv <= 8.  Others return KV_EINVAL.
+ *  - Supported shapes: page_size 16; d in {64, 128}.  The fused decode kernel
+ *    takes Hq / Hkv in {1, 2, 4, 8} and Hkv <= 8, the tensor-core engine any
+ *    Hq / Hkv <= 64 (and any Hkv).  Others return KV_EINVAL.
  *  - Workspace: `ws` is caller-allocated device memory of at least the size
  *    the matching *_workspace_size function returns, 256-byte aligned.  Its
  *    first 256 bytes hold the status word.  One workspace may serve several
@@ -136,7 +137,7 @@ size_t kv_decode_workspace_size(int B, int Hq, int Hkv, int d, int max_pages, in
  * recombined by a log-sum-exp merge done by whichever split finishes last.
  * One kernel launch (two for B > 1024: a page-offset pass first).
  * pages_per_split = KV_DECODE_TENSOR_CORE selects the tensor-core engine
- * instead (d = 128, page_size 16, G <= 64; else KV_EINVAL): the same split
+ * instead (d = 64 or 128, page_size 16, G <= 64; else KV_EINVAL): the same split
  * rule with the automatic chunk, one CTA per chunk streaming whole pages by
  * TMA tensor copies, Q K^T and P V on mma.sync (fp32 accumulation), and a
  * merge kernel for the split sequences (kv_attend_multi with T = 1).  Both
@@ -160,14 +161,12 @@ int kv_decode(const void *q, const void *k_pool, const void *v_pool, int num_pag
  * a query with no token to attend to gets out = 0 and lse = -inf.
  * q [B][T][Hq][d] 16-bit, out [B][T][Hq][d] fp32, lse [B][T][Hq] fp32
  * (device).  Other arguments and errors as kv_decode; the workspace is
- * kv_attend_multi_workspace_size bytes (give it its own).  With d = 128 and
- * page_size 16 (G <= 64) the tensor-core engine serves up to 64 / G tokens
- * per pass over the pages (T * G <= 64: one pass for all T tokens; T = 1 is
- * kv_decode's KV_DECODE_TENSOR_CORE engine); larger T runs as
- * ceil(T * G / 64) consecutive passes over chunks of at most 64 / G tokens
- * (as even as possible), so each page is streamed that many times.  With d = 64 the fused decode kernel runs on B*T
- * causal views of the batch, streaming each page once per query token, and
- * the workspace keeps its merge tickets between calls as kv_decode's does. */
+ * kv_attend_multi_workspace_size bytes (give it its own).  The tensor-core
+ * engine (d = 64 or 128, page_size 16, G <= 64; else KV_EINVAL) serves up to
+ * 64 / G tokens per pass over the pages (T * G <= 64: one pass for all T
+ * tokens; T = 1 is kv_decode's KV_DECODE_TENSOR_CORE engine); larger T runs
+ * as ceil(T * G / 64) consecutive passes over chunks of at most 64 / G
+ * tokens (as even as possible), so each page is streamed that many times. */
 size_t kv_attend_multi_workspace_size(int B, int T, int Hq, int Hkv, int d, int max_pages,
                                       int page_size, int pages_per_split);
 int kv_attend_multi(const void *q, const void *k_pool, const void *v_pool, int num_pages,

@@ -174,7 +174,7 @@ int engine_launch(const void* q, const void* k_pool, const void* v_pool, int num
   const size_t region = tensor_core_region(B, Hq, Hkv, d, max_pages, page_size);
   if (!region) return KV_EINVAL;
   return mma_attend_launch(q, k_pool, v_pool, num_pages, block_table, max_pages, seq_lens, B, 1,
-                           1, 0, Hq, Hkv, dtype, scale, 0, out, lse, ws, ws_bytes, region, s);
+                           1, 0, Hq, Hkv, d, dtype, scale, 0, out, lse, ws, ws_bytes, region, s);
 }
 
 }  // namespace
@@ -185,7 +185,7 @@ size_t kv_decode_workspace_size(int B, int Hq, int Hkv, int d, int max_pages, in
   if (pages_per_split == KV_DECODE_TENSOR_CORE) {
     if (!tensor_core_ok(page_size, Hq, Hkv, d)) return 0;
     const size_t region = tensor_core_region(B, Hq, Hkv, d, max_pages, page_size);
-    return region ? mma_attend_workspace_size(B, Hkv, Hq / Hkv, max_pages, 0, region) : 0;
+    return region ? mma_attend_workspace_size(B, Hkv, Hq / Hkv, d, max_pages, 0, region) : 0;
   }
   if (pages_per_split < 0) return 0;
   const int nw = decode_workers_both(Hq, Hkv, d, page_size);

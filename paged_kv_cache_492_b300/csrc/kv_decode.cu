@@ -82,7 +82,6 @@ struct DecodeParams {
   long long chunk_req;      // > 0: pages per chunk; 0: automatic
   long long max_slots;      // partial slots the workspace holds
   int B, num_pages, max_pages, Hq, Hkv, stages, min_chunk;
-  int seqs_per_row;         // sequence b reads block-table row b / seqs_per_row
   float scale_log2;         // softmax scale * log2(e)
   uint32_t kv_bytes;        // one page, all KV heads: Hkv * 16 * d * 2
   uint32_t q_bytes;         // one sequence's q: Hq * d * 2
@@ -211,7 +210,7 @@ __global__ void __launch_bounds__(kDecodeThreadsMax, 1) decode_kernel(const Deco
         const int p0 = (int)lo, p1 = (int)hi;
         const int slot_id = ns == 1 ? -1 : (int)(2 * c + (s == 0 ? 1 : 0));
         const int L = __ldg(p.seq_lens + b);
-        const int32_t* trow = p.table + (size_t)(b / p.seqs_per_row) * p.max_pages;
+        const int32_t* trow = p.table + (size_t)b * p.max_pages;
         for (int jw = p0; jw < p1 && !aborted; jw += 32) {
           const int j = jw + lane;
           int id = 0;
@@ -849,8 +848,7 @@ int decode_launch(const void* q, const void* k_pool, const void* v_pool, int num
                   const int32_t* block_table, int max_pages, const int32_t* seq_lens, int B,
                   int page_size, int Hq, int Hkv, int d, int dtype, float scale,
                   int pages_per_split, float* out, float* lse, void* ws, size_t ws_bytes,
-                  cudaStream_t stream, int seqs_per_row) {
-  if (seqs_per_row < 1) return KV_EINVAL;
+                  cudaStream_t stream) {
   if (!shape_ok(page_size, Hq, Hkv, d, dtype)) return KV_EINVAL;
   if (B < 0 || num_pages < 0 || max_pages < 0 || pages_per_split < 0) return KV_EINVAL;
   if (B == 0) return KV_OK;
@@ -905,7 +903,6 @@ int decode_launch(const void* q, const void* k_pool, const void* v_pool, int num
   dp.Hkv = Hkv;
   dp.stages = k.stages;
   dp.min_chunk = kMinChunk;
-  dp.seqs_per_row = seqs_per_row;
   dp.scale_log2 = scale * 1.4426950408889634f;
   dp.kv_bytes = k.kv_bytes;
   dp.q_bytes = k.q_bytes;
@@ -1065,7 +1062,6 @@ int decode_noalloc(const void* q, const void* k_pool, const void* v_pool, int nu
   dp.Hkv = Hkv;
   dp.stages = k.stages;
   dp.min_chunk = kMinChunk;
-  dp.seqs_per_row = 1;
   dp.scale_log2 = scale * 1.4426950408889634f;
   dp.kv_bytes = k.kv_bytes;
   dp.q_bytes = k.q_bytes;

@@ -91,13 +91,11 @@ DecodeLayout decode_layout(int B, int Hq, int Hkv, int d, int max_pages, int pag
                            int pages_per_split, long long n_workers);
 
 // Decode entry used by both the device-pointer and the host-IO calls.
-// seqs_per_row > 1: sequences b read block-table row b / seqs_per_row (the
-// virtual sequences of a multi-token query share their sequence's row).
 int decode_launch(const void* q, const void* k_pool, const void* v_pool, int num_pages,
                   const int32_t* block_table, int max_pages, const int32_t* seq_lens, int B,
                   int page_size, int Hq, int Hkv, int d, int dtype, float scale,
                   int pages_per_split, float* out, float* lse, void* ws, size_t ws_bytes,
-                  cudaStream_t stream, int seqs_per_row = 1);
+                  cudaStream_t stream);
 int decode_num_workers(int Hq, int Hkv, int d, int page_size, int dtype);
 
 // Tensor-core attention of T * G <= 64 query rows per KV head (d = 128,
@@ -109,14 +107,14 @@ int decode_num_workers(int Hq, int Hkv, int d, int page_size, int dtype);
 // head); 0 where the kernel does not apply.
 int mma_attend_max_tokens(int Hq, int Hkv, int d);
 bool mma_attend_supported(int Hq, int Hkv, int d, int Tq);
-size_t mma_attend_workspace_size(int B, int Hkv, int rows, int max_pages, int pages_per_split,
-                                 size_t region);
+size_t mma_attend_workspace_size(int B, int Hkv, int rows, int d, int max_pages,
+                                 int pages_per_split, size_t region);
 // q, out and lse hold Tstride query tokens per sequence; this call serves Tq
 // of them (from row 0 of the pointers passed), which see max(0, L - len_shift)
 // cached tokens causally (decode: Tq = Tstride = 1, len_shift = 0).
 int mma_attend_launch(const void* q, const void* k_pool, const void* v_pool, int num_pages,
                       const int32_t* block_table, int max_pages, const int32_t* seq_lens, int B,
-                      int Tq, int Tstride, int len_shift, int Hq, int Hkv, int dtype,
+                      int Tq, int Tstride, int len_shift, int Hq, int Hkv, int d, int dtype,
                       float scale, int pages_per_split, float* out, float* lse, void* ws,
                       size_t ws_bytes, size_t region, cudaStream_t stream);
 

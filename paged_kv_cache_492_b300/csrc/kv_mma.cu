@@ -37,6 +37,7 @@
 #include <stdio.h>
 #include <string.h>
 
+#include <array>
 #include <mutex>
 
 #include "kv_internal.h"
@@ -44,7 +45,7 @@
 namespace kvb {
 namespace {
 
-constexpr int kMmaD = 128;              // head dimension of this path
+// head dimension d: 64 or 128 (one or two 64-channel halves of 128 bytes)
 constexpr int kMmaRows = 16;            // query rows of one m16 tile (one consumer warp)
 constexpr int kMaxRowBlocks = 4;        // up to 64 query rows per KV head
 constexpr int kMaxStages = 12;          // pages in flight per CTA (3 at 8 heads .. 12)
@@ -142,25 +143,26 @@ __device__ __forceinline__ int shifted_len(int L, int shift) {
 }
 
 // Stage layout: K then V; each is [channel half][head of the block][token]
-// rows of 128 bytes (64 channels), i.e. a (half, head) sub-tile of 2 KiB.
-// The 128-byte swizzle stores logical 16-byte chunk c of a row at chunk
-// c ^ (token % 8), so the eight rows one ldmatrix reads fall in eight
-// different bank groups.  Offset of logical chunk `chunk` (0..15 over the
-// 128 channels) of token `t` within one head's tile:
+// rows of 128 bytes (64 channels), i.e. a (half, head) sub-tile of 2 KiB; a
+// head has d / 64 halves.  The 128-byte swizzle stores logical 16-byte chunk
+// c of a row at chunk c ^ (token % 8), so the eight rows one ldmatrix reads
+// fall in eight different bank groups.  Offset of logical chunk `chunk`
+// (0 .. d/8 - 1 over the d channels) of token `t` within one head's tile:
 __device__ __forceinline__ uint32_t tile_off(int t, int chunk, uint32_t half_stride) {
   return (uint32_t)(chunk >> 3) * half_stride + (uint32_t)(t * 128 + (((chunk & 7) ^ (t & 7)) << 4));
 }
 
-template <class T>
+template <class T, int D>
 __global__ void __launch_bounds__(32 * (1 + kMaxHeadBlock), 1)
     mma_attend_kernel(const __grid_constant__ CUtensorMap tmk,
                       const __grid_constant__ CUtensorMap tmv, const MmaParams p) {
+  constexpr int kHalves = D / 64;  // 64-channel halves of a head's row (one 128-byte atom each)
   extern __shared__ __align__(1024) uint8_t smem[];
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem);  // full[S], empty[S]
   const uint32_t raw = smem_u32(smem);
   uint8_t* stages = smem + (((raw + kBarBytes + 1023) & ~1023u) - raw);  // 1024-aligned
   const uint32_t half_stride = (uint32_t)p.hb * kHalfTile;
-  const uint32_t stage_bytes = 4 * half_stride;  // K and V, two halves each
+  const uint32_t stage_bytes = 2 * kHalves * half_stride;  // K and V, kHalves halves each
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int c = blockIdx.x / p.nhb, hblk = blockIdx.x - (blockIdx.x / p.nhb) * p.nhb;
 
@@ -262,9 +264,10 @@ __global__ void __launch_bounds__(32 * (1 + kMaxHeadBlock), 1)
               const uint32_t st = smem_u32(stages) + (uint32_t)slot * stage_bytes;
               mbar_arrive_expect_tx(bar, stage_bytes);
 #pragma unroll
-              for (int half = 0; half < 2; ++half) {
+              for (int half = 0; half < kHalves; ++half) {
                 tma_load_5d(st + half * half_stride, &tmk, 0, half, 0, h0, pid, bar, pol);
-                tma_load_5d(st + (2 + half) * half_stride, &tmv, 0, half, 0, h0, pid, bar, pol);
+                tma_load_5d(st + (kHalves + half) * half_stride, &tmv, 0, half, 0, h0, pid, bar,
+                            pol);
               }
             }
           }
@@ -316,13 +319,13 @@ __global__ void __launch_bounds__(32 * (1 + kMaxHeadBlock), 1)
     auto qrow = [&](int r) -> const uint16_t* {
       if (r >= p.rows) return nullptr;
       const int i = r / p.G, g = r - (r / p.G) * p.G;
-      return p.q + (((size_t)b * p.Tstride + i) * p.Hq + (size_t)h * p.G + g) * kMmaD;
+      return p.q + (((size_t)b * p.Tstride + i) * p.Hq + (size_t)h * p.G + g) * D;
     };
     const uint16_t* q0 = qrow(qr0);
     const uint16_t* q1 = qrow(qr1);
-    uint32_t qa[8][4];
+    uint32_t qa[D / 16][4];
 #pragma unroll
-    for (int kk = 0; kk < 8; ++kk) {
+    for (int kk = 0; kk < D / 16; ++kk) {
       const int cc = kk * 16 + qc;
       qa[kk][0] = q0 ? __ldg(reinterpret_cast<const uint32_t*>(q0 + cc)) : 0u;
       qa[kk][1] = q1 ? __ldg(reinterpret_cast<const uint32_t*>(q1 + cc)) : 0u;
@@ -333,9 +336,9 @@ __global__ void __launch_bounds__(32 * (1 + kMaxHeadBlock), 1)
     const int lim0 = qr0 < p.rows ? L - p.Tq + 1 + qr0 / p.G : 0;
     const int lim1 = qr1 < p.rows ? L - p.Tq + 1 + qr1 / p.G : 0;
 
-    float o[16][4];
+    float o[D / 8][4];
 #pragma unroll
-    for (int n = 0; n < 16; ++n) o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0.f;
+    for (int n = 0; n < D / 8; ++n) o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0.f;
     float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
 
     for (int j = p0; j < p1; ++j) {
@@ -345,11 +348,11 @@ __global__ void __launch_bounds__(32 * (1 + kMaxHeadBlock), 1)
         return;
       }
       const uint32_t kt = smem_u32(stages) + (uint32_t)slot * stage_bytes + hw * kHalfTile;
-      const uint32_t vt = kt + 2 * half_stride;
+      const uint32_t vt = kt + kHalves * half_stride;
       // ---- S = Q K^T: two n-tiles of 8 tokens, eight k-steps of 16 channels
       float s[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
 #pragma unroll
-      for (int kk = 0; kk < 8; ++kk) {
+      for (int kk = 0; kk < D / 16; ++kk) {
         // matrices: (tokens 0-7, ch lo), (0-7, ch hi), (8-15, lo), (8-15, hi)
         const int t = (mi >> 1) * 8 + mr, chunk = kk * 2 + (mi & 1);
         uint32_t b00, b01, b10, b11;
@@ -392,7 +395,7 @@ __global__ void __launch_bounds__(32 * (1 + kMaxHeadBlock), 1)
       l0 = l0 * al0 + pr[0][0] + pr[0][1] + pr[1][0] + pr[1][1];
       l1 = l1 * al1 + pr[0][2] + pr[0][3] + pr[1][2] + pr[1][3];
 #pragma unroll
-      for (int n = 0; n < 16; ++n) {
+      for (int n = 0; n < D / 8; ++n) {
         o[n][0] *= al0;
         o[n][1] *= al0;
         o[n][2] *= al1;
@@ -412,7 +415,7 @@ __global__ void __launch_bounds__(32 * (1 + kMaxHeadBlock), 1)
         }
       }
 #pragma unroll
-      for (int n2 = 0; n2 < 8; ++n2) {
+      for (int n2 = 0; n2 < D / 16; ++n2) {
         // matrices: (tokens 0-7, ch tile 2n2), (8-15, 2n2), (0-7, 2n2+1), (8-15, 2n2+1)
         const int t = (mi & 1) * 8 + mr, chunk = n2 * 2 + (mi >> 1);
         uint32_t v00, v01, v10, v11;
@@ -446,11 +449,11 @@ __global__ void __launch_bounds__(32 * (1 + kMaxHeadBlock), 1)
       if (single) {
         const int i = r / p.G, g = r - (r / p.G) * p.G;
         const size_t row = ((size_t)b * p.Tstride + i) * p.Hq + (size_t)h * p.G + g;
-        *o_ptr = p.out + row * kMmaD;
+        *o_ptr = p.out + row * D;
         *l_ptr = p.lse + row;
       } else {
         const size_t part = (size_t)slot_id * p.Hkv + h;
-        *o_ptr = p.part_o + (part * p.rows_pad + r) * kMmaD;
+        *o_ptr = p.part_o + (part * p.rows_pad + r) * D;
         *l_ptr = p.part_lse + part * p.rows_pad + r;
       }
     };
@@ -458,7 +461,7 @@ __global__ void __launch_bounds__(32 * (1 + kMaxHeadBlock), 1)
       float *po, *pl;
       dst_row(qr0, &po, &pl);
 #pragma unroll
-      for (int n = 0; n < 16; ++n)
+      for (int n = 0; n < D / 8; ++n)
         *reinterpret_cast<float2*>(po + n * 8 + qc) = make_float2(o[n][0] * inv0, o[n][1] * inv0);
       if ((lane & 3) == 0) *pl = ls0;
     }
@@ -466,12 +469,14 @@ __global__ void __launch_bounds__(32 * (1 + kMaxHeadBlock), 1)
       float *po, *pl;
       dst_row(qr1, &po, &pl);
 #pragma unroll
-      for (int n = 0; n < 16; ++n)
+      for (int n = 0; n < D / 8; ++n)
         *reinterpret_cast<float2*>(po + n * 8 + qc) = make_float2(o[n][2] * inv1, o[n][3] * inv1);
       if ((lane & 3) == 0) *pl = ls1;
     }
   }
 }
+
+using AttendFn = void (*)(const CUtensorMap, const CUtensorMap, const MmaParams);
 
 // Combine the splits of each (sequence, KV head): per row
 // lse = ln sum_s e^{lse_s}, out = sum_s e^{lse_s - lse} out_s (parts with
@@ -495,10 +500,36 @@ struct MmaMergeParams {
   int B, Hq, Hkv, G, Tstride, rows, rows_pad;
 };
 
-template <int kMergeWarps>
-__global__ void __launch_bounds__(kMergeWarps * 32) mma_merge_kernel(const MmaMergeParams p) {
+// CPL consecutive fp32 channels of one lane (4 at d = 128, 2 at d = 64).
+template <int CPL>
+struct Chans {
+  float v[CPL];
+};
+template <int CPL>
+__device__ __forceinline__ Chans<CPL> ldcg_chans(const float* p) {
+  Chans<CPL> r;
+  if constexpr (CPL == 4) {
+    const float4 x = __ldcg(reinterpret_cast<const float4*>(p));
+    r.v[0] = x.x, r.v[1] = x.y, r.v[2] = x.z, r.v[3] = x.w;
+  } else {
+    const float2 x = __ldcg(reinterpret_cast<const float2*>(p));
+    r.v[0] = x.x, r.v[1] = x.y;
+  }
+  return r;
+}
+template <int CPL>
+__device__ __forceinline__ void st_chans(float* p, const Chans<CPL>& c) {
+  if constexpr (CPL == 4)
+    *reinterpret_cast<float4*>(p) = make_float4(c.v[0], c.v[1], c.v[2], c.v[3]);
+  else
+    *reinterpret_cast<float2*>(p) = make_float2(c.v[0], c.v[1]);
+}
+
+template <int kMergeWarps, int D>
+__global__ void __launch_bounds__(kMergeWarps * 32, 1) mma_merge_kernel(const MmaMergeParams p) {
+  constexpr int CPL = D / 32;  // channels per lane
   __shared__ float sm_m[kMergeWarps], sm_l[kMergeWarps];
-  __shared__ float4 sm_acc[kMergeWarps][32];
+  __shared__ Chans<CPL> sm_acc[kMergeWarps][32];
   pdl_wait();
   const int b = blockIdx.x / p.Hkv, h = blockIdx.x - (blockIdx.x / p.Hkv) * p.Hkv;
   const int r = blockIdx.y;
@@ -508,28 +539,31 @@ __global__ void __launch_bounds__(kMergeWarps * 32) mma_merge_kernel(const MmaMe
   const int i = r / p.G, g = r - (r / p.G) * p.G;
   const size_t row = ((size_t)b * p.Tstride + i) * p.Hq + (size_t)h * p.G + g;
   if (ns == 0) {
-    if (threadIdx.x < kMmaD) p.out[row * kMmaD + threadIdx.x] = 0.f;
+    if (threadIdx.x < D) p.out[row * D + threadIdx.x] = 0.f;
     if (threadIdx.x == 0) p.lse[row] = -INFINITY;
     return;
   }
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, c4 = lane * 4;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, c0 = lane * CPL;
   const long long cf = Ob / chunk;
   auto part = [&](long long s) {
     return ((size_t)(s == 0 ? 2 * cf + 1 : 2 * (cf + s)) * p.Hkv + h) * p.rows_pad + r;
   };
-  auto load_o = [&](long long s) {
-    return __ldcg(reinterpret_cast<const float4*>(p.part_o + part(s) * kMmaD + c4));
-  };
+  auto load_o = [&](long long s) { return ldcg_chans<CPL>(p.part_o + part(s) * D + c0); };
   const long long q = (ns + kMergeWarps - 1) / kMergeWarps;
   const long long sa = min(ns, warp * q), sb = min(ns, sa + q);
   float m = -INFINITY, l = 0.f;
-  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  Chans<CPL> acc;
+#pragma unroll
+  for (int e = 0; e < CPL; ++e) acc.v[e] = 0.f;
+  Chans<CPL> zero;
+#pragma unroll
+  for (int e = 0; e < CPL; ++e) zero.v[e] = 0.f;
   for (long long s0 = sa; s0 < sb; s0 += 32) {
     const int n = (int)min(32ll, sb - s0);
     const float ls = lane < n ? __ldcg(p.part_lse + part(s0 + lane)) : -INFINITY;
-    float4 v[16];
+    Chans<CPL> v[16];
 #pragma unroll
-    for (int k = 0; k < 16; ++k) v[k] = k < n ? load_o(s0 + k) : make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int k = 0; k < 16; ++k) v[k] = k < n ? load_o(s0 + k) : zero;
     float mb = ls;
 #pragma unroll
     for (int off = 16; off; off >>= 1) mb = fmaxf(mb, __shfl_xor_sync(FULLM, mb, off));
@@ -537,27 +571,22 @@ __global__ void __launch_bounds__(kMergeWarps * 32) mma_merge_kernel(const MmaMe
     const float mn = fmaxf(m, mb);
     const float keep = m == -INFINITY ? 0.f : expf(m - mn);
     m = mn;
-    acc.x *= keep;
-    acc.y *= keep;
-    acc.z *= keep;
-    acc.w *= keep;
+#pragma unroll
+    for (int e = 0; e < CPL; ++e) acc.v[e] *= keep;
     const float w_mine = ls == -INFINITY ? 0.f : expf(ls - m);
     float wsum = w_mine;
 #pragma unroll
     for (int off = 16; off; off >>= 1) wsum += __shfl_xor_sync(FULLM, wsum, off);
     l = l * keep + wsum;
-    auto add = [&](const float4& x, float w) {
-      acc.x = fmaf(w, x.x, acc.x);
-      acc.y = fmaf(w, x.y, acc.y);
-      acc.z = fmaf(w, x.z, acc.z);
-      acc.w = fmaf(w, x.w, acc.w);
+    auto add = [&](const Chans<CPL>& x, float w) {
+#pragma unroll
+      for (int e = 0; e < CPL; ++e) acc.v[e] = fmaf(w, x.v[e], acc.v[e]);
     };
 #pragma unroll
     for (int k = 0; k < 16; ++k) add(v[k], __shfl_sync(FULLM, w_mine, k));
     if (n > 16) {
 #pragma unroll
-      for (int k = 0; k < 16; ++k)
-        v[k] = 16 + k < n ? load_o(s0 + 16 + k) : make_float4(0.f, 0.f, 0.f, 0.f);
+      for (int k = 0; k < 16; ++k) v[k] = 16 + k < n ? load_o(s0 + 16 + k) : zero;
 #pragma unroll
       for (int k = 0; k < 16; ++k) add(v[k], __shfl_sync(FULLM, w_mine, 16 + k));
     }
@@ -572,7 +601,7 @@ __global__ void __launch_bounds__(kMergeWarps * 32) mma_merge_kernel(const MmaMe
   float M = -INFINITY;
 #pragma unroll
   for (int w = 0; w < kMergeWarps; ++w) M = fmaxf(M, sm_m[w]);
-  float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
+  Chans<CPL> o = zero;
   float Lr = -INFINITY;
   if (M > -INFINITY) {
     float L = 0.f;
@@ -585,16 +614,14 @@ __global__ void __launch_bounds__(kMergeWarps * 32) mma_merge_kernel(const MmaMe
     const float inv = 1.f / L;
 #pragma unroll
     for (int w = 0; w < kMergeWarps; ++w) {
-      const float4 a = sm_acc[w][lane];
+      const Chans<CPL> a = sm_acc[w][lane];
       const float f = sc[w] * inv;
-      o.x = fmaf(f, a.x, o.x);
-      o.y = fmaf(f, a.y, o.y);
-      o.z = fmaf(f, a.z, o.z);
-      o.w = fmaf(f, a.w, o.w);
+#pragma unroll
+      for (int e = 0; e < CPL; ++e) o.v[e] = fmaf(f, a.v[e], o.v[e]);
     }
     Lr = M + logf(L);
   }
-  *reinterpret_cast<float4*>(p.out + row * kMmaD + c4) = o;
+  st_chans<CPL>(p.out + row * D + c0, o);
   if (lane == 0) p.lse[row] = Lr;
 }
 
@@ -621,17 +648,18 @@ int encode_fn(EncodeTiledFn* out) {
   return KV_OK;
 }
 
-// Pool [P][Hkv][16][128] seen as 5-D (64 channels, channel half, slot, head,
-// page); one box is one channel half of `hb` heads of one page: hb x 16 rows
-// of 128 bytes, 128-byte swizzled.  A map depends only on these arguments,
-// so the last few are kept and reused (encoding is host work on every call
-// otherwise).
+// Pool [P][Hkv][16][d] seen as 5-D (64 channels, channel half, slot, head,
+// page; d / 64 halves); one box is one channel half of `hb` heads of one
+// page: hb x 16 rows of 128 bytes, 128-byte swizzled.  A map depends only on
+// these arguments, so the last few are kept and reused (encoding is host
+// work on every call otherwise).
 int encode_pool_map_uncached(CUtensorMap* m, const void* pool, int num_pages, int Hkv, int hb,
-                             int dtype);
-int encode_pool_map(CUtensorMap* m, const void* pool, int num_pages, int Hkv, int hb, int dtype) {
+                             int dtype, int d);
+int encode_pool_map(CUtensorMap* m, const void* pool, int num_pages, int Hkv, int hb, int dtype,
+                    int d) {
   struct Entry {
     const void* pool;
-    int num_pages, Hkv, hb, dtype;
+    int num_pages, Hkv, hb, dtype, d;
     CUtensorMap map;
   };
   constexpr int kEntries = 8;
@@ -643,29 +671,30 @@ int encode_pool_map(CUtensorMap* m, const void* pool, int num_pages, int Hkv, in
     for (int i = 0; i < used; ++i) {
       const Entry& e = cache[i];
       if (e.pool == pool && e.num_pages == num_pages && e.Hkv == Hkv && e.hb == hb &&
-          e.dtype == dtype) {
+          e.dtype == dtype && e.d == d) {
         *m = e.map;
         return KV_OK;
       }
     }
   }
-  const int rc = encode_pool_map_uncached(m, pool, num_pages, Hkv, hb, dtype);
+  const int rc = encode_pool_map_uncached(m, pool, num_pages, Hkv, hb, dtype, d);
   if (rc) return rc;
   std::lock_guard<std::mutex> lk(mu);
   Entry& e = cache[next];
-  e = Entry{pool, num_pages, Hkv, hb, dtype, *m};
+  e = Entry{pool, num_pages, Hkv, hb, dtype, d, *m};
   next = (next + 1) % kEntries;
   if (used < kEntries) ++used;
   return KV_OK;
 }
 
 int encode_pool_map_uncached(CUtensorMap* m, const void* pool, int num_pages, int Hkv, int hb,
-                             int dtype) {
+                             int dtype, int d) {
   EncodeTiledFn fn;
   int rc = encode_fn(&fn);
   if (rc) return rc;
-  const cuuint64_t dims[5] = {64, 2, 16, (cuuint64_t)Hkv, (cuuint64_t)num_pages};
-  const cuuint64_t strides[4] = {128, 256, 4096, (cuuint64_t)Hkv * 4096};
+  const cuuint64_t row = (cuuint64_t)d * 2;  // bytes of one token's head row
+  const cuuint64_t dims[5] = {64, (cuuint64_t)d / 64, 16, (cuuint64_t)Hkv, (cuuint64_t)num_pages};
+  const cuuint64_t strides[4] = {128, row, 16 * row, (cuuint64_t)Hkv * 16 * row};
   const cuuint32_t box[5] = {64, 1, 16, (cuuint32_t)hb, 1};
   const cuuint32_t estr[5] = {1, 1, 1, 1, 1};
   const CUresult r = fn(m, dtype == KV_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
@@ -691,13 +720,13 @@ int head_block(int Hkv, int rb) {
   return 1;
 }
 // Ring depth: about kRingBytes in flight whatever the head block (a stage is
-// one page of hb heads, K and V).
-int ring_stages(int hb) {
-  const int s = kRingBytes / (4 * hb * kHalfTile);
+// one page of hb heads, K and V, d / 64 halves each).
+int ring_stages(int hb, int d) {
+  const int s = kRingBytes / (2 * (d / 64) * hb * kHalfTile);
   return s < 3 ? 3 : (s > kMaxStages ? kMaxStages : s);
 }
-size_t mma_smem(int hb) {
-  return kBarBytes + 1024 + (size_t)ring_stages(hb) * 4 * hb * kHalfTile;
+size_t mma_smem(int hb, int d) {
+  return kBarBytes + 1024 + (size_t)ring_stages(hb, d) * 2 * (d / 64) * hb * kHalfTile;
 }
 
 struct MmaLayout {
@@ -705,7 +734,7 @@ struct MmaLayout {
   long long max_chunks;
 };
 
-MmaLayout mma_layout(int B, int Hkv, int rows, int max_pages, int pages_per_split,
+MmaLayout mma_layout(int B, int Hkv, int rows, int d, int max_pages, int pages_per_split,
                      long long n_chunks, size_t region) {
   const size_t rows_pad = (size_t)row_blocks(rows) * kMmaRows;
   MmaLayout L{};
@@ -721,69 +750,73 @@ MmaLayout mma_layout(int B, int Hkv, int rows, int max_pages, int pages_per_spli
   };
   L.page_off = take((size_t)(B + 1) * 4);
   L.chunk = take(4);
-  L.part_o = take((size_t)slots * Hkv * rows_pad * kMmaD * 4);
+  L.part_o = take((size_t)slots * Hkv * rows_pad * d * 4);
   L.part_lse = take((size_t)slots * Hkv * rows_pad * 4);
   L.total = off;
   return L;
 }
 
 // Chunks of the automatic split: one per CTA that fits on the device at once.
-int mma_chunks(int Hkv, int rows, long long* out) {
+int mma_chunks(int Hkv, int rows, int d, long long* out) {
   static std::mutex mu;
-  static int cached[64][kMaxHeadBlock + 1][kMaxRowBlocks + 1] = {};
+  static int cached[64][2][kMaxHeadBlock + 1][kMaxRowBlocks + 1] = {};
   int dev = 0;
   KV_CUDA_CHECK(cudaGetDevice(&dev));
   if (dev < 0 || dev >= 64) return KV_EINVAL;
   const int rb = row_blocks(rows);
   if (rb < 1 || rb > kMaxRowBlocks) return KV_EINVAL;
-  const int hb = head_block(Hkv, rb);
+  const int hb = head_block(Hkv, rb), di = d == 64 ? 0 : 1;
   std::lock_guard<std::mutex> lk(mu);
-  if (!cached[dev][hb][rb]) {
+  if (!cached[dev][di][hb][rb]) {
     int sms = 0, per = 0;
     KV_CUDA_CHECK(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev));
-    for (auto fn : {mma_attend_kernel<F16>, mma_attend_kernel<BF16>}) {
+    const auto fns = d == 64 ? std::array<AttendFn, 2>{mma_attend_kernel<F16, 64>,
+                                                       mma_attend_kernel<BF16, 64>}
+                             : std::array<AttendFn, 2>{mma_attend_kernel<F16, 128>,
+                                                       mma_attend_kernel<BF16, 128>};
+    for (auto fn : fns) {
       KV_CUDA_CHECK(cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)mma_smem(kMaxHeadBlock)));
+                                         (int)mma_smem(kMaxHeadBlock, d)));
       int n = 0;
-      KV_CUDA_CHECK(
-          cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, fn, 32 * (1 + hb * rb), mma_smem(hb)));
+      KV_CUDA_CHECK(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, fn, 32 * (1 + hb * rb),
+                                                                  mma_smem(hb, d)));
       per = per == 0 ? n : min(per, n);
     }
     if (per < 1) return cuda_failed(cudaErrorInvalidConfiguration, "tensor-core attend occupancy");
-    cached[dev][hb][rb] = sms * per;
+    cached[dev][di][hb][rb] = sms * per;
   }
   const int nhb = Hkv / hb;
-  *out = (cached[dev][hb][rb] + nhb - 1) / nhb;
+  *out = (cached[dev][di][hb][rb] + nhb - 1) / nhb;
   return KV_OK;
 }
 
 }  // namespace
 
 int mma_attend_max_tokens(int Hq, int Hkv, int d) {
-  if (d != kMmaD || Hkv <= 0 || Hq <= 0 || Hq % Hkv) return 0;
+  if ((d != 64 && d != 128) || Hkv <= 0 || Hq <= 0 || Hq % Hkv) return 0;
   return kMmaRows * kMaxRowBlocks / (Hq / Hkv);  // 0 when G > 64
 }
 
 bool mma_attend_supported(int Hq, int Hkv, int d, int Tq) {
-  return d == kMmaD && Hkv > 0 && Hq % Hkv == 0 && Tq >= 1 &&
+  return (d == 64 || d == 128) && Hkv > 0 && Hq % Hkv == 0 && Tq >= 1 &&
          (long long)(Hq / Hkv) * Tq <= (long long)kMmaRows * kMaxRowBlocks;
 }
 
-size_t mma_attend_workspace_size(int B, int Hkv, int rows, int max_pages, int pages_per_split,
-                                 size_t region) {
+size_t mma_attend_workspace_size(int B, int Hkv, int rows, int d, int max_pages,
+                                 int pages_per_split, size_t region) {
   long long chunks = 0;
   if (B < 0 || Hkv < 1 || rows < 1 || rows > kMmaRows * kMaxRowBlocks || max_pages < 0 ||
-      pages_per_split < 0 || mma_chunks(Hkv, rows, &chunks))
+      pages_per_split < 0 || (d != 64 && d != 128) || mma_chunks(Hkv, rows, d, &chunks))
     return 0;
-  return mma_layout(B, Hkv, rows, max_pages, pages_per_split, chunks, region).total;
+  return mma_layout(B, Hkv, rows, d, max_pages, pages_per_split, chunks, region).total;
 }
 
 int mma_attend_launch(const void* q, const void* k_pool, const void* v_pool, int num_pages,
                       const int32_t* block_table, int max_pages, const int32_t* seq_lens, int B,
-                      int Tq, int Tstride, int len_shift, int Hq, int Hkv, int dtype,
+                      int Tq, int Tstride, int len_shift, int Hq, int Hkv, int d, int dtype,
                       float scale, int pages_per_split, float* out, float* lse, void* ws,
                       size_t ws_bytes, size_t region, cudaStream_t stream) {
-  if (!mma_attend_supported(Hq, Hkv, kMmaD, Tq) || (dtype != KV_F16 && dtype != KV_BF16))
+  if (!mma_attend_supported(Hq, Hkv, d, Tq) || (dtype != KV_F16 && dtype != KV_BF16))
     return KV_EINVAL;
   if (Tstride < Tq || len_shift < 0) return KV_EINVAL;
   if (B < 0 || num_pages < 1 || max_pages < 0 || pages_per_split < 0) return KV_EINVAL;
@@ -796,16 +829,16 @@ int mma_attend_launch(const void* q, const void* k_pool, const void* v_pool, int
     return KV_EINVAL;
   long long chunks = 0;
   const int rows = (Hq / Hkv) * Tq, rb = row_blocks(rows);
-  int rc = mma_chunks(Hkv, rows, &chunks);
+  int rc = mma_chunks(Hkv, rows, d, &chunks);
   if (rc) return rc;
-  const MmaLayout L = mma_layout(B, Hkv, rows, max_pages, pages_per_split, chunks, region);
+  const MmaLayout L = mma_layout(B, Hkv, rows, d, max_pages, pages_per_split, chunks, region);
   if (ws_bytes < L.total) return KV_EWORKSPACE;
   uint8_t* w = static_cast<uint8_t*>(ws);
   const int hb = head_block(Hkv, rb), nhb = Hkv / hb;
   CUtensorMap tmk, tmv;
-  rc = encode_pool_map(&tmk, k_pool, num_pages, Hkv, hb, dtype);
+  rc = encode_pool_map(&tmk, k_pool, num_pages, Hkv, hb, dtype, d);
   if (rc) return rc;
-  rc = encode_pool_map(&tmv, v_pool, num_pages, Hkv, hb, dtype);
+  rc = encode_pool_map(&tmv, v_pool, num_pages, Hkv, hb, dtype, d);
   if (rc) return rc;
 
   int* status = reinterpret_cast<int*>(w);
@@ -847,7 +880,7 @@ int mma_attend_launch(const void* q, const void* k_pool, const void* v_pool, int
   mp.len_shift = len_shift;
   mp.rows = rows;
   mp.rows_pad = rb * kMmaRows;
-  mp.stages = ring_stages(hb);
+  mp.stages = ring_stages(hb, d);
   mp.rb = rb;
   mp.hb = hb;
   mp.nhb = nhb;
@@ -862,12 +895,11 @@ int mma_attend_launch(const void* q, const void* k_pool, const void* v_pool, int
   take_profile_events(&ev_before, &ev_after);
   if (ev_before) KV_CUDA_CHECK(cudaEventRecord(ev_before, stream));
   const dim3 block(32 * (1 + hb * rb));
-  if (dtype == KV_BF16)
-    KV_CUDA_CHECK(launch(mma_attend_kernel<BF16>, dim3((unsigned)grid), block, mma_smem(hb), stream,
-                         true, tmk, tmv, mp));
-  else
-    KV_CUDA_CHECK(launch(mma_attend_kernel<F16>, dim3((unsigned)grid), block, mma_smem(hb), stream,
-                         true, tmk, tmv, mp));
+  const AttendFn kernel = dtype == KV_BF16
+                              ? (d == 64 ? mma_attend_kernel<BF16, 64> : mma_attend_kernel<BF16, 128>)
+                              : (d == 64 ? mma_attend_kernel<F16, 64> : mma_attend_kernel<F16, 128>);
+  KV_CUDA_CHECK(launch(kernel, dim3((unsigned)grid), block, mma_smem(hb, d), stream, true, tmk, tmv,
+                       mp));
   if (ev_after) KV_CUDA_CHECK(cudaEventRecord(ev_after, stream));  // the attention kernel alone
   MmaMergeParams gp{};
   gp.page_off = page_off;
@@ -887,10 +919,13 @@ int mma_attend_launch(const void* q, const void* k_pool, const void* v_pool, int
   int dev = 0, sms = 0;
   KV_CUDA_CHECK(cudaGetDevice(&dev));
   KV_CUDA_CHECK(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev));
-  if ((long long)B * Hkv * mp.rows <= sms)
-    KV_CUDA_CHECK(launch(mma_merge_kernel<16>, mgrid, dim3(16 * 32), 0, stream, true, gp));
+  const bool wide = (long long)B * Hkv * mp.rows <= sms;  // 16 warps per row, else 4
+  if (d == 64)
+    KV_CUDA_CHECK(launch(wide ? mma_merge_kernel<16, 64> : mma_merge_kernel<4, 64>, mgrid,
+                         dim3((wide ? 16 : 4) * 32), 0, stream, true, gp));
   else
-    KV_CUDA_CHECK(launch(mma_merge_kernel<4>, mgrid, dim3(4 * 32), 0, stream, true, gp));
+    KV_CUDA_CHECK(launch(wide ? mma_merge_kernel<16, 128> : mma_merge_kernel<4, 128>, mgrid,
+                         dim3((wide ? 16 : 4) * 32), 0, stream, true, gp));
   return KV_OK;
 }
 

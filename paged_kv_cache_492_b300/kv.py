@@ -324,7 +324,7 @@ class DecodePolicy:
 
     def usable(self, B, Hq, Hkv, d, max_pages, page_size=16):
         """The candidates this shape supports (the tensor-core engine needs
-        d = 128 and G <= 64; an unsupported variant has workspace size 0)."""
+        d = 64 or 128 and G <= 64; an unsupported variant has workspace size 0)."""
         return [c for c in self.candidates
                 if kv_decode_workspace_size(B, Hq, Hkv, d, max_pages, page_size, c) > 0]
 

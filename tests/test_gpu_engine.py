@@ -37,6 +37,12 @@ SMALL = [
     (66, 2, 20, 5, 128, [2300, 64], W.F16),                    # head block 5, 4-stage ring
     (67, 2, 56, 7, 128, [1000, 999], W.BF16),                  # head block 7, 3-stage ring
     (68, 2, 48, 1, 128, [1800, 33], W.F16),                    # Hkv = 1, G = 48: three row blocks
+    # d = 64: one 64-channel half per head row, twice the ring stages
+    (70, 1, 4, 1, 64, [256], W.F16),                           # the tiny workload's shape
+    (71, 3, 8, 2, 64, [1, 15, 700], W.F16),
+    (72, 4, 32, 8, 64, [17, 0, 300, 5000], W.BF16),
+    (73, 2, 64, 4, 64, [2000, 33], W.F16),                     # G = 16
+    (74, 2, 128, 2, 64, [1500, 40], W.BF16),                   # G = 64: four row blocks
 ]
 
 
@@ -62,6 +68,7 @@ FULL = {
     "zipf": W.zipf_lengths,
     "bucket128k": lambda: W.bucketed_long(131072),
     "budgeted_b64": lambda: W.budgeted_serving()["decode"],
+    "tiny": lambda: W.tiny()["decode"],
 }
 
 
@@ -240,11 +247,12 @@ def test_engine_keeps_no_state_between_calls():
 
 
 def test_engine_argument_checks():
-    # d = 64 and groups above 64 have no tensor-core form
-    assert kv.kv_decode_workspace_size(2, 8, 2, 64, 4, 16, TC) == 0
+    # d = 96 and groups above 64 have no tensor-core form
+    assert kv.kv_decode_workspace_size(2, 8, 2, 96, 4, 16, TC) == 0
     assert kv.kv_decode_workspace_size(2, 256, 2, 128, 4, 16, TC) == 0
     assert kv.kv_decode_workspace_size(2, 8, 2, 128, 4, 16, -2) == 0
-    x = W.small_decode(58, 1, 8, 2, 64, [40])
+    assert kv.kv_decode_workspace_size(2, 8, 2, 64, 4, 16, TC) > 0
+    x = W.small_decode(58, 1, 8, 2, 96, [40])
     dd = DeviceDecode(x)
     ws = kv.alloc_workspace(1 << 20)
     with pytest.raises(kv.KVError) as e:

@@ -77,6 +77,23 @@ def test_attend_multi_small(T, dtype, G, lens, pps):
     _check(x, T, out, lse, ref_out, ref_lse)
 
 
+@pytest.mark.parametrize("T,dtype,G,lens", [
+    (4, W.F16, 4, [900, 3, 0, 2000]),           # 16 rows: one pass
+    (16, W.BF16, 4, [1500, 20, 700]),           # 64 rows: one pass, four row blocks
+    (20, W.F16, 4, [1200, 7, 300]),             # 80 rows: two passes of 10 tokens
+    (3, W.BF16, 8, [640, 2]),
+])
+def test_attend_multi_d64(T, dtype, G, lens):
+    """d = 64 on the tensor-core kernel (one 64-channel half per head row)."""
+    rng = np.random.default_rng(T * 7 + G)
+    Hkv = 4
+    x = W.small_decode(190 + T, len(lens), Hkv * G, Hkv, 64, lens, dtype=dtype, pad_pages=1)
+    qm = W.normal_bits(rng, (x.B, T, x.Hq, x.d), dtype)
+    out, lse = _run(x, qm, T)
+    ref_out, ref_lse = O.attend_multi(x, qm, nthreads=NCPU)
+    _check(x, T, out, lse, ref_out, ref_lse)
+
+
 def test_attend_multi_bimodal_t4():
     """Four query tokens per sequence on the batch-8 bimodal fp16 workload."""
     x = W.bimodal()
