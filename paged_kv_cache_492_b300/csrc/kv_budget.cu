@@ -1417,18 +1417,36 @@ __global__ void __launch_bounds__(kStepThreads, 1) budget_step_kernel(const Step
   if (tid == 0) s_last = atomicAdd(a.ticket, 1u) == (unsigned)(a.B - 1);
   __syncthreads();
   if (s_last) finisher = true;
+  if (finisher) break;  // every sequence has arrived: no item is left to take
   }  // items
-  // the last block to stop taking items puts the counters back to zero
-  if (tid == 0 && atomicAdd(a.exits, 1u) == gridDim.x - 1) {
-    *a.grab = 0;
-    *a.exits = 0;
+  // the last block to stop taking items (the finisher stops after its work)
+  // puts the counters back to zero
+  auto leave = [&]() {
+    if (tid == 0 && atomicAdd(a.exits, 1u) == gridDim.x - 1) {
+      *a.grab = 0;
+      *a.exits = 0;
+    }
+  };
+  if (!finisher) {
+    leave();
+    return;
   }
-  if (!finisher) return;
   __syncthreads();
   __threadfence();
   const int free_count = __ldcg(a.free_top);
   int* pend = reinterpret_cast<int*>(sel_sm);  // [B] rows to compact here, then offsets
   int* cnt_s = pend + a.B;                     // [B] pages freed per row
+  int* pg_pre = pend + 2 * a.B;                // [B] the token's page of rows needing none new
+  int* pops = pend + 3 * a.B;                  // [B] the free-list ids the appends pop
+  // A row whose length is not a page multiple was not at a boundary: it keeps
+  // its length and table, and its token goes to the page its length ends in.
+  // Loaded now, used by the append plan below.
+  for (int bb = tid; bb < a.B; bb += blockDim.x) {
+    const int Lo = a.seq_lens[bb];
+    pg_pre[bb] = Lo > 0 && Lo % a.ps != 0 && Lo / a.ps < a.max_pages
+                     ? __ldcg(a.table + (size_t)bb * a.max_pages + Lo / a.ps)
+                     : -1;
+  }
   // grants in ascending b while free pages last (as select_grant_kernel);
   // rows that wanted a page and got none are compacted here
   if (tid == 0) {
@@ -1539,15 +1557,16 @@ __global__ void __launch_bounds__(kStepThreads, 1) budget_step_kernel(const Step
       if (Lb / a.ps >= a.max_pages) s_carry[0] = 1;
       ++my_need;
     } else {
-      pg = __ldcg(a.table + (size_t)bb * a.max_pages + Lb / a.ps);
+      pg = pg_pre[bb];  // Lb is the row's unchanged length here
       if (pg < 0 || pg >= a.num_pages) s_carry[1] = 1;
     }
     dest[bb] = make_int2(pg, Lb);  // (page or -1 for a pop, length) until the pops are known
   }
   const int total = block_sum_int(my_need, red);
-  if (total <= top)
+  if (total <= top)  // at most one pop per sequence: total <= B
     for (int i = tid; i < total; i += blockDim.x) {
       const int p = __ldcg(a.free_list + (top - 1 - i));
+      pops[i] = p;
       if (p < 0 || p >= a.num_pages) s_carry[1] = 1;
     }
   __syncthreads();
@@ -1561,6 +1580,7 @@ __global__ void __launch_bounds__(kStepThreads, 1) budget_step_kernel(const Step
       *a.ctl = 1;
       *a.ticket = 0;
     }
+    leave();
     return;
   }
   for (int base = 0; base < a.B; base += blockDim.x) {
@@ -1579,7 +1599,7 @@ __global__ void __launch_bounds__(kStepThreads, 1) budget_step_kernel(const Step
     if (bb < a.B) {
       int pg = dl.x;
       if (nd) {
-        pg = __ldcg(a.free_list + (top - 1 - (carry + before + x)));
+        pg = pops[carry + before + x];
         a.table[(size_t)bb * a.max_pages + Lb / a.ps] = pg;
       }
       dest[bb] = make_int2(pg, Lb % a.ps);
@@ -1600,14 +1620,17 @@ __global__ void __launch_bounds__(kStepThreads, 1) budget_step_kernel(const Step
     *a.ctl = 0;
     *a.ticket = 0;  // ready for the next call
   }
+  leave();
 }
 
 // The step's token: K and V rows (all heads) of sequence blockIdx.x into the
 // (page, slot) the fused step planned (nothing when its append failed), and
 // the sequence's final length into seq_lens.
 __global__ void __launch_bounds__(128) step_copy_kernel(const StepArgs a) {
-  pdl_wait();  // launched early: the step kernel's plan must be complete
+  // the decode that follows may be scheduled now (it waits for this grid to
+  // finish before it reads anything); this kernel waits for the step's plan
   pdl_launch_dependents();
+  pdl_wait();
   const int b = blockIdx.x;
   if (threadIdx.x == 0) a.seq_lens[b] = a.new_len[b];
   if (*a.ctl) return;
@@ -1918,7 +1941,7 @@ static size_t step_smem(int B, int Hkv, int d, int max_pages) {
   while (p2 < (size_t)max_pages) p2 <<= 1;
   // packed keys, R, flags, ranks (two), unpacked keys above 1024 pages
   const size_t sel = (size_t)max_pages * (8 + 4 + 1 + 2 + 2 + 8) + p2 * 2 + 32;
-  return (size_t)2 * Hkv * d * 4 + std::max(align_up(sel, 16), (size_t)B * 8);
+  return (size_t)2 * Hkv * d * 4 + std::max(align_up(sel, 16), (size_t)B * 16);
 }
 
 size_t kv_budget_step_workspace_size(int B, int max_pages) { return step_layout(B, max_pages).total; }
