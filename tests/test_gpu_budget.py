@@ -651,6 +651,35 @@ def test_fused_step_many_sequences(B):
             assert int(fused.active.sum()) > B // 10  # many rows at a boundary
 
 
+def test_fused_step_tied_scores():
+    """Rows whose pages hold identical keys score every candidate alike, so
+    the selection's order comes from the page index alone (and half tied in
+    another row): the fused step's threshold selection against the separate
+    calls' ranks, bit for bit, over three steps."""
+    lens = [16 * 12, 16 * 9, 16 * 20, 16 * 7 + 5]
+    budget = np.array([12, 9, 20, 6], np.int32)
+    x = W.small_decode(94, len(lens), 8, 2, 128, lens, dtype=W.BF16, pool_factor=1.5, pad_pages=3)
+    for b, share in ((0, 1.0), (2, 0.5)):  # all / half of the row's pages copies of one page
+        row = x.block_table[b][: lens[b] // 16]
+        for p in row[: int(len(row) * share)]:
+            x.k_pool[p] = x.k_pool[row[0]]
+    cfg = BG.BudgetConfig(a_fast=0.9, a_slow=0.999, n_first=1, n_last=1, delta=0.3)
+    fused, calls = _pair(x, budget, cfg)
+    rng = np.random.default_rng(7)
+    for t in range(3):
+        q = bits_to_dev(W.normal_bits(rng, (x.B, x.Hq, 128), W.BF16), W.BF16)
+        kn = bits_to_dev(W.normal_bits(rng, (x.B, x.Hkv, 128), W.BF16), W.BF16)
+        vn = bits_to_dev(W.normal_bits(rng, (x.B, x.Hkv, 128), W.BF16), W.BF16)
+        for dec in (fused, calls):
+            if t == 0:
+                dec.update_summaries(q, True)
+            dec.step(q, kn, vn, t)
+        torch.cuda.synchronize()
+        _same(fused, calls, f"step {t}")
+        if t == 0:
+            assert int(fused.active.sum()) == 3
+
+
 def test_fused_step_append_failure():
     """A row whose last page is full but which is below its budget needs a
     page the free list does not have: both paths report KV_ENOSPACE and
