@@ -1,10 +1,12 @@
 """Benchmark: one paged GQA decode step (per-CTA workqueue + split-KV decode +
-LSE merge, by the engine a calibrated policy picks) on the batch-8 bimodal fp16 workload (Hq=32,
-Hkv=8, d=128, page 16, lengths half U[512, 2048] and half U[16384, 32768],
-pages scattered in a pool of 1.25x the pages used), measured as KV HBM GB/s
-and tokens/s.  The `budget_step` object times the whole budgeted step (query
-EMAs, page summaries, scoring, selection, compaction, append, decode) on the
-batch-64 bf16 workload with per-sequence page budgets.
+LSE merge, by the engine a calibrated policy picks) on the batch-8 bimodal
+fp16 workload (Hq=32, Hkv=8, d=128, page 16, lengths half U[512, 2048] and
+half U[16384, 32768], pages scattered in a pool of 1.25x the pages used),
+measured as KV HBM GB/s and tokens/s.  The `budget_step` object times the
+whole budgeted step (query EMAs, page summaries, scoring, selection,
+compaction, append, decode) on the batch-64 bf16 workload with per-sequence
+page budgets; `multi_token` and `multi_token_t32` time 4 and 32 query tokens
+per sequence.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
                     [--workload bimodal|uniform|zipf|bucket32k|bucket64k|bucket128k|tiny]
@@ -12,14 +14,15 @@ batch-64 bf16 workload with per-sequence page budgets.
 Prints one JSON line.  `value` is algorithmic bytes (valid K/V tokens + q +
 block-table entries) per step / device time per step, with inputs resident in
 HBM and L2 flushed between steps (a 512 MiB memset, then its first 256 MiB
-read back so the lines left in L2 are clean; both outside the timed events).  `e2e` times the host-buffer entry point (q, block table and
-lengths copied in, out and lse copied back, per step).  `roofline` reports
-the attention kernel alone (events bracket it inside the call) against the
-measured HBM copy bandwidth.  `cpu_baseline` times the CPU oracle on a
-bounded sample of the same workload.  With --impl reference the CPU oracle is
-the measured arm.  Under torchrun (N > 1) every rank runs an independent
-replica (the step does not shard), the max time over ranks is reported and
-`value` sums all ranks' bytes.
+read back so the lines left in L2 are clean; both outside the timed events).
+`e2e` times the host-buffer entry point (q, block table and lengths copied
+in, out and lse copied back, per step).  `roofline` reports the attention
+kernel alone (events bracket it inside the call) against the measured HBM
+copy bandwidth.  `cpu_baseline` times the CPU oracle on a bounded sample of
+the same workload.  With --impl reference the CPU oracle is the measured arm.
+Under torchrun (N > 1) every rank runs an independent replica (the step does
+not shard), the max time over ranks is reported and `value` sums all ranks'
+bytes.
 """
 from __future__ import annotations
 

@@ -53,7 +53,8 @@ cudaError_t launch_segs_copy(const CopySegs& c, cudaStream_t s) {
 // the half of the flush buffer that the preceding memset already pushed out
 // of L2): the lines it brings in are clean, so the dirty lines the memset
 // left behind are written back here rather than inside the next timed call.
-// The xor of what was read goes to *sink so the loads cannot be dropped.
+// A store to *sink depends on the xor of what was read, so the loads cannot
+// be dropped.
 __global__ void __launch_bounds__(256) l2_clean_kernel(const uint4* src, size_t n16, uint4* sink) {
   uint4 x = make_uint4(0u, 0u, 0u, 0u);
   for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < n16;
