@@ -166,7 +166,8 @@ int kv_decode(const void *q, const void *k_pool, const void *v_pool, int num_pag
  * 64 / G tokens per pass over the pages (T * G <= 64: one pass for all T
  * tokens; T = 1 is kv_decode's KV_DECODE_TENSOR_CORE engine); larger T runs
  * as ceil(T * G / 64) consecutive passes over chunks of at most 64 / G
- * tokens (as even as possible), so each page is streamed that many times. */
+ * tokens (ceil(T / passes) each, the last one taking the rest), so each page
+ * is streamed that many times. */
 size_t kv_attend_multi_workspace_size(int B, int T, int Hq, int Hkv, int d, int max_pages,
                                       int page_size, int pages_per_split);
 int kv_attend_multi(const void *q, const void *k_pool, const void *v_pool, int num_pages,

@@ -6,10 +6,11 @@
 //
 // The tensor-core kernel (kv_mma.cu, d = 64 or 128, page size 16) takes up
 // to 64 rows per KV head (T * G) in one pass over the pages.  More query
-// tokens are served in ceil(T * G / 64) passes over chunks of at most 64 / G
-// tokens, as even as possible: chunk [t0, t0 + Tc) sees L_b - (T - t0 - Tc)
-// cached tokens, and the usual causal rule within the chunk then gives every
-// token its own limit.  Each page is streamed once per pass.
+// tokens are served in the fewest passes that fit, P = ceil(T * G / 64), over
+// chunks of ceil(T / P) tokens (the last one takes the rest): chunk
+// [t0, t0 + Tc) sees L_b - (T - t0 - Tc) cached tokens, and the usual causal
+// rule within the chunk then gives every token its own limit.  Each page is
+// streamed once per pass.
 #include "kv_internal.h"
 
 namespace kvb {
@@ -50,7 +51,7 @@ int kv_attend_multi(const void* q, const void* k_pool, const void* v_pool, int n
   const int tc = mma_chunk_tokens(page_size, Hq, Hkv, d, T);
   if (!tc) return KV_EINVAL;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  // the fewest passes of at most tc tokens, as even as possible (a pass's
+  // the fewest passes of at most tc tokens, ceil(T / passes) each (a pass's
   // time grows with its rows), in order on the stream (one workspace)
   const int passes = (T + tc - 1) / tc, per = (T + passes - 1) / passes;
   const size_t qrow = (size_t)Hq * d * 2;  // bytes of one query token's heads

@@ -41,7 +41,7 @@ def _check(x, T, out, lse, ref_out, ref_lse):
 
 
 # d = 128 runs on the tensor-core kernel (one consumer warp per 16 rows), in
-# the fewest even passes of at most 64 / G tokens where T * G > 64.
+# the fewest passes of at most 64 / G tokens where T * G > 64.
 @pytest.mark.parametrize("T,dtype,G,lens,pps", [
     (4, W.F16, 4, [3000, 17, 0, 2, 900], 0),
     (4, W.BF16, 4, [2500, 3, 0, 16, 48, 4100], 0),
