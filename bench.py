@@ -625,17 +625,37 @@ def measure_multi(x, dev, peak, T=4, steps=10):
         raise SystemExit("device error in kv_attend_multi")
     t = statistics.median(ms) / 1e3
     algo = x.kv_bytes() + x.B * T * x.Hq * x.d * 2 + 4 * sum(-(-int(L) // 16) for L in x.seq_lens)
-    most = max(1, 64 // (x.Hq // x.Hkv)) if x.d == 128 else 1
-    per_pass = -(-T // -(-T // most))  # the library's even split into the fewest passes
-    streamed, passes = 0, 0
-    for t0 in range(0, T, per_pass):
-        shift = T - t0 - min(per_pass, T - t0)
+    plan = multi_pass_plan(T, x.Hq // x.Hkv)
+    streamed, t0 = 0, 0
+    for n in plan:
+        shift = T - t0 - n
         streamed += int(np.maximum(x.seq_lens.astype(np.int64) - shift, 0).sum()) * 2 * x.Hkv * x.d * 2
-        passes += 1
+        t0 += n
+    passes = len(plan)
     return {"T": T, "ms_per_step": t * 1e3, "tokens_per_s": x.B * T / t,
             "algorithmic_gbs": algo / t / 1e9, "algorithmic_frac_of_peak": algo / t / 1e9 / peak,
             "streamed_gbs": streamed / t / 1e9, "passes": passes,
-            "note": f"tensor-core engine: up to {per_pass} query tokens per pass over the pages"}
+            "pass_tokens": plan,
+            "note": "tensor-core engine: passes of at most 64 rows per KV head over the pages"}
+
+
+def multi_pass_plan(T, G):
+    """Query tokens per pass of kv_attend_multi (the library's rule): the
+    fewest passes of at most 64 rows per KV head; where G divides 16 the
+    ceil(T * G / 16) row blocks are dealt out evenly (larger shares first, the
+    last pass taking the remaining tokens), otherwise full passes and the rest
+    last."""
+    most = max(1, 64 // G)
+    passes = -(-T // most)
+    tpb = 16 // G if 16 % G == 0 else 0
+    blocks = -(-T // tpb) if tpb else 0
+    plan, t0 = [], 0
+    for p in range(passes):
+        n = (blocks // passes + (1 if p < blocks % passes else 0)) * tpb if tpb else most
+        n = min(n, T - t0)
+        plan.append(n)
+        t0 += n
+    return plan
 
 
 def kernel_hash(engine="fused"):

@@ -166,8 +166,9 @@ int kv_decode(const void *q, const void *k_pool, const void *v_pool, int num_pag
  * 64 / G tokens per pass over the pages (T * G <= 64: one pass for all T
  * tokens; T = 1 is kv_decode's KV_DECODE_TENSOR_CORE engine); larger T runs
  * as ceil(T * G / 64) consecutive passes over chunks of at most 64 / G
- * tokens (ceil(T / passes) each, the last one taking the rest), so each page
- * is streamed that many times. */
+ * tokens, so each page is streamed that many times.  The chunks use as few
+ * 16-row blocks as the T tokens need, spread evenly over the passes (where G
+ * divides 16; otherwise every pass but the last is full). */
 size_t kv_attend_multi_workspace_size(int B, int T, int Hq, int Hkv, int d, int max_pages,
                                       int page_size, int pages_per_split);
 int kv_attend_multi(const void *q, const void *k_pool, const void *v_pool, int num_pages,

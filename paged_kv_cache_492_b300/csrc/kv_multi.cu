@@ -6,11 +6,14 @@
 //
 // The tensor-core kernel (kv_mma.cu, d = 64 or 128, page size 16) takes up
 // to 64 rows per KV head (T * G) in one pass over the pages.  More query
-// tokens are served in the fewest passes that fit, P = ceil(T * G / 64), over
-// chunks of ceil(T / P) tokens (the last one takes the rest): chunk
-// [t0, t0 + Tc) sees L_b - (T - t0 - Tc) cached tokens, and the usual causal
-// rule within the chunk then gives every token its own limit.  Each page is
-// streamed once per pass.
+// tokens are served in the fewest passes that fit: chunk [t0, t0 + Tc) sees
+// L_b - (T - t0 - Tc) cached tokens, and the usual causal rule within the
+// chunk then gives every token its own limit.  Each page is streamed once per
+// pass.  A pass's time grows with its 16-row blocks (one consumer warp each),
+// so the chunks use as few blocks as the T tokens need, spread evenly: where
+// G divides 16, the ceil(T * G / 16) blocks are dealt out over the passes
+// (larger shares first, the last pass taking the remaining tokens); otherwise
+// every pass but the last is full.
 #include "kv_internal.h"
 
 namespace kvb {
@@ -51,18 +54,23 @@ int kv_attend_multi(const void* q, const void* k_pool, const void* v_pool, int n
   const int tc = mma_chunk_tokens(page_size, Hq, Hkv, d, T);
   if (!tc) return KV_EINVAL;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  // the fewest passes of at most tc tokens, ceil(T / passes) each (a pass's
-  // time grows with its rows), in order on the stream (one workspace)
-  const int passes = (T + tc - 1) / tc, per = (T + passes - 1) / passes;
+  // the fewest passes of at most tc tokens, in order on the stream (one
+  // workspace); tokens per pass from the row-block plan above
+  const int G = Hq / Hkv, passes = (T + tc - 1) / tc;
+  const int tpb = 16 % G == 0 ? 16 / G : 0;  // tokens per 16-row block
+  const int blocks = tpb ? (T + tpb - 1) / tpb : 0;
   const size_t qrow = (size_t)Hq * d * 2;  // bytes of one query token's heads
-  for (int t0 = 0; t0 < T; t0 += per) {
-    const int n = T - t0 < per ? T - t0 : per;
+  int t0 = 0;
+  for (int pass = 0; pass < passes; ++pass) {
+    int n = tpb ? (blocks / passes + (pass < blocks % passes ? 1 : 0)) * tpb : tc;
+    if (n > T - t0) n = T - t0;
     const int rc = mma_attend_launch(
         q ? static_cast<const uint8_t*>(q) + (size_t)t0 * qrow : nullptr, k_pool, v_pool,
         num_pages, block_table, max_pages, seq_lens, B, n, T, T - t0 - n, Hq, Hkv, d, dtype,
         scale, pages_per_split, out ? out + (size_t)t0 * Hq * d : nullptr,
         lse ? lse + (size_t)t0 * Hq : nullptr, ws, ws_bytes, kHeaderBytes, s);
     if (rc) return rc;
+    t0 += n;
   }
   return KV_OK;
 }

@@ -59,9 +59,9 @@ def _check(x, T, out, lse, ref_out, ref_lse):
     (12, W.BF16, 2, [64, 2000], 0),             # 24 rows
     (12, W.F16, 4, [900, 11, 2600], 0),         # 48 rows: three row blocks
     (16, W.F16, 8, [1200, 20], 0),              # 128 rows: two passes of 8 tokens
-    (20, W.F16, 4, [1500, 7, 0, 300], 0),       # 80 rows: passes of 10 + 10 tokens
-    (33, W.BF16, 2, [900, 40, 2, 33], 0),       # 66 rows: 17 + 16 tokens; L < T rows
-    (70, W.F16, 1, [500, 69, 71, 64], 0),       # G = 1: 35 + 35 tokens
+    (20, W.F16, 4, [1500, 7, 0, 300], 0),       # 80 rows: passes of 12 + 8 tokens
+    (33, W.BF16, 2, [900, 40, 2, 33], 0),       # 66 rows: 24 + 9 tokens; L < T rows
+    (70, W.F16, 1, [500, 69, 71, 64], 0),       # G = 1: 48 + 22 tokens
     (24, W.BF16, 8, [2000, 10, 25], 3),         # 192 rows: three passes, fixed splits
     (40, W.F16, 4, [4000, 1, 39, 41], 1),       # 160 rows, one-page splits
     (1, W.F16, 4, [20000, 40, 0], 1),           # 1250 one-page splits: groups of 36
@@ -80,7 +80,7 @@ def test_attend_multi_small(T, dtype, G, lens, pps):
 @pytest.mark.parametrize("T,dtype,G,lens", [
     (4, W.F16, 4, [900, 3, 0, 2000]),           # 16 rows: one pass
     (16, W.BF16, 4, [1500, 20, 700]),           # 64 rows: one pass, four row blocks
-    (20, W.F16, 4, [1200, 7, 300]),             # 80 rows: two passes of 10 tokens
+    (20, W.F16, 4, [1200, 7, 300]),             # 80 rows: passes of 12 + 8 tokens
     (3, W.BF16, 8, [640, 2]),
 ])
 def test_attend_multi_d64(T, dtype, G, lens):
@@ -130,7 +130,7 @@ def _rows_of(x, rows):
 def test_attend_multi_large_batch_passes():
     """Above 1024 sequences the page offsets come from a separate pass, which
     takes each pass's shortened lengths: 1100 sequences, T = 20 (80 rows per
-    KV head: two passes of 10 tokens), lengths from 0 to 60 (many below T)."""
+    KV head: passes of 12 + 8 tokens), lengths from 0 to 60 (many below T)."""
     rng = np.random.default_rng(61)
     lens = rng.integers(0, 61, size=1100).astype(np.int32)
     x = W.small_decode(61, 1100, 32, 8, 128, lens.tolist(), dtype=W.F16)

@@ -9,32 +9,37 @@ the oracle's per-row arithmetic is identical and the rows agree bit for bit."""
 import numpy as np
 import pytest
 
+import bench
 from oracle import oracle as O
 from paged_kv_cache_492_b300 import workloads as W
 
 
-def _passes(T, most):
-    passes = -(-T // most)
-    per = -(-T // passes)
-    return [(t0, min(per, T - t0)) for t0 in range(0, T, per)]
+def _passes(T, G):
+    plan, t0 = [], 0
+    for n in bench.multi_pass_plan(T, G):
+        plan.append((t0, n))
+        t0 += n
+    return plan
 
 
-@pytest.mark.parametrize("T,G,lens,most", [
-    (20, 4, [0, 3, 19, 20, 21, 100], 16),    # passes of 10 + 10 tokens; L < T rows
-    (33, 2, [1, 32, 33, 34, 250], 32),       # 17 + 16
-    (9, 8, [5, 8, 9, 64], 8),                # 5 + 4
-    (40, 4, [39, 40, 41, 300], 16),          # 14 + 14 + 12
+@pytest.mark.parametrize("T,G,lens,most,plan", [
+    (20, 4, [0, 3, 19, 20, 21, 100], 16, [12, 8]),    # 3 + 2 row blocks; L < T rows
+    (17, 4, [1, 16, 17, 18, 90], 16, [12, 5]),
+    (33, 2, [1, 32, 33, 34, 250], 32, [24, 9]),
+    (9, 8, [5, 8, 9, 64], 8, [6, 3]),
+    (40, 4, [39, 40, 41, 300], 16, [16, 12, 12]),
+    (7, 12, [3, 6, 7, 50], 5, [5, 2]),                # G does not divide 16: full passes
 ])
-def test_passes_reproduce_the_one_pass_rows(T, G, lens, most):
+def test_passes_reproduce_the_one_pass_rows(T, G, lens, most, plan):
     Hkv = 2
     x = W.small_decode(400 + T, len(lens), Hkv * G, Hkv, 64, lens, dtype=W.F16)
     rng = np.random.default_rng(T)
     qm = W.normal_bits(rng, (x.B, T, x.Hq, x.d), x.dtype)
     full_o, full_l = O.attend_multi(x, qm)
-    plan = _passes(T, most)
-    assert len(plan) == -(-T // most) and sum(n for _, n in plan) == T
-    assert all(n <= most for _, n in plan)
-    for t0, n in plan:
+    passes = _passes(T, G)
+    assert [n for _, n in passes] == plan
+    assert len(passes) == -(-T // most) and all(n <= most for _, n in passes)
+    for t0, n in passes:
         shift = T - t0 - n
         y = W.DecodeInputs(**{**x.__dict__,
                               "seq_lens": np.maximum(x.seq_lens - shift, 0).astype(np.int32)})
